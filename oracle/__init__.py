@@ -1,0 +1,143 @@
+"""float64 CPU oracle for row-wise softmax and fused softmax+TopK.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product library never loads it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C99, IEEE double, host libm
+``exp``); this module compiles it with gcc on first use and wraps it with
+ctypes/numpy.  Inputs of any real dtype are widened to float64 exactly
+(bf16 and fp32 values are exact in double) before the C code sees them.
+
+Functions and the passages they follow are listed in ``oracle.c``'s header:
+``softmax`` (three-pass safe softmax), ``row_stats`` ((m, d) by definition),
+``online_stats`` (the single-pass recurrence), ``combine`` (the binary
+operator on (m, d) with identity (-inf, 0)) and ``topk`` (full sort by
+logit descending, index ascending; v = e^(u - m)/d).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dbl_p = ctypes.POINTER(ctypes.c_double)
+_i32_p = ctypes.POINTER(ctypes.c_int32)
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB_PATH, defines: tuple = ()) -> str:
+    """Compile ``src`` into a shared library at ``out`` with gcc (OpenMP on)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-fopenmp",
+           *[f"-D{d}" for d in defines], src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Build the oracle library if it is missing or older than its source."""
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        compile_oracle()
+    return _LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the oracle library (or another build of the same source at ``path``)."""
+    lib = ctypes.CDLL(path or build())
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_row_stats_f64.argtypes = [_dbl_p, _dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64]
+    lib.oracle_softmax_f64.argtypes = [_dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64]
+    lib.oracle_online_stats_f64.argtypes = [_dbl_p, ctypes.c_int64, _dbl_p, _dbl_p]
+    lib.oracle_combine_f64.argtypes = [ctypes.c_double] * 4 + [_dbl_p, _dbl_p]
+    lib.oracle_topk_f64.argtypes = [_dbl_p, _dbl_p, _i32_p, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_int32]
+    lib.oracle_topk_f64.restype = ctypes.c_int
+    return lib
+
+
+def _get() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load()
+    return _lib
+
+
+def _as_rows(x) -> np.ndarray:
+    """Widen to a C-contiguous float64 matrix (exact for fp32 and bf16 data)."""
+    if hasattr(x, "detach"):  # a torch tensor: widen on its device-independent CPU copy
+        x = x.detach().to("cpu").double().numpy()
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    if a.ndim == 1:
+        a = a[None, :]
+    if a.ndim != 2:
+        raise ValueError("oracle inputs are rows: a 1-D or 2-D array")
+    return a
+
+
+def _p(a: np.ndarray, t=_dbl_p):
+    return a.ctypes.data_as(t)
+
+
+def num_threads(lib: ctypes.CDLL | None = None) -> int:
+    return (lib or _get()).oracle_num_threads()
+
+
+def softmax(x, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """float64 softmax of each row of ``x`` (three-pass safe softmax)."""
+    a = _as_rows(x)
+    y = np.empty_like(a)
+    (lib or _get()).oracle_softmax_f64(_p(a), _p(y), a.shape[0], a.shape[1])
+    return y
+
+
+def row_stats(x, lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row (m, d): the row maximum and sum_j e^(x_j - m)."""
+    a = _as_rows(x)
+    m = np.empty(a.shape[0])
+    d = np.empty(a.shape[0])
+    (lib or _get()).oracle_row_stats_f64(_p(a), _p(m), _p(d), a.shape[0], a.shape[1])
+    return m, d
+
+
+def online_stats(x, lib: ctypes.CDLL | None = None) -> tuple[float, float]:
+    """(m, d) of a 1-D sequence by the element-by-element recurrence."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64).ravel())
+    m = ctypes.c_double()
+    d = ctypes.c_double()
+    (lib or _get()).oracle_online_stats_f64(_p(a), a.size, ctypes.byref(m), ctypes.byref(d))
+    return m.value, d.value
+
+
+def combine(s1, s2, lib: ctypes.CDLL | None = None) -> tuple[float, float]:
+    """(m1, d1) (+) (m2, d2)."""
+    m = ctypes.c_double()
+    d = ctypes.c_double()
+    (lib or _get()).oracle_combine_f64(float(s1[0]), float(s1[1]), float(s2[0]), float(s2[1]),
+                                       ctypes.byref(m), ctypes.byref(d))
+    return m.value, d.value
+
+
+def topk(x, K: int, lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """Top-K (probability float64, index int32) of each row, best first."""
+    a = _as_rows(x)
+    rows, cols = a.shape
+    vals = np.empty((rows, K))
+    idx = np.empty((rows, K), dtype=np.int32)
+    rc = (lib or _get()).oracle_topk_f64(_p(a), _p(vals), _p(idx, _i32_p), rows, cols, K)
+    if rc != 0:
+        raise ValueError(f"oracle topk rejected K={K} for {cols} columns")
+    return vals, idx

@@ -1,0 +1,53 @@
+"""Plausible mistakes planted in copies of the oracle must each fail a pin.
+
+Every mutant is the oracle's C source with one textual change, compiled on
+the CPU into a temporary directory.  The pins of test_oracle_pins.py run on
+each mutant; the test passes only if at least one pin rejects it.  This shows
+the pins would notice a dropped term, a wrong sign or index, a swapped
+operand, a wrong initial state, the wrong-order update that the Lesson 7 page
+warns about (section 3), or a reversed tie rule.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests.test_oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "sum_without_max_shift": ("d += exp(x[j] - m);", "d += exp(x[j]);"),
+    "combine_wrong_sign": ("d1 * exp(m1 - m)", "d1 * exp(m - m1)"),
+    "combine_drops_second_term": ("d1 * exp(m1 - m) + d2 * exp(m2 - m)", "d1 * exp(m1 - m)"),
+    "combine_swapped_operands": ("d2 * exp(m2 - m)", "d2 * exp(m1 - m)"),
+    "recurrence_overwrites_max_first": (
+        "d = d * exp(m - m_new) + exp(x[j] - m_new);\n        m = m_new;",
+        "m = m_new;\n        d = d * exp(m - m_new) + exp(x[j] - m_new);"),
+    "max_starts_at_zero": ("double m = -INFINITY;\n    for", "double m = 0.0;\n    for"),
+    "output_divides_by_max": ("yr[j] = exp(xr[j] - m) / d;", "yr[j] = exp(xr[j] - m) / (d + m * 0.0 + 1e-3);"),
+    "topk_ties_to_higher_index": ("return (a->j > b->j) - (a->j < b->j);",
+                                  "return (a->j < b->j) - (a->j > b->j);"),
+    "topk_value_transposed": ("vals[r * K + k] = exp(order[k].x - m) / d;",
+                              "vals[r * K + k] = exp(m - order[k].x) / d;"),
+    "topk_ascending": ("if (a->x > b->x) return -1;\n    if (a->x < b->x) return 1;",
+                       "if (a->x < b->x) return -1;\n    if (a->x > b->x) return 1;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    before, after = MUTANTS[name]
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(before) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / "oracle_mutant.c"
+    src.write_text(text.replace(before, after))
+    lib = oracle.load(oracle.compile_oracle(str(src), str(tmp_path / "liboracle_mutant.so")))
+    failures = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failures.append(pin.__name__)
+    assert failures, f"no pin rejects the mutant {name}"

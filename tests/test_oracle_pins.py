@@ -1,0 +1,254 @@
+"""Pins of the float64 oracle to facts fixed outside the oracle itself.
+
+Each ``pin_*`` function checks one such fact against an oracle library handle
+and raises AssertionError when it does not hold.  The tests below run every pin
+on the real oracle; tests/test_oracle_mutants.py runs the same pins on
+deliberately broken copies of the oracle and requires each copy to fail one.
+
+Sources of the facts (pages named by title and section):
+  * Lesson 7 "Online Softmax and associative state", worked two-shard example
+    and the NumPy chunked-simulation check (tests/golden/).
+  * The same page, section 3: identity element (-inf, 0).
+  * "Online normalizer calculation for softmax" notes, section 3.2: the
+    recurrence's d equals sum_j e^(x_j - m) (induction proof) and
+    1 <= d_j <= j; section 3.3: the operator is associative and commutative;
+    section 4: top-K of y equals top-K of the logits (softmax is monotone).
+  * "CUDA operator optimization (3): Softmax", subtract-max trick: softmax is
+    invariant under adding a constant to every entry.
+  * Closed forms: one entry -> 1; constant row -> 1/n; two entries -> the
+    logistic function of their difference; y_i = 1 / sum_j e^(x_j - x_i).
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import _golden
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def _lib():
+    return oracle.load()
+
+
+# ---------------------------------------------------------------- (m, d) state
+def pin_two_shard_example(lib):
+    g = _golden.load("two_shard_example.txt")
+    step = 10.0 ** -int(g["printed_decimals"])
+
+    def shown(value, printed):  # the page truncates after the last printed decimal
+        return 0.0 <= value - printed < step
+
+    ma, da = (v[0] for v in oracle.row_stats(g["shard_a"], lib))
+    mb, db = (v[0] for v in oracle.row_stats([g["shard_b"]], lib))
+    assert ma == g["m_a"] and shown(da, g["d_a"]), (ma, da)
+    assert mb == g["m_b"] and shown(db, g["d_b"]), (mb, db)
+    m, d = oracle.combine((ma, da), (mb, db), lib)
+    assert m == g["m_ab"] and shown(d, g["d_ab"]), (m, d)
+    mw, dw = (v[0] for v in oracle.row_stats(g["shard_a"] + [g["shard_b"]], lib))
+    assert mw == g["m_ab"] and shown(dw, g["d_three_pass"]), (mw, dw)
+    e2 = oracle.row_stats([[1.0, 3.0]], lib)[1][0] - 1.0    # e^(1-3)
+    e1 = oracle.row_stats([[2.0, 3.0]], lib)[1][0] - 1.0    # e^(2-3)
+    assert shown(e2, g["exp_minus_2"]) and shown(e1, g["exp_minus_1"]), (e2, e1)
+    # the merged state is the whole-row state, not just close to the printed value
+    assert abs(d - dw) <= 1e-15 * dw
+    assert abs(dw - (math.exp(-2) + math.exp(-1) + 1.0)) <= 1e-15
+
+
+def pin_identity_element(lib):
+    rng = np.random.default_rng(11)
+    for _ in range(50):
+        s = (float(rng.normal() * 30), float(rng.uniform(1, 1e4)))
+        assert oracle.combine(s, (-math.inf, 0.0), lib) == s
+        assert oracle.combine((-math.inf, 0.0), s, lib) == s
+    assert oracle.combine((-math.inf, 0.0), (-math.inf, 0.0), lib) == (-math.inf, 0.0)
+
+
+def pin_combine_associative_commutative(lib):
+    rng = np.random.default_rng(12)
+    for _ in range(40):
+        n = int(rng.integers(3, 40))
+        x = rng.normal(size=n) * rng.choice([1.0, 10.0, 60.0])
+        whole = tuple(v[0] for v in oracle.row_stats(x, lib))
+        a, b = sorted(rng.choice(np.arange(1, n), 2, replace=False))
+        parts = [tuple(v[0] for v in oracle.row_stats(p, lib)) for p in (x[:a], x[a:b], x[b:])]
+        left = oracle.combine(oracle.combine(parts[0], parts[1], lib), parts[2], lib)
+        right = oracle.combine(parts[0], oracle.combine(parts[1], parts[2], lib), lib)
+        swapped = oracle.combine(parts[2], oracle.combine(parts[1], parts[0], lib), lib)
+        for s in (left, right, swapped):
+            assert s[0] == whole[0]
+            assert abs(s[1] - whole[1]) <= 1e-12 * whole[1], (s, whole)
+
+
+def pin_online_recurrence_equals_definition(lib):
+    rng = np.random.default_rng(13)
+    rows = [rng.normal(size=n) * s for n in (1, 2, 7, 64, 1000) for s in (1.0, 25.0)]
+    rows.append(np.arange(200, dtype=float))           # new maximum at every step
+    rows.append(np.arange(200, dtype=float)[::-1])     # maximum first
+    rows.append(np.array([-np.inf, -np.inf, 3.0, -np.inf, 1.0]))  # leading -inf
+    for x in rows:
+        m, d = oracle.online_stats(x, lib)
+        md, dd = (v[0] for v in oracle.row_stats(x, lib))
+        assert m == md and abs(d - dd) <= 1e-12 * dd, (len(x), m, d, md, dd)
+
+
+def pin_normalizer_bound(lib):
+    rng = np.random.default_rng(14)
+    for n in (1, 5, 100, 4096):
+        x = rng.normal(size=(8, n)) * 5
+        x[:, ::7] = -np.inf
+        x[:, 0] = rng.normal(size=8)      # keep one finite entry per row
+        finite = np.isfinite(x).sum(axis=1)
+        _, d = oracle.row_stats(x, lib)
+        assert np.all(d >= 1.0) and np.all(d <= finite), (d, finite)
+
+
+# ---------------------------------------------------------------- softmax
+def pin_lesson7_numpy_check(lib):
+    g = _golden.load("lesson7_numpy_check.txt")
+    x = np.array(g["input_f32"], dtype=np.float32).astype(np.float64)
+    y = oracle.softmax(x, lib)[0]
+    # exactly rounded reference: y_i = 1 / sum_j e^(x_j - x_i), no shift by the max
+    ref = np.array([1.0 / math.fsum(math.exp(xj - xi) for xj in x) for xi in x])
+    assert np.allclose(y, ref, atol=g["atol"], rtol=0)
+    assert abs(math.fsum(y) - 1.0) <= g["sum_atol"]
+    assert np.all(np.abs(y - ref) <= 1e-15 * ref)
+    # the entry below FLT_MIN stays below it; the one just above FLT_MIN does too
+    assert y[5] < np.finfo(np.float32).tiny <= y[0]
+
+
+def pin_closed_forms(lib):
+    assert oracle.softmax([[3.25]], lib)[0, 0] == 1.0
+    for n in (1, 3, 17, 1000):
+        y = oracle.softmax(np.full((1, n), -2.5), lib)[0]
+        assert np.all(np.abs(y - 1.0 / n) <= 1e-15 / n)
+    rng = np.random.default_rng(15)
+    for a, b in rng.normal(size=(50, 2)) * 10:
+        y = oracle.softmax([[a, b]], lib)[0]
+        assert abs(y[0] - 1.0 / (1.0 + math.exp(b - a))) <= 1e-15
+        assert abs(y[1] - 1.0 / (1.0 + math.exp(a - b))) <= 1e-15
+
+
+def pin_shift_invariance(lib):
+    rng = np.random.default_rng(16)
+    # dyadic entries and power-of-two shifts: x + c is exact, so the output must be bit-identical
+    x = np.round(rng.normal(size=(6, 33)) * 64) / 64
+    y = oracle.softmax(x, lib)
+    for c in (1.0, -8.0, 1024.0, 2.0 ** 20):
+        assert np.array_equal(oracle.softmax(x + c, lib), y)
+
+
+def pin_brute_force_tiny_rows(lib):
+    rng = np.random.default_rng(17)
+    for n in range(1, 9):
+        for _ in range(10):
+            x = rng.normal(size=n) * rng.choice([0.5, 5.0, 40.0])
+            if n > 2:
+                x[rng.integers(n)] = -np.inf
+                x[rng.integers(n)] = x.max() if np.isfinite(x.max()) else 0.0
+            y = oracle.softmax(x, lib)[0]
+            for i in range(n):
+                if x[i] == -np.inf:
+                    assert y[i] == 0.0
+                    continue
+                ref = 1.0 / math.fsum(math.exp(xj - x[i]) for xj in x if xj != -np.inf)
+                assert abs(y[i] - ref) <= 1e-14 * ref, (x, i, y[i], ref)
+            assert abs(math.fsum(y) - 1.0) <= 1e-14
+
+
+def pin_rows_sum_to_one(lib):
+    rng = np.random.default_rng(18)
+    x = rng.normal(size=(20, 5000)) * 8
+    x[rng.random(x.shape) < 0.05] = -np.inf
+    x[:, 17] = 1.0
+    y = oracle.softmax(x, lib)
+    for row in y:
+        assert abs(math.fsum(row) - 1.0) <= 1e-12
+
+
+def pin_causal_and_spike_rows(lib):
+    rng = np.random.default_rng(19)
+    n = 128
+    x = rng.normal(size=(n, n))
+    x[np.arange(n)[None, :] > np.arange(n)[:, None]] = -np.inf
+    y = oracle.softmax(x, lib)
+    assert y[0, 0] == 1.0 and np.all(y[0, 1:] == 0.0)
+    assert np.all(y[np.arange(n)[None, :] > np.arange(n)[:, None]] == 0.0)
+    # four exact +40 ties: each spike is 1 / (4 + sum of the rest scaled by e^(x - 40))
+    x = rng.normal(size=300) * 3
+    spikes = [5, 90, 170, 299]
+    x[spikes] = 40.0
+    y = oracle.softmax(x, lib)[0]
+    rest = math.fsum(math.exp(v - 40.0) for i, v in enumerate(x) if i not in spikes)
+    for s in spikes:
+        assert abs(y[s] - 1.0 / (4.0 + rest)) <= 1e-15
+    assert len(set(y[spikes])) == 1
+
+
+# ---------------------------------------------------------------- TopK
+def _exhaustive_topk(x, K):
+    """Pick the best remaining entry K times: larger logit, then lower index."""
+    taken, out = set(), []
+    for _ in range(K):
+        best = None
+        for j, v in enumerate(x):
+            if j in taken:
+                continue
+            if best is None or v > x[best]:
+                best = j
+        taken.add(best)
+        out.append(best)
+    return out
+
+
+def pin_topk_exhaustive(lib):
+    rng = np.random.default_rng(20)
+    for n in (1, 2, 5, 9, 33, 70):
+        for _ in range(6):
+            x = np.round(rng.normal(size=n) * 3, 1)        # coarse values: many ties
+            if n > 3:
+                x[rng.integers(n, size=2)] = -np.inf
+            for K in sorted({1, min(n, 3), min(n, 8), n}):
+                vals, idx = oracle.topk(x, K, lib)
+                assert list(idx[0]) == _exhaustive_topk(list(x), K), (x, K, idx)
+                y = oracle.softmax(x, lib)[0]
+                assert np.array_equal(vals[0], y[idx[0]])
+
+
+def pin_topk_ties_lower_index(lib):
+    x = np.array([[0.5, 2.0, 2.0, -1.0, 2.0, 2.0, 0.5, -np.inf, -np.inf]])
+    vals, idx = oracle.topk(x, 9, lib)
+    assert list(idx[0]) == [1, 2, 4, 5, 0, 6, 3, 7, 8]
+    assert vals[0, 0] == vals[0, 3] and vals[0, 7] == 0.0 and vals[0, 8] == 0.0
+
+
+PINS = [pin_two_shard_example, pin_identity_element, pin_combine_associative_commutative,
+        pin_online_recurrence_equals_definition, pin_normalizer_bound, pin_lesson7_numpy_check,
+        pin_closed_forms, pin_shift_invariance, pin_brute_force_tiny_rows, pin_rows_sum_to_one,
+        pin_causal_and_spike_rows, pin_topk_exhaustive, pin_topk_ties_lower_index]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin):
+    pin(_lib())
+
+
+def test_oracle_topk_rejects_bad_k():
+    with pytest.raises(ValueError):
+        oracle.topk(np.zeros((1, 4)), 5)
+    with pytest.raises(ValueError):
+        oracle.topk(np.zeros((1, 4)), 0)
+
+
+def test_oracle_threads_reported():
+    assert oracle.num_threads() >= 1
+
+
+def test_exhaustive_helper_itself():
+    # the helper is tested on a case small enough to check by hand
+    assert _exhaustive_topk([1.0, 3.0, 3.0, 2.0], 4) == [1, 2, 3, 0]
+    for perm in itertools.permutations([0.0, 1.0, 2.0]):
+        assert _exhaustive_topk(list(perm), 1) == [perm.index(2.0)]
