@@ -1,0 +1,486 @@
+"""Benchmark: achieved HBM GB/s and rows/s of the online softmax and fused TopK.
+
+One step = one pass of the hot path over one batch of each headline workload:
+  * softmax 4096 x 32000 fp32 -> fp32
+  * softmax 8192 x 128256 bf16 -> bf16 (4 spikes at +40 per row, 1% -inf)
+  * fused softmax+TopK 256 x 50257 fp32, K = 8 and K = 64
+`value` is the step's compulsory HBM bytes (softmax: one read of x and one
+write of y; TopK: one read of x plus K*8 bytes of output) divided by the
+device time of the step, summed over all ranks' work, over the max rank time.
+
+Timing: CUDA events on the launching stream, W untimed warm-up steps, then K
+timed steps between barriers and synchronisations.  The softmax inputs are
+larger than L2; the TopK input (51 MB) rotates over enough copies to cover
+three times the L2 size, so no timed launch reads a cache-resident input.
+
+Also printed: `e2e` (the same metric through the public API with pinned host
+buffers: host->device copy of every input and device->host copy of every
+output inside the timed region), `roofline` of the dominant kernel,
+`cpu_baseline` (the float64 oracle on the host cores on a bounded sample),
+`clocks` (nvidia-smi samples taken during the timed region).
+
+`--impl reference` times the oracle alone (the reference arm of this build:
+the method's own definition run on the host cores), on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+SOFTMAX_STEP = ["softmax_4096x32000_f32", "softmax_8192x128256_bf16"]
+TOPK_NAME = "topk_256x50257_f32"
+TOPK_KS = (8, 64)
+EXTRA = ["softmax_64x1024_f32", "causal_1048576x128_f32", "increasing_65536x4096_f32"]
+METRIC = ("achieved HBM GB/s (compulsory bytes) of one step: softmax 4096x32000 fp32 + "
+          "softmax 8192x128256 bf16 + fused softmax+TopK 256x50257 fp32 K=8 and K=64")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ bytes
+def softmax_bytes(w) -> int:
+    b = 4 if w.dtype == "f32" else 2
+    return w.rows * w.cols * 2 * b
+
+
+def topk_bytes(w, K) -> int:
+    return w.rows * w.cols * 4 + w.rows * K * 8
+
+
+def step_units():
+    """(label, bytes, rows) of every launch in one step."""
+    out = []
+    for n in SOFTMAX_STEP:
+        w = workloads.WORKLOADS[n]
+        out.append((n, softmax_bytes(w), w.rows))
+    w = workloads.WORKLOADS[TOPK_NAME]
+    for K in TOPK_KS:
+        out.append((f"{TOPK_NAME}_K{K}", topk_bytes(w, K), w.rows))
+    return out
+
+
+# ------------------------------------------------------------------ environment
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "softmax_topk_gb300", "csrc", "**", "*.cu*"),
+                              recursive=True)):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel sources as they are now (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, t0: float, t1: float) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 1 <= r[0] <= t1 + 1]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "whole run"
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ our arm
+def make_step_inputs(dev, st):
+    """Device inputs and outputs for one step; TopK inputs rotated over L2."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    items = []
+    for n in SOFTMAX_STEP:
+        w = workloads.WORKLOADS[n]
+        x = workloads.make(w, device=dev)
+        y = torch.empty_like(x)
+        items.append(("softmax", n, [x], y, None))
+    w = workloads.WORKLOADS[TOPK_NAME]
+    xt = workloads.make(w, device=dev)
+    copies = -(-3 * l2 // (xt.numel() * 4)) + 1
+    xs = [xt] + [xt.clone() for _ in range(copies - 1)]
+    for K in TOPK_KS:
+        vals = torch.empty(w.rows, K, device=dev)
+        idx = torch.empty(w.rows, K, dtype=torch.int32, device=dev)
+        items.append(("topk", f"{TOPK_NAME}_K{K}", xs, (vals, idx), K))
+    return items, copies
+
+
+def launch(st, item, it):
+    kind, _, xs, out, K = item
+    x = xs[it % len(xs)]
+    if kind == "softmax":
+        st.softmax(x, out=out)
+    else:
+        st.softmax_topk(x, K, vals=out[0], idx=out[1])
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    import softmax_topk_gb300 as st
+
+    items, topk_copies = make_step_inputs(dev, st)
+    units = step_units()
+    stream = torch.cuda.current_stream(dev)
+
+    for it in range(args.warmup):
+        for item in items:
+            launch(st, item, it)
+    torch.cuda.synchronize(dev)
+
+    n_items = len(items)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_items + 1)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for it in range(args.steps):
+        evs[it][0].record(stream)
+        for j, item in enumerate(items):
+            launch(st, item, it)
+            evs[it][j + 1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.time()
+    clock_info = clocks.stop(t0, t1) if clocks else None
+
+    total_ms = start.elapsed_time(end)
+    per_item_ms = [sum(evs[it][j].elapsed_time(evs[it][j + 1]) for it in range(args.steps))
+                   / args.steps for j in range(n_items)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    step_bytes = sum(u[1] for u in units)
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    e2e = run_e2e(st, dev, args) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    per = {}
+    for (label, b, rows), ms in zip(units, per_item_ms):
+        per[label] = {"ms": round(ms, 5), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                      "rows_per_s": round(rows / (ms * 1e-3), 1),
+                      "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                      "frac_of_8tbs_nominal": round(b / (ms * 1e-3) / 1e9 / 8000.0, 4)}
+    dom = max(range(n_items), key=lambda j: per_item_ms[j])
+    dom_label, dom_bytes, _ = units[dom]
+    achieved = dom_bytes / (per_item_ms[dom] * 1e-3) / 1e9
+    kernel_name = kernel_of(st, dom_label)
+    traffic = recorded_traffic(kernel_name)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded generators in workloads/, shapes and distributions of the "
+                "pages' workloads)",
+        "config": {"workload": "softmax 4096x32000 f32 + softmax 8192x128256 bf16 + TopK "
+                               "256x50257 f32 K=8,64",
+                   "l2": f"softmax inputs larger than L2; TopK input rotated over {topk_copies} "
+                         "copies (> 3x L2)",
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+        "per_workload": per,
+        "rows_per_s": {k: v["rows_per_s"] for k, v in per.items()},
+        "roofline": {"kernel": kernel_name, "workload": dom_label, "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": dom_bytes, "traffic": traffic},
+        "gpu_launches": n_items * args.steps,
+        "e2e": e2e,
+        "clocks": clock_info,
+    }
+    if args.extra:
+        line["extra_workloads"] = run_extra(st, dev, args)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def kernel_of(st, label: str) -> str:
+    if label.startswith("topk"):
+        return "topk_rows_kernel"
+    w = workloads.WORKLOADS[label]
+    code = st.OS_F32 if w.dtype == "f32" else st.OS_BF16
+    p = st.plan((w.rows, w.cols), code)
+    fam = {st.OS_PATH_WARP: "warp_rows_kernel", st.OS_PATH_ONCHIP: "onchip_rows_kernel",
+           st.OS_PATH_STREAM: "stream_rows_kernel"}[p["path"]]
+    return f"{fam}<{w.dtype},{w.dtype},threads={p['threads']},cluster={p['cluster']}>"
+
+
+def run_e2e(st, dev, args):
+    """Same step through the public API from pinned host buffers."""
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for n in SOFTMAX_STEP:
+        w = workloads.WORKLOADS[n]
+        x = workloads.make(w, device=dev).cpu().pin_memory()
+        host_in.append(x)
+        host_out.append(torch.empty_like(x).pin_memory())
+        h2d += x.numel() * x.element_size()
+        d2h += x.numel() * x.element_size()
+    w = workloads.WORKLOADS[TOPK_NAME]
+    xt = workloads.make(w, device=dev).cpu().pin_memory()
+    h2d += xt.numel() * 4
+    topk_out = []
+    for K in TOPK_KS:
+        topk_out.append((torch.empty(w.rows, K).pin_memory(),
+                         torch.empty(w.rows, K, dtype=torch.int32).pin_memory()))
+        d2h += w.rows * K * 8
+    dev_in = [torch.empty_like(h, device=dev) for h in host_in]
+    dev_out = [torch.empty_like(h, device=dev) for h in host_in]
+    dev_xt = torch.empty_like(xt, device=dev)
+    dev_topk = [(torch.empty(w.rows, K, device=dev), torch.empty(w.rows, K, dtype=torch.int32,
+                                                                  device=dev)) for K in TOPK_KS]
+
+    def one_step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        dev_xt.copy_(xt, non_blocking=True)
+        for d, o in zip(dev_in, dev_out):
+            st.softmax(d, out=o)
+        for K, (v, i) in zip(TOPK_KS, dev_topk):
+            st.softmax_topk(dev_xt, K, vals=v, idx=i)
+        for o, h in zip(dev_out, host_out):
+            h.copy_(o, non_blocking=True)
+        for (v, i), (hv, hi) in zip(dev_topk, topk_out):
+            hv.copy_(v, non_blocking=True)
+            hi.copy_(i, non_blocking=True)
+
+    steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        one_step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    step_bytes = sum(u[1] for u in step_units())
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_extra(st, dev, args):
+    """The other workloads (parity cases), timed the same way, for reference."""
+    out = {}
+    peak, _ = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.current_stream(dev)
+    for n in EXTRA:
+        w = workloads.WORKLOADS[n]
+        x = workloads.make(w, device=dev)
+        copies = max(1, -(-3 * l2 // (x.numel() * x.element_size())) + 1)
+        xs = [x] + [x.clone() for _ in range(copies - 1)] if x.numel() * 4 < 3 * l2 else [x]
+        y = torch.empty_like(x)
+        for i in range(3):
+            st.softmax(xs[i % len(xs)], out=y)
+        steps = max(10, args.steps)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for i in range(steps):
+            st.softmax(xs[i % len(xs)], out=y)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / steps
+        gbs = softmax_bytes(w) / (ms * 1e-3) / 1e9
+        out[n] = {"ms": round(ms, 5), "gbs": round(gbs, 1), "rows_per_s": round(w.rows / ms * 1e3),
+                  "frac_of_measured_hbm": round(gbs / peak, 4), "input_copies": len(xs)}
+        del xs, x, y
+    return out
+
+
+# ------------------------------------------------------------------ oracle (CPU) legs
+def oracle_sample_run(rows_fraction: float, seed_offset: int = 0):
+    """Run the float64 oracle on the first rows of every step workload.
+    Returns (seconds, compulsory bytes of the sample, description)."""
+    import oracle
+    oracle.build()
+    t_total, b_total, parts = 0.0, 0, []
+    for n in SOFTMAX_STEP + [TOPK_NAME]:
+        w = workloads.WORKLOADS[n]
+        rows = max(1, int(round(w.rows * rows_fraction)))
+        x = workloads.make(w.scaled(rows=rows), device="cpu",
+                           seed=w.seed + seed_offset).double().numpy()
+        if w.op == "softmax":
+            t = time.perf_counter()
+            oracle.softmax(x)
+            t_total += time.perf_counter() - t
+            b_total += softmax_bytes(w.scaled(rows=rows))
+        else:
+            for K in TOPK_KS:
+                t = time.perf_counter()
+                oracle.topk(x, K)
+                t_total += time.perf_counter() - t
+                b_total += topk_bytes(w.scaled(rows=rows), K)
+        parts.append(f"{rows} rows of {n}")
+    return t_total, b_total, "; ".join(parts)
+
+
+def cpu_baseline(target_seconds: float) -> dict:
+    import oracle
+    frac = 1.0 / 256
+    t, b, desc = oracle_sample_run(frac)
+    if t < target_seconds / 4:  # grow the sample toward the target CPU time
+        frac = min(1.0, frac * target_seconds / max(t, 1e-3) / 2)
+        t, b, desc = oracle_sample_run(frac)
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(t, 2),
+            "sample": f"{desc} (fraction {frac:.5f} of each step workload's rows)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    frac = 1.0 / 1024
+    secs = []
+    for i in range(args.warmup + args.steps):
+        t, b, desc = oracle_sample_run(frac, seed_offset=i)
+        if i >= args.warmup:
+            secs.append(t)
+    t = sum(secs) / len(secs)
+    value = b / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "softmax 4096x32000 f32 + softmax 8192x128256 bf16 + TopK "
+                                   "256x50257 f32 K=8,64",
+                       "sample": f"each step: {desc}"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                             "cores": oracle.num_threads(), "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--extra", action="store_true", help="also time the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,154 @@
+/*
+ * os_softmax.h -- C ABI of libos_softmax.so: row-wise online-normalizer
+ * softmax and fused softmax+TopK on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Operations (statement of the problem):
+ *   softmax : for each row r of x[rows, cols], y[r, i] = e^(x[r,i] - m_r) / d_r
+ *             with m_r = max_j x[r,j] and d_r = sum_j e^(x[r,j] - m_r)
+ *             ("Online normalizer calculation for softmax" notes, section 2,
+ *             safe softmax; computed with the single-pass online normalizer of
+ *             its section 3 and the (m, d) combine of section 3.3).
+ *   topk    : for each row, the K largest probabilities v and their column
+ *             indices z, without writing the full probability row (same notes,
+ *             section 4, "Softmax and top-k fusion": select the K largest
+ *             logits u in the normalizer's single pass, then
+ *             v_i = e^(u_i - m_r) / d_r).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers into dense row-major buffers (row stride =
+ *     cols elements) that the caller allocates, owns and frees.  The library
+ *     allocates no device or host memory and keeps no per-call state.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  The return value reports argument errors and launch
+ *     errors (the return code of the CUDA launch); a fault inside a kernel
+ *     surfaces at the caller's next synchronisation, as for any CUDA launch.
+ *   - rows == 0 is a no-op returning OS_OK.  cols must be in [1, 2^31 - 1].
+ *   - Inputs are assumed free of NaN.  -inf entries are allowed and get
+ *     probability exactly +0; a row whose entries are ALL -inf has no defined
+ *     softmax and its outputs are unspecified (NaN in practice).
+ *   - Arithmetic: fp32 throughout (bf16 inputs widened exactly, fp32
+ *     accumulation, bf16 outputs rounded to nearest even).  The exponential is
+ *     the library's own fp32 routine on the FMA pipe (no ex2.approx).
+ *   - Work runs on the device current at the call (cudaGetDevice); the
+ *     pointers and the stream must belong to it.  There is no CPU fallback.
+ */
+#ifndef OS_SOFTMAX_H
+#define OS_SOFTMAX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t. */
+typedef struct CUstream_st *os_stream_t;
+
+typedef enum {
+    OS_F32 = 0,  /* IEEE binary32 */
+    OS_BF16 = 1  /* bfloat16 */
+} os_dtype;
+
+typedef enum {
+    OS_OK = 0,
+    OS_ERR_NULL = 1,    /* a required pointer is NULL (with rows > 0) */
+    OS_ERR_SHAPE = 2,   /* rows < 0, cols outside [1, 2^31 - 1] */
+    OS_ERR_DTYPE = 3,   /* dtype value not in os_dtype */
+    OS_ERR_K = 4,       /* K outside [1, min(cols, 64)] */
+    OS_ERR_ALIAS = 5,   /* an output overlaps an input or another output */
+    OS_ERR_CUDA = 6,    /* the CUDA runtime reported an error (launch or device query) */
+    OS_ERR_TIMEOUT = 7, /* reserved: a device-side bounded wait gave up */
+    OS_ERR_PATH = 8,    /* the requested kernel family cannot run this shape */
+    OS_ERR_ALIGN = 9    /* a pointer is not aligned to its element size */
+} os_status;
+
+/* Kernel families (see os_softmax_fwd_path). */
+typedef enum {
+    OS_PATH_AUTO = 0,   /* choose by row length, dtype and device */
+    OS_PATH_WARP = 1,   /* 1..32 lanes per row, row held in registers; short rows */
+    OS_PATH_ONCHIP = 2, /* one CTA or a thread-block cluster per row, row held
+                           in registers across the cluster; one HBM read */
+    OS_PATH_STREAM = 3  /* two passes over the row (running (m, d), then
+                           normalise); any row length */
+} os_path;
+
+/* Launch configuration chosen for a call (see os_softmax_plan / os_topk_plan). */
+typedef struct {
+    int32_t path;               /* os_path actually used (never AUTO) */
+    int32_t threads;            /* threads per CTA */
+    int32_t vectors_per_thread; /* 16-byte input vectors held per thread (per chunk for STREAM) */
+    int32_t cluster;            /* CTAs per row (thread-block cluster size), 1 if none */
+    int32_t lanes_per_row;      /* WARP path: lanes that share one row; else 0 */
+    int32_t reserved;
+    int64_t grid;               /* CTAs launched */
+} os_plan;
+
+/*
+ * y = softmax(x) row by row.
+ *   x         device pointer, rows*cols elements of in_dtype, read only.
+ *   y         device pointer, rows*cols elements of out_dtype, written.
+ *             Must not overlap x (OS_ERR_ALIAS).
+ *   in_dtype, out_dtype: OS_F32 or OS_BF16, in any combination.
+ * Pointers must be aligned to their element size (OS_ERR_ALIGN); 16-byte
+ * alignment of both and cols a multiple of 16/sizeof(in) give 128-bit access.
+ */
+os_status os_softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols,
+                         os_dtype in_dtype, os_dtype out_dtype, os_stream_t stream);
+
+/*
+ * Fused softmax + TopK: for each row the K largest probabilities, best first.
+ *   x     device pointer, rows*cols fp32 logits, read only (4-byte aligned is
+ *         enough; rows need not start on 16-byte boundaries).
+ *   vals  device pointer, rows*K fp32: vals[r*K + k] = e^(x[r,z] - m_r) / d_r
+ *         of the k-th best column z.
+ *   idx   device pointer, rows*K int32: the column indices z.
+ *   K     1 <= K <= min(cols, 64).
+ * Order: larger logit first; equal logits (ties) go to the LOWER column index.
+ * Selection compares the input logits, so distinct logits whose probabilities
+ * round to the same fp32 value keep their logit order.  vals and idx must not
+ * overlap x or each other (OS_ERR_ALIAS).
+ */
+os_status os_softmax_topk(const float *x, float *vals, int32_t *idx, int64_t rows,
+                          int64_t cols, int32_t K, os_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *os_status_string(os_status status);
+
+/*
+ * os_softmax_fwd with the kernel family fixed by the caller (tests and
+ * benchmarks use it to exercise every family on the same shape).
+ * OS_PATH_AUTO behaves exactly like os_softmax_fwd.  A family that cannot
+ * hold the row (WARP beyond 32 x 8 vectors, ONCHIP beyond the largest
+ * cluster the device can launch) returns OS_ERR_PATH and launches nothing.
+ */
+os_status os_softmax_fwd_path(const void *x, void *y, int64_t rows, int64_t cols,
+                              os_dtype in_dtype, os_dtype out_dtype, os_path path,
+                              os_stream_t stream);
+
+/*
+ * The launch configuration os_softmax_fwd_path would use for this shape on the
+ * current device, written to *plan; nothing is launched.  Same argument
+ * checks as the launching call, minus the pointer checks.
+ */
+os_status os_softmax_plan(int64_t rows, int64_t cols, os_dtype in_dtype, os_dtype out_dtype,
+                          os_path path, os_plan *plan);
+
+/* The launch configuration os_softmax_topk would use; nothing is launched. */
+os_status os_topk_plan(int64_t rows, int64_t cols, int32_t K, os_plan *plan);
+
+/*
+ * out[i] = e^(z[i]) for n fp32 values with the library's own exponential, the
+ * routine every kernel above uses (Cody-Waite reduction z = n ln2 + r, a
+ * degree-6 minimax polynomial for e^r, 2^n written into the exponent field;
+ * no ex2.approx).  Defined for z <= 88: within about 1 ulp of e^z for
+ * z >= -87.33, 0 or a value below FLT_MIN for smaller z, exactly +0 for
+ * z = -inf.  Exposed so the routine can be tested on its own.
+ *   z, out  device pointers to n fp32 values (may be the same buffer).
+ */
+os_status os_exp_f32(const float *z, float *out, int64_t n, os_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OS_SOFTMAX_H */

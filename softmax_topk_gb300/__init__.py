@@ -1,0 +1,183 @@
+"""Python binding of libos_softmax.so (row-wise online softmax, fused softmax+TopK).
+
+The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
+``os_softmax_fwd``, ``os_softmax_topk``, ``os_softmax_fwd_path``,
+``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_status_string``.  They take raw
+device pointers (ints) and a raw stream handle, exactly like the C functions,
+and raise ``OsError`` on a non-OK status.
+
+``softmax`` and ``softmax_topk`` are the tensor-level conveniences: they take
+torch CUDA tensors, allocate outputs with torch, pass the current torch
+stream, and call the same C entry points.  PyTorch only provides memory and
+streams; every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is not built, importing this package
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libos_softmax.so")
+
+OS_F32, OS_BF16 = 0, 1
+OS_PATH_AUTO, OS_PATH_WARP, OS_PATH_ONCHIP, OS_PATH_STREAM = 0, 1, 2, 3
+PATHS = {"auto": OS_PATH_AUTO, "warp": OS_PATH_WARP, "onchip": OS_PATH_ONCHIP,
+         "stream": OS_PATH_STREAM}
+STATUS = ["OS_OK", "OS_ERR_NULL", "OS_ERR_SHAPE", "OS_ERR_DTYPE", "OS_ERR_K", "OS_ERR_ALIAS",
+          "OS_ERR_CUDA", "OS_ERR_TIMEOUT", "OS_ERR_PATH", "OS_ERR_ALIGN"]
+KMAX = 64
+
+
+class OsError(RuntimeError):
+    """A libos_softmax call returned a status other than OS_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.name = STATUS[status] if 0 <= status < len(STATUS) else str(status)
+        super().__init__(f"{where}: {os_status_string(status)}")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("vectors_per_thread", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("lanes_per_row", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("grid", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libos_softmax.so is not built ({LIB_PATH} missing); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` or "
+            "`python softmax_topk_gb300/build.py` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+    lib.os_softmax_fwd.argtypes = [vp, vp, i64, i64, st, st, vp]
+    lib.os_softmax_fwd_path.argtypes = [vp, vp, i64, i64, st, st, st, vp]
+    lib.os_softmax_topk.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+    lib.os_softmax_plan.argtypes = [i64, i64, st, st, st, ctypes.POINTER(Plan)]
+    lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
+    lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
+    lib.os_status_string.argtypes = [st]
+    lib.os_status_string.restype = ctypes.c_char_p
+    for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_softmax_plan",
+                 "os_topk_plan", "os_exp_f32"):
+        getattr(lib, name).restype = st
+    return lib
+
+
+_lib = _load()
+
+
+def os_status_string(status: int) -> str:
+    return _lib.os_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise OsError(status, where)
+
+
+# ---------------------------------------------------------------- raw C entry points
+def os_softmax_fwd(x: int, y: int, rows: int, cols: int, in_dtype: int, out_dtype: int,
+                   stream: int | None) -> None:
+    _check(_lib.os_softmax_fwd(x, y, rows, cols, in_dtype, out_dtype, stream), "os_softmax_fwd")
+
+
+def os_softmax_fwd_path(x: int, y: int, rows: int, cols: int, in_dtype: int, out_dtype: int,
+                        path: int, stream: int | None) -> None:
+    _check(_lib.os_softmax_fwd_path(x, y, rows, cols, in_dtype, out_dtype, path, stream),
+           "os_softmax_fwd_path")
+
+
+def os_softmax_topk(x: int, vals: int, idx: int, rows: int, cols: int, K: int,
+                    stream: int | None) -> None:
+    _check(_lib.os_softmax_topk(x, vals, idx, rows, cols, K, stream), "os_softmax_topk")
+
+
+def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
+    _check(_lib.os_exp_f32(z, out, n, stream), "os_exp_f32")
+
+
+def os_softmax_plan(rows: int, cols: int, in_dtype: int, out_dtype: int, path: int = 0) -> dict:
+    p = Plan()
+    _check(_lib.os_softmax_plan(rows, cols, in_dtype, out_dtype, path, ctypes.byref(p)),
+           "os_softmax_plan")
+    return p.as_dict()
+
+
+def os_topk_plan(rows: int, cols: int, K: int) -> dict:
+    p = Plan()
+    _check(_lib.os_topk_plan(rows, cols, K, ctypes.byref(p)), "os_topk_plan")
+    return p.as_dict()
+
+
+# ---------------------------------------------------------------- torch conveniences
+def _dtype_code(t) -> int:
+    import torch
+    if t == torch.float32:
+        return OS_F32
+    if t == torch.bfloat16:
+        return OS_BF16
+    raise TypeError(f"unsupported dtype {t}: float32 or bfloat16")
+
+
+def _stream_handle(x) -> int:
+    import torch
+    return torch.cuda.current_stream(x.device).cuda_stream
+
+
+def softmax(x, out_dtype=None, path: str | int = "auto", out=None):
+    """Row-wise softmax of a 2-D CUDA tensor (fp32 or bf16) along its last dim."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D CUDA tensor")
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    elif out.shape != x.shape or out.dtype != out_dtype or not out.is_contiguous():
+        raise ValueError("out must be contiguous with x's shape and out_dtype")
+    code = PATHS[path] if isinstance(path, str) else int(path)
+    with torch.cuda.device(x.device):
+        os_softmax_fwd_path(x.data_ptr(), out.data_ptr(), x.shape[0], x.shape[1],
+                            _dtype_code(x.dtype), _dtype_code(out_dtype), code,
+                            _stream_handle(x))
+    return out
+
+
+def softmax_topk(x, K: int, vals=None, idx=None):
+    """(probabilities fp32 [rows, K], column indices int32 [rows, K]) of each row's top K."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous() or x.dtype != torch.float32:
+        raise ValueError("x must be a contiguous 2-D float32 CUDA tensor")
+    rows = x.shape[0]
+    if vals is None:
+        vals = torch.empty((rows, K), dtype=torch.float32, device=x.device)
+    if idx is None:
+        idx = torch.empty((rows, K), dtype=torch.int32, device=x.device)
+    with torch.cuda.device(x.device):
+        os_softmax_topk(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, x.shape[1], K,
+                        _stream_handle(x))
+    return vals, idx
+
+
+def exp(z):
+    """e^z elementwise (fp32 CUDA tensor) with the library's own exponential."""
+    import torch
+    if not z.is_cuda or z.dtype != torch.float32 or not z.is_contiguous():
+        raise ValueError("z must be a contiguous float32 CUDA tensor")
+    out = torch.empty_like(z)
+    with torch.cuda.device(z.device):
+        os_exp_f32(z.data_ptr(), out.data_ptr(), z.numel(), _stream_handle(z))
+    return out
+
+
+def plan(x_shape, in_dtype=OS_F32, out_dtype=None, path: str | int = "auto") -> dict:
+    out_dtype = in_dtype if out_dtype is None else out_dtype
+    code = PATHS[path] if isinstance(path, str) else int(path)
+    return os_softmax_plan(int(x_shape[0]), int(x_shape[1]), in_dtype, out_dtype, code)

@@ -1,0 +1,21 @@
+// Elementwise e^z with the library's own fp32 exponential (os_exp_f32).
+#include "host_common.h"
+#include "internal.h"
+#include "kernels/ops.cuh"
+
+namespace os {
+
+__global__ void exp_kernel(const float* z, float* out, int64_t n) {  // z and out may alias
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        out[i] = exp1(z[i]);
+}
+
+cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return cudaErrorNoDevice;
+    const int64_t grid = min64(ceil_div(n, 256), int64_t(dev->sms) * 8);
+    return launch_kernel(exp_kernel, grid, 256, 1, stream, z, out, n);
+}
+
+}  // namespace os

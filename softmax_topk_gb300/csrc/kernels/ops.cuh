@@ -1,0 +1,256 @@
+// ops.cuh -- device building blocks shared by the softmax and TopK kernels.
+//
+//  * packed fp32 pair arithmetic (the sm_100-family f32x2 FMA/ADD/MUL forms),
+//  * the library's own fp32 exponential (no ex2.approx / MUFU),
+//  * the (m, d) online-normalizer state and its merge over lanes,
+//  * 128-bit vector loads/stores with bf16 <-> fp32 conversion,
+//  * thread-block-cluster helpers (rank, barrier, distributed shared memory).
+//
+// The (m, d) state and its operator follow "Online normalizer calculation for
+// softmax" (notes), section 3.3: (m1,d1) (+) (m2,d2) = (max, d1 e^(m1-max) +
+// d2 e^(m2-max)), associative and commutative, identity (-inf, 0) (Lesson 7
+// "Online Softmax and associative state", section 3).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace os {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// ------------------------------------------------------------------ f32x2
+// One instruction operates on two fp32 lanes held in a 64-bit register pair,
+// halving the issue slots of the exponential's FMA chain.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// Three-input maximum (one instruction on sm_100-family GPUs).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// ------------------------------------------------------------------ exp
+// e^z for z <= 88, in fp32, on the FMA pipe only.
+//
+//   z := max(z, -88)                      (-inf and NaN become -88: result 0)
+//   n  = rint(z log2 e)                   via the 1.5*2^23 rounding constant
+//   r  = (z - n ln2_hi) - n ln2_lo        Cody & Waite reduction, |r| <~ ln2/2
+//   p  = 1 + c1 r + ... + c6 r^6          minimax fit of e^r on that interval
+//   e^z = p * 2^n                         2^n written into the exponent field
+//
+// For z >= -87.33 the result is within about 1 ulp of e^z; for z in
+// [-88, -87.33) it is 0 or a value below FLT_MIN (e^z itself is below FLT_MIN
+// there); z = -inf gives exactly +0.  The polynomial coefficients come from
+// the Lawson fit in csrc/fit_exp_poly.py, not from any library.
+namespace expc {
+constexpr float kLog2e = 1.442695022e+00f;   // fp32(log2 e)
+constexpr float kRound = 12582912.0f;        // 1.5 * 2^23: adding it rounds to an integer
+constexpr float kLn2Hi = 0.693145751953125f; // ln 2 with its low bits cleared (exact n*ln2_hi)
+constexpr float kLn2Lo = 1.428606765e-06f;   // ln 2 - kLn2Hi
+constexpr float kFloor = -88.0f;
+constexpr float c1 = 1.0f;
+constexpr float c2 = 0.49999994f;
+constexpr float c3 = 0.1666643f;
+constexpr float c4 = 0.041668005f;
+constexpr float c5 = 0.008374209f;
+constexpr float c6 = 0.0013843592f;
+}  // namespace expc
+
+// 2^n from t = kRound + n: the low bits of t's pattern hold n; shifting them
+// into the exponent field and adding the bias gives 2^n (n = -127 -> +0).
+__device__ __forceinline__ float pow2_from_rounded(float t) {
+    return __uint_as_float((__float_as_uint(t) << 23) + 0x3f800000u);
+}
+
+__device__ __forceinline__ float2 exp2x(float2 z) {
+    using namespace expc;
+    z.x = fmaxf(z.x, kFloor);
+    z.y = fmaxf(z.y, kFloor);
+    const float2 t = fma2(z, splat2(kLog2e), splat2(kRound));
+    const float2 n = add2(t, splat2(-kRound));
+    float2 r = fma2(n, splat2(-kLn2Hi), z);
+    r = fma2(n, splat2(-kLn2Lo), r);
+    float2 p = fma2(splat2(c6), r, splat2(c5));
+    p = fma2(p, r, splat2(c4));
+    p = fma2(p, r, splat2(c3));
+    p = fma2(p, r, splat2(c2));
+    p = fma2(p, r, splat2(c1));
+    p = fma2(p, r, splat2(1.0f));
+    return mul2(p, make_float2(pow2_from_rounded(t.x), pow2_from_rounded(t.y)));
+}
+
+__device__ __forceinline__ float exp1(float z) {
+    using namespace expc;
+    z = fmaxf(z, kFloor);
+    const float t = fmaf(z, kLog2e, kRound);
+    const float n = t - kRound;
+    float r = fmaf(n, -kLn2Hi, z);
+    r = fmaf(n, -kLn2Lo, r);
+    float p = fmaf(c6, r, c5);
+    p = fmaf(p, r, c4);
+    p = fmaf(p, r, c3);
+    p = fmaf(p, r, c2);
+    p = fmaf(p, r, c1);
+    p = fmaf(p, r, 1.0f);
+    return p * pow2_from_rounded(t);
+}
+
+// ------------------------------------------------------------------ (m, d)
+// Rescale factor e^(m - M) of a state with maximum m into a merge whose
+// maximum is M >= m.  m == M gives 1 (also when both are -inf: the NaN of
+// -inf - -inf becomes 0 inside exp1, and such a state has d = 0 anyway).
+__device__ __forceinline__ float rescale(float m, float M) {
+    return m == M ? 1.0f : exp1(m - M);
+}
+
+// n-ary (+) over aligned groups of G lanes (G a power of two <= 32): the
+// maxima are max-reduced, every lane rescales its own d once to the group
+// maximum, and the rescaled d are sum-reduced.  By associativity this equals
+// folding the pairwise operator over the group; every lane ends with the
+// group's state.  All 32 lanes of the warp must call it together.
+template <int G>
+__device__ __forceinline__ void group_merge(float& m, float& d) {
+    float M = m;
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+    d *= rescale(m, M);
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) d += __shfl_xor_sync(kFullMask, d, o);
+    m = M;
+}
+
+// ------------------------------------------------------------------ vectors
+// A 16-byte input vector holds EPV = 16 / sizeof(T) elements.
+template <typename T> struct VecTraits;
+template <> struct VecTraits<float> { static constexpr int EPV = 4; };
+template <> struct VecTraits<__nv_bfloat16> { static constexpr int EPV = 8; };
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Unpack one 16-byte vector of T into EPV floats.
+__device__ __forceinline__ void unpack(const uint4& v, float* out, float) {
+    out[0] = __uint_as_float(v.x); out[1] = __uint_as_float(v.y);
+    out[2] = __uint_as_float(v.z); out[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void unpack(const uint4& v, float* out, __nv_bfloat16) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Store N consecutive outputs (N = EPV of the input type) with the widest
+// aligned vector stores; streaming (evict-first) cache hint.
+template <typename TO, int N> struct VecStore;
+template <> struct VecStore<float, 4> {
+    __device__ __forceinline__ static void run(float* p, const float* v) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+    }
+};
+template <> struct VecStore<float, 8> {
+    __device__ __forceinline__ static void run(float* p, const float* v) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
+    }
+};
+template <> struct VecStore<__nv_bfloat16, 4> {
+    __device__ __forceinline__ static void run(__nv_bfloat16* p, const float* v) {
+        uint2 w = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        __stcs(reinterpret_cast<uint2*>(p), w);
+    }
+};
+template <> struct VecStore<__nv_bfloat16, 8> {
+    __device__ __forceinline__ static void run(__nv_bfloat16* p, const float* v) {
+        uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        __stcs(reinterpret_cast<uint4*>(p), w);
+    }
+};
+
+// ------------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Full barrier over all threads of all CTAs of the cluster; the release /
+// acquire pair orders shared-memory writes to peers before their reads.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `local` (a __shared__ object of this CTA) in CTA `rank`'s
+// shared memory window of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void* local, uint32_t rank) {
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(v.x), "f"(v.y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_b64(uint32_t addr, uint32_t lo, uint32_t hi) {
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" :: "r"(addr), "r"(lo), "r"(hi)
+                 : "memory");
+}
+
+}  // namespace os

@@ -1,0 +1,323 @@
+// softmax_kernels.cuh -- row-wise online-normalizer softmax, three kernel families.
+//
+// All three compute, per row, y_i = e^(x_i - m) / d with (m, d) the row's
+// online-normalizer state ("Online normalizer calculation for softmax"
+// notes, section 3; "5.2 CUDA Online Softmax", sections 2-7):
+//
+//   * each thread reduces the elements it owns to a state (m_t, d_t) with
+//     the chunked update m' = max(m, max chunk), d' = d e^(m - m') +
+//     sum_chunk e^(x - m') (Lesson 7, NumPy chunked simulation);
+//   * thread states are merged with the (+) operator: across lanes with
+//     shuffles, across warps through shared memory, across the CTAs of a
+//     thread-block cluster through distributed shared memory;
+//   * the output pass writes y_i = e^(x_i - m) / d.
+//
+// warp_rows   Rows of at most 32 x VPT vectors.  A group of L lanes owns one
+//             row, held in registers: one HBM read and one write per element
+//             ("CUDA operator optimization (3)", warp per row; "5.2", V3
+//             register cache).
+// onchip_rows Rows up to CLUSTER x THREADS x VPT vectors.  The row is split
+//             over the CTAs of a cluster and held in registers; each thread
+//             keeps e^(x - m_t) for its elements, so the output pass is one
+//             multiply by e^(m_t - m)/d per element (one exponential per
+//             element in total) and HBM sees one read and one write.
+// stream_rows Any row length.  Pass 1 streams the row and keeps a running
+//             (m, d) per thread with one rescale per chunk of UNROLL vectors;
+//             pass 2 re-reads the row and writes y ("5.2", V2/V4 two-pass).
+//
+// Layout: x and y are dense row-major [rows, cols]; a "vector" is 16 bytes of
+// input (4 fp32 or 8 bf16).  When cols is a multiple of the vector width and
+// both base pointers are 16-byte aligned ("aligned"), every row starts on a
+// vector boundary and all traffic is 128-bit; otherwise the same register
+// layout is filled and drained element by element.
+#pragma once
+
+#include "ops.cuh"
+
+namespace os {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Load vector slot v of a row (elements v*EPV .. v*EPV+EPV-1) into out[];
+// elements at or beyond `cols` read as -inf.
+template <typename TI>
+__device__ __forceinline__ void load_slot(const TI* row, int64_t v, int cols, bool aligned,
+                                          float* out) {
+    constexpr int EPV = VecTraits<TI>::EPV;
+    if (aligned) {
+        unpack(ld_stream_v4(row + v * EPV), out, TI());
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const int64_t j = v * EPV + e;
+            out[e] = j < cols ? to_f32(row[j]) : kNegInf;
+        }
+    }
+}
+
+template <typename TI, typename TO>
+__device__ __forceinline__ void store_slot(TO* row, int64_t v, int cols, bool aligned,
+                                           const float* vals) {
+    constexpr int EPV = VecTraits<TI>::EPV;
+    if (aligned) {
+        VecStore<TO, EPV>::run(row + v * EPV, vals);
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const int64_t j = v * EPV + e;
+            if (j < cols) row[j] = from_f32<TO>(vals[e]);
+        }
+    }
+}
+
+// e[i] := e^(e[i] - m) for all N entries, returning the sum (pairs on f32x2).
+template <int N>
+__device__ __forceinline__ float exp_shift_sum(float* e, float m) {
+    static_assert(N % 2 == 0, "pairs");
+    float2 acc = make_float2(0.f, 0.f);
+    const float2 neg_m = splat2(-m);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        float2 z = add2(make_float2(e[i], e[i + 1]), neg_m);
+        float2 p = exp2x(z);
+        e[i] = p.x;
+        e[i + 1] = p.y;
+        acc = add2(acc, p);
+    }
+    return acc.x + acc.y;
+}
+
+// sum of e^(e[i] - m) over N entries, leaving e unchanged.
+template <int N>
+__device__ __forceinline__ float exp_sum(const float* e, float m) {
+    static_assert(N % 2 == 0, "pairs");
+    float2 acc = make_float2(0.f, 0.f);
+    const float2 neg_m = splat2(-m);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) acc = add2(acc, exp2x(add2(make_float2(e[i], e[i + 1]), neg_m)));
+    return acc.x + acc.y;
+}
+
+template <int N>
+__device__ __forceinline__ float max_of(const float* e) {
+    float m = e[0];
+    int i = 1;
+#pragma unroll
+    for (; i + 1 < N; i += 2) m = max3(m, e[i], e[i + 1]);
+    if (i < N) m = fmaxf(m, e[i]);
+    return m;
+}
+
+template <int N>
+__device__ __forceinline__ void scale_all(float* e, float s) {
+    const float2 s2 = splat2(s);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        float2 p = mul2(make_float2(e[i], e[i + 1]), s2);
+        e[i] = p.x;
+        e[i + 1] = p.y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// warp_rows: L lanes per row (L in 1..32, power of two), VPT vectors per lane.
+// Lane l of a group owns vector slots l, l + L, ..., l + (VPT-1) L, so a warp
+// instruction covers 32 consecutive vectors of one row (or 32/L rows).
+template <typename TI, typename TO, int L, int VPT, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+warp_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+                 int aligned) {
+    constexpr int EPV = VecTraits<TI>::EPV, EPT = VPT * EPV, RPW = 32 / L;
+    const int lane_in_row = threadIdx.x % L;
+    const int64_t warp = (int64_t(blockIdx.x) * THREADS + threadIdx.x) / 32;
+    const int64_t nwarps = int64_t(gridDim.x) * THREADS / 32;
+    const int64_t nv = (cols + EPV - 1) / EPV;
+
+    for (int64_t base = warp * RPW; base < rows; base += nwarps * RPW) {
+        const int64_t row = base + (threadIdx.x % 32) / L;
+        const bool live = row < rows;
+        const TI* xr = x + (live ? row : 0) * int64_t(cols);
+        TO* yr = y + (live ? row : 0) * int64_t(cols);
+
+        float e[EPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t v = int64_t(k) * L + lane_in_row;
+            if (live && v < nv) {
+                load_slot(xr, v, cols, aligned, e + k * EPV);
+            } else {
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
+            }
+        }
+        float m = max_of<EPT>(e);
+        float d = exp_shift_sum<EPT>(e, m);
+        const float m_t = m;
+        group_merge<L>(m, d);
+        scale_all<EPT>(e, rescale(m_t, m) * (1.0f / d));
+        if (live) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int64_t v = int64_t(k) * L + lane_in_row;
+                if (v < nv) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge of per-thread states of one CTA (and of the CTAs of a cluster).
+// Each CTA's state goes into slot[parity][rank] of every CTA of the cluster;
+// after one cluster barrier every thread folds the CLUSTER slots itself.
+// The parity double buffer keeps row r+1's writes away from row r's reads:
+// a CTA writes row r+2's slots only after the barrier of row r+1, which every
+// peer reaches after reading row r's slots.
+template <int THREADS, int CLUSTER>
+struct RowMergeSmem {
+    float2 warp_state[THREADS / 32];
+    float2 slot[2][CLUSTER];
+};
+
+template <int THREADS, int CLUSTER>
+__device__ __forceinline__ float2 merge_row_state(RowMergeSmem<THREADS, CLUSTER>& sm, float m,
+                                                  float d, int parity, uint32_t rank) {
+    constexpr int NW = THREADS / 32;
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    group_merge<32>(m, d);
+    if (lane == 0) sm.warp_state[warp] = make_float2(m, d);
+    __syncthreads();
+    if (warp == 0) {
+        float2 s = lane < NW ? sm.warp_state[lane] : make_float2(kNegInf, 0.f);
+        group_merge<32>(s.x, s.y);
+        if (lane < CLUSTER) {
+            if (CLUSTER == 1) {
+                sm.slot[parity][0] = s;
+            } else {
+                st_cluster_f2(map_to_rank(&sm.slot[parity][rank], lane), s);
+            }
+        }
+    }
+    if (CLUSTER == 1) {
+        __syncthreads();
+        return sm.slot[parity][0];
+    }
+    cluster_sync();
+    float M = kNegInf;
+#pragma unroll
+    for (int c = 0; c < CLUSTER; ++c) M = fmaxf(M, sm.slot[parity][c].x);
+    float D = 0.f;
+#pragma unroll
+    for (int c = 0; c < CLUSTER; ++c) D += sm.slot[parity][c].y * rescale(sm.slot[parity][c].x, M);
+    return make_float2(M, D);
+}
+
+// ---------------------------------------------------------------------------
+// onchip_rows: one cluster of CLUSTER CTAs per row (persistent over rows).
+// CTA `rank` owns vector slots [rank*S, rank*S + S) with S = THREADS*VPT;
+// thread t owns slots rank*S + t + k*THREADS.
+template <typename TI, typename TO, int THREADS, int VPT, int CLUSTER>
+__global__ void __launch_bounds__(THREADS, 1)
+onchip_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+                   int aligned) {
+    constexpr int EPV = VecTraits<TI>::EPV, EPT = VPT * EPV;
+    __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
+    const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
+    const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
+    const int64_t nv = (cols + EPV - 1) / EPV;
+    const int64_t v0 = int64_t(rank) * THREADS * VPT + threadIdx.x;
+    if (CLUSTER > 1) cluster_sync();  // every CTA of the cluster is running before DSMEM use
+
+    int parity = 0;
+    for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
+        const TI* xr = x + row * int64_t(cols);
+        TO* yr = y + row * int64_t(cols);
+        float e[EPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t v = v0 + int64_t(k) * THREADS;
+            if (v < nv) {
+                load_slot(xr, v, cols, aligned, e + k * EPV);
+            } else {
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
+            }
+        }
+        const float m_t = max_of<EPT>(e);
+        const float d_t = exp_shift_sum<EPT>(e, m_t);
+        const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m_t, d_t, parity, rank);
+        scale_all<EPT>(e, rescale(m_t, md.x) * (1.0f / md.y));
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t v = v0 + int64_t(k) * THREADS;
+            if (v < nv) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// stream_rows: one cluster per row (persistent over rows); CTA `rank` owns a
+// contiguous range of vector slots; two passes over it.
+template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER>
+__global__ void __launch_bounds__(THREADS)
+stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+                   int aligned) {
+    constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV;
+    __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
+    const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
+    const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
+    const int64_t nv = (cols + EPV - 1) / EPV;
+    const int64_t per_cta = (nv + CLUSTER - 1) / CLUSTER;
+    const int64_t begin = int64_t(rank) * per_cta;
+    const int64_t end = begin + per_cta < nv ? begin + per_cta : nv;
+    if (CLUSTER > 1) cluster_sync();
+
+    int parity = 0;
+    for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
+        const TI* xr = x + row * int64_t(cols);
+        TO* yr = y + row * int64_t(cols);
+        // pass 1: running (m, d), one rescale per chunk of UNROLL vectors
+        float m = kNegInf, d = 0.f;
+        for (int64_t v = begin + threadIdx.x; v < end; v += int64_t(THREADS) * UNROLL) {
+            float e[EPC];
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+                const int64_t vk = v + int64_t(k) * THREADS;
+                if (vk < end) {
+                    load_slot(xr, vk, cols, aligned, e + k * EPV);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
+                }
+            }
+            const float m_new = fmaxf(m, max_of<EPC>(e));
+            const float s = exp_shift_sum<EPC>(e, m_new);
+            d = d * rescale(m, m_new) + s;
+            m = m_new;
+        }
+        const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m, d, parity, rank);
+        const float inv_d = 1.0f / md.y;
+        // pass 2: y = e^(x - m) / d
+        for (int64_t v = begin + threadIdx.x; v < end; v += int64_t(THREADS) * UNROLL) {
+            float e[EPC];
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+                const int64_t vk = v + int64_t(k) * THREADS;
+                if (vk < end) {
+                    load_slot(xr, vk, cols, aligned, e + k * EPV);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
+                }
+            }
+            exp_shift_sum<EPC>(e, md.x);
+            scale_all<EPC>(e, inv_d);
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+                const int64_t vk = v + int64_t(k) * THREADS;
+                if (vk < end) store_slot<TI, TO>(yr, vk, cols, aligned, e + k * EPV);
+            }
+        }
+    }
+}
+
+}  // namespace os

@@ -1,0 +1,157 @@
+// softmax_dispatch.cuh -- kernel choice and launch for one (input, output) dtype
+// pair.  Included by one translation unit per pair, which instantiates it.
+//
+// Choice by row length, in 16-byte input vectors nv = ceil(cols / EPV):
+//   WARP    nv <= 256: L = 1..32 lanes per row with 4 vectors per lane, or 32
+//           lanes with 8 vectors (rows of up to 1024 fp32 / 2048 bf16).
+//   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV): one CTA
+//           of 128/256/512 threads per row, or a cluster of 2..16 CTAs of 512
+//           threads when one CTA cannot hold the row (rows of up to 262144
+//           fp32 / 524288 bf16; 16-CTA clusters only where the device can
+//           schedule them).
+//   STREAM  anything longer: one CTA per row when there are enough rows to
+//           fill the GPU, else a cluster of 8 CTAs per row.
+// "5.2 CUDA Online Softmax" (sections 6.3 and 8.3) makes the same split on
+// its hardware: the register-cached single read (V3) for short rows, the
+// two-pass kernel (V2/V4) beyond the register budget.
+#pragma once
+
+#include "host_common.h"
+#include "kernels/softmax_kernels.cuh"
+
+namespace os {
+
+constexpr int kWarpThreads = 256;
+constexpr int kOnchipThreadsMax = 512;
+constexpr int kOnchipElemsPerThread = 32;
+constexpr int kStreamThreads = 512;
+constexpr int kStreamUnroll = 4;
+constexpr int kMaxCluster = 16;
+
+template <typename TI, typename TO>
+struct SoftmaxFamily {
+    using Kernel = void (*)(const TI*, TO*, int64_t, int, int);
+    static constexpr int EPV = VecTraits<TI>::EPV;
+    static constexpr int VPT = kOnchipElemsPerThread / EPV;
+
+    static Kernel warp(int lanes, int vpt) {
+        if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads>;
+        switch (lanes) {
+            case 1: return warp_rows_kernel<TI, TO, 1, 4, kWarpThreads>;
+            case 2: return warp_rows_kernel<TI, TO, 2, 4, kWarpThreads>;
+            case 4: return warp_rows_kernel<TI, TO, 4, 4, kWarpThreads>;
+            case 8: return warp_rows_kernel<TI, TO, 8, 4, kWarpThreads>;
+            case 16: return warp_rows_kernel<TI, TO, 16, 4, kWarpThreads>;
+            default: return warp_rows_kernel<TI, TO, 32, 4, kWarpThreads>;
+        }
+    }
+    static Kernel onchip(int threads, int cluster) {
+        if (cluster == 1) {
+            switch (threads) {
+                case 128: return onchip_rows_kernel<TI, TO, 128, VPT, 1>;
+                case 256: return onchip_rows_kernel<TI, TO, 256, VPT, 1>;
+                default: return onchip_rows_kernel<TI, TO, 512, VPT, 1>;
+            }
+        }
+        switch (cluster) {
+            case 2: return onchip_rows_kernel<TI, TO, 512, VPT, 2>;
+            case 4: return onchip_rows_kernel<TI, TO, 512, VPT, 4>;
+            case 8: return onchip_rows_kernel<TI, TO, 512, VPT, 8>;
+            default: return onchip_rows_kernel<TI, TO, 512, VPT, 16>;
+        }
+    }
+    static Kernel streaming(int cluster) {
+        return cluster == 1 ? stream_rows_kernel<TI, TO, kStreamThreads, kStreamUnroll, 1>
+                            : stream_rows_kernel<TI, TO, kStreamThreads, kStreamUnroll, 8>;
+    }
+
+    // Largest cluster size of the ONCHIP family the current device can run.
+    static int onchip_cluster_limit(const DeviceInfo& dev) {
+        static int cache[64] = {0};
+        int& c = cache[dev.device & 63];
+        if (c == 0) c = max_active_clusters(onchip(512, 16), 512, 16) > 0 ? 16 : 8;
+        return c;
+    }
+
+    static os_status plan(int64_t rows, int64_t cols, os_path path, os_plan* p) {
+        const DeviceInfo* dev = device_info();
+        if (!dev) return OS_ERR_CUDA;
+        const int64_t nv = ceil_div(cols, EPV);
+        const bool warp_ok = nv <= 256;
+        const int64_t cta_cap = int64_t(kOnchipThreadsMax) * VPT;
+        const bool onchip_ok = nv <= int64_t(onchip_cluster_limit(*dev)) * cta_cap;
+        if (path == OS_PATH_AUTO) path = warp_ok ? OS_PATH_WARP : onchip_ok ? OS_PATH_ONCHIP : OS_PATH_STREAM;
+        os_plan q = {};
+        q.path = path;
+        switch (path) {
+            case OS_PATH_WARP: {
+                if (!warp_ok) return OS_ERR_PATH;
+                q.vectors_per_thread = nv <= 128 ? 4 : 8;
+                q.lanes_per_row = q.vectors_per_thread == 8 ? 32 : pow2_at_least(ceil_div(nv, 4));
+                q.threads = kWarpThreads;
+                q.cluster = 1;
+                const int64_t rows_per_cta = kWarpThreads / q.lanes_per_row;
+                const int occ = blocks_per_sm(warp(q.lanes_per_row, q.vectors_per_thread), kWarpThreads);
+                q.grid = min64(ceil_div(rows, rows_per_cta), int64_t(dev->sms) * (occ > 0 ? occ : 1));
+                break;
+            }
+            case OS_PATH_ONCHIP: {
+                if (!onchip_ok) return OS_ERR_PATH;
+                q.vectors_per_thread = VPT;
+                if (nv <= cta_cap) {
+                    q.cluster = 1;
+                    q.threads = nv <= 128 * VPT ? 128 : nv <= 256 * VPT ? 256 : 512;
+                } else {
+                    q.cluster = pow2_at_least(ceil_div(nv, cta_cap));
+                    q.threads = kOnchipThreadsMax;
+                }
+                q.grid = min64(rows, kMaxClustersPerLaunch) * q.cluster;
+                break;
+            }
+            case OS_PATH_STREAM: {
+                q.threads = kStreamThreads;
+                q.vectors_per_thread = kStreamUnroll;
+                q.cluster = rows >= 2 * int64_t(dev->sms) ? 1 : 8;
+                q.grid = min64(rows, kMaxClustersPerLaunch) * q.cluster;
+                break;
+            }
+            default:
+                return OS_ERR_PATH;
+        }
+        *p = q;
+        return OS_OK;
+    }
+
+    static cudaError_t launch(const os_plan& p, const void* x, void* y, int64_t rows, int cols,
+                              bool aligned, cudaStream_t stream) {
+        const TI* xi = static_cast<const TI*>(x);
+        TO* yo = static_cast<TO*>(y);
+        const int al = aligned ? 1 : 0;
+        Kernel k = nullptr;
+        switch (p.path) {
+            case OS_PATH_WARP: k = warp(p.lanes_per_row, p.vectors_per_thread); break;
+            case OS_PATH_ONCHIP: k = onchip(p.threads, p.cluster); break;
+            default: k = streaming(p.cluster); break;
+        }
+        if (p.cluster > 8) {
+            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_kernel(k, p.grid, p.threads, p.cluster, stream, xi, yo, rows, cols, al);
+    }
+};
+
+}  // namespace os
+
+// One translation unit per dtype pair defines these two entry points.
+#define OS_DEFINE_SOFTMAX_PAIR(NAME, TI, TO)                                                   \
+    namespace os {                                                                             \
+    os_status plan_softmax_##NAME(int64_t rows, int64_t cols, os_path path, os_plan* p) {      \
+        return SoftmaxFamily<TI, TO>::plan(rows, cols, path, p);                               \
+    }                                                                                          \
+    cudaError_t launch_softmax_##NAME(const os_plan& p, const void* x, void* y, int64_t rows,  \
+                                      int cols, bool aligned, cudaStream_t stream) {           \
+        return SoftmaxFamily<TI, TO>::launch(p, x, y, rows, cols, aligned, stream);           \
+    }                                                                                          \
+    }

@@ -1,0 +1,132 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+function include/*.h declares, and rejects bad arguments before touching the
+device.  No kernel is launched here."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "softmax_topk_gb300", "lib", "libos_softmax.so")
+
+F32, BF16 = 0, 1
+OK, NULL, SHAPE, DTYPE, KERR, ALIAS, CUDA, TIMEOUT, PATH, ALIGN = range(10)
+
+
+def _ensure_built():
+    from softmax_topk_gb300 import build
+    build.build()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _ensure_built()
+    import softmax_topk_gb300 as st
+    return st._lib
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(os_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("os_softmax_fwd", "os_softmax_topk", "os_status_string"):
+        assert required in names, names
+
+
+def test_every_declared_function_is_exported(lib):
+    raw = ctypes.CDLL(LIB)
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    import softmax_topk_gb300 as st
+    for code, name in enumerate(st.STATUS):
+        assert st.os_status_string(code).startswith(name)
+    assert st.os_status_string(99) == "unknown os_status"
+
+
+A, B, C = 0x10000, 0x4000000, 0x8000000  # disjoint fake device addresses, 16-byte aligned
+
+
+def test_softmax_argument_errors(lib):
+    f = lib.os_softmax_fwd_path
+    assert f(A, B, 4, 8, 2, F32, 0, None) == DTYPE
+    assert f(A, B, 4, 8, F32, -1, 0, None) == DTYPE
+    assert f(A, B, -1, 8, F32, F32, 0, None) == SHAPE
+    assert f(A, B, 4, 0, F32, F32, 0, None) == SHAPE
+    assert f(A, B, 4, 2 ** 31, F32, F32, 0, None) == SHAPE
+    assert f(A, B, 2 ** 62, 2 ** 20, F32, F32, 0, None) == SHAPE
+    assert f(A, B, 4, 8, F32, F32, 7, None) == PATH
+    assert f(None, B, 4, 8, F32, F32, 0, None) == NULL
+    assert f(A, None, 4, 8, F32, F32, 0, None) == NULL
+    assert f(A + 2, B, 4, 8, F32, F32, 0, None) == ALIGN
+    assert f(A, B + 1, 4, 8, F32, BF16, 0, None) == ALIGN
+    assert f(A, A, 4, 8, F32, F32, 0, None) == ALIAS
+    assert f(A, A + 4 * 31, 4, 8, F32, F32, 0, None) == ALIAS     # last element shared
+    # rows == 0 is a no-op, even with NULL pointers
+    assert f(None, None, 0, 8, F32, F32, 0, None) == OK
+    assert lib.os_softmax_fwd(None, None, 0, 8, BF16, BF16, None) == OK
+
+
+def _no_device():
+    import torch
+    return not torch.cuda.is_available()
+
+
+# These two pass fake addresses that are only safe because no device exists:
+# with a GPU present they would launch on them, so they are skipped there.
+@pytest.mark.skipif(not _no_device(), reason="only meaningful (and only safe) without a GPU")
+def test_softmax_without_device_fails_loudly(lib):
+    # valid arguments but no GPU: the call reports a CUDA error, it never computes on the host
+    assert lib.os_softmax_fwd(A, A + 4 * 32, 4, 8, F32, F32, None) == CUDA
+
+
+def test_topk_argument_errors(lib):
+    f = lib.os_softmax_topk
+    assert f(A, B, C, 4, 100, 0, None) == KERR
+    assert f(A, B, C, 4, 100, 65, None) == KERR
+    assert f(A, B, C, 4, 5, 6, None) == KERR
+    assert f(A, B, C, 4, 0, 1, None) == SHAPE
+    assert f(A, B, C, -2, 100, 8, None) == SHAPE
+    assert f(None, B, C, 4, 100, 8, None) == NULL
+    assert f(A, None, C, 4, 100, 8, None) == NULL
+    assert f(A, B, None, 4, 100, 8, None) == NULL
+    assert f(A + 1, B, C, 4, 100, 8, None) == ALIGN
+    assert f(A, A + 16, C, 4, 100, 8, None) == ALIAS
+    assert f(A, B, B + 8, 4, 100, 8, None) == ALIAS
+    assert f(None, None, None, 0, 100, 8, None) == OK
+
+
+def test_exp_argument_errors(lib):
+    assert lib.os_exp_f32(A, B, -1, None) == SHAPE
+    assert lib.os_exp_f32(None, B, 5, None) == NULL
+    assert lib.os_exp_f32(A + 2, B, 5, None) == ALIGN
+    assert lib.os_exp_f32(None, None, 0, None) == OK
+
+
+def test_tensor_helpers_refuse_host_tensors(lib):
+    import torch
+
+    import softmax_topk_gb300 as st
+    with pytest.raises(ValueError):
+        st.softmax(torch.zeros(2, 3))
+    with pytest.raises(ValueError):
+        st.softmax_topk(torch.zeros(2, 3), 1)
+
+
+@pytest.mark.skipif(not _no_device(), reason="only meaningful without a GPU")
+def test_plan_without_device_reports_cuda_error(lib):
+    import softmax_topk_gb300 as st
+    with pytest.raises(st.OsError) as e:
+        st.os_softmax_plan(4, 1000, F32, F32)
+    assert e.value.name == "OS_ERR_CUDA"

@@ -1,0 +1,58 @@
+"""The library's own fp32 exponential against float64 exp and CUDA's expf."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+FLT_MIN = float(np.finfo(np.float32).tiny)
+
+
+@pytest.fixture(scope="module")
+def st():
+    import softmax_topk_gb300
+    return softmax_topk_gb300
+
+
+def _ulps(got: np.ndarray, want64: np.ndarray) -> np.ndarray:
+    ulp = np.spacing(want64.astype(np.float32)).astype(np.float64)
+    return np.abs(got.astype(np.float64) - want64) / ulp
+
+
+def test_error_bound_on_the_softmax_domain(st):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    z = torch.cat([-torch.rand(1 << 22, generator=g, device="cuda") * 87.33,
+                   -torch.rand(1 << 20, generator=g, device="cuda") * 2.0,
+                   -torch.rand(1 << 16, generator=g, device="cuda") * 1e-3,
+                   torch.linspace(-87.33, 0.0, 1 << 20, device="cuda")])
+    got = st.exp(z)
+    torch.cuda.synchronize()
+    z64 = z.double().cpu().numpy()
+    want = np.exp(z64)
+    ulps = _ulps(got.cpu().numpy(), want)
+    assert ulps.max() <= 2.0, f"max {ulps.max():.3f} ulp at z={z64[np.argmax(ulps)]}"
+    cuda = torch.exp(z).cpu().numpy()          # CUDA's expf on the same inputs
+    assert _ulps(cuda, want).max() <= 2.0
+    diff = np.abs(got.cpu().numpy().astype(np.float64) - cuda) / want
+    assert diff.max() <= 3 * 2.0 ** -23
+
+
+def test_special_values(st):
+    z = torch.tensor([0.0, -0.0, -np.inf, -88.0, -87.5, -100.0, -1e30, -87.33, 1.0, 10.0, 88.0],
+                     device="cuda")
+    got = st.exp(z).cpu().numpy()
+    assert got[0] == 1.0 and got[1] == 1.0
+    assert got[2] == 0.0 and not np.signbit(got[2])
+    assert 0.0 <= got[3] <= FLT_MIN and 0.0 <= got[4] <= FLT_MIN
+    assert got[5] == 0.0 and got[6] == 0.0
+    assert got[7] >= FLT_MIN
+    want = np.exp(np.array([1.0, 10.0, 88.0]))
+    assert np.all(_ulps(got[8:], want) <= 2.0)
+
+
+def test_in_place(st):
+    z = -torch.rand(1000, device="cuda") * 50
+    ref = st.exp(z)
+    st.os_exp_f32(z.data_ptr(), z.data_ptr(), z.numel(), torch.cuda.current_stream().cuda_stream)
+    assert torch.equal(z, ref)

@@ -1,0 +1,231 @@
+"""Softmax parity on the GPU: every kernel family against the float64 oracle.
+
+Small shapes sweep the column counts that cross every dispatch boundary and
+ragged tail (vector width, warp, CTA and cluster capacities); the workload
+recipes run scaled down on all rows, and at full size on sampled rows plus
+properties checked on every row.  Tolerances: fp32 output 1e-5 relative,
+bf16 output 8e-3 relative (tests/_compare.py states the full rule).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._compare import FLT_MIN, SUM_TOL, assert_softmax_close
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+PAIRS = [("f32", "f32"), ("bf16", "bf16"), ("f32", "bf16"), ("bf16", "f32")]
+PATHS = ["auto", "warp", "onchip", "stream"]
+COLS = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256,
+        257, 511, 512, 513, 1023, 1024, 1025, 2047, 2048, 2049, 4095, 4096, 4097, 8191, 8192,
+        8193, 16383, 16384, 16385, 32000, 32768, 32769, 50257, 65535, 65536, 65537, 128256,
+        131072, 131073, 262144, 262145, 524288, 524289]
+
+
+@pytest.fixture(scope="module")
+def st():
+    import softmax_topk_gb300
+    return softmax_topk_gb300
+
+
+def _inputs(rows, cols, dtype, seed, scale=3.0, neg_inf_p=0.02):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g, device="cuda") * scale
+    if cols > 2:
+        x.masked_fill_(torch.rand(rows, cols, generator=g, device="cuda") < neg_inf_p, -np.inf)
+        x[:, (seed * 7919) % cols] = 0.5  # at least one finite entry per row
+    return x.to(DT[dtype])
+
+
+def _check(st, x, out, path, label):
+    try:
+        y = st.softmax(x, out_dtype=DT[out], path=path)
+    except st.OsError as e:
+        if e.name == "OS_ERR_PATH":
+            pytest.skip(f"{path} cannot hold {tuple(x.shape)}")
+        raise
+    torch.cuda.synchronize()
+    x64 = x.double().cpu().numpy()
+    ref = oracle.softmax(x64)
+    return assert_softmax_close(x64, y.double().cpu().numpy(), ref, out, label)
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+def test_cols_sweep_auto(st, cols, pair):
+    rows = 3 if cols > 100000 else 5
+    x = _inputs(rows, cols, pair[0], seed=cols)
+    _check(st, x, pair[1], "auto", f"auto {pair} cols={cols}")
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("path", ["warp", "onchip", "stream"])
+@pytest.mark.parametrize("pair", [("f32", "f32"), ("bf16", "bf16")], ids=lambda p: f"{p[0]}-{p[1]}")
+def test_cols_sweep_forced_path(st, cols, path, pair):
+    rows = 3 if cols > 100000 else 6
+    x = _inputs(rows, cols, pair[0], seed=cols + 17)
+    _check(st, x, pair[1], path, f"{path} {pair} cols={cols}")
+
+
+SOFTMAX_WORKLOADS = [n for n, w in workloads.WORKLOADS.items() if w.op == "softmax"]
+
+
+@pytest.mark.parametrize("name", SOFTMAX_WORKLOADS)
+@pytest.mark.parametrize("path", PATHS)
+def test_workload_recipe_scaled(st, name, path):
+    w = workloads.WORKLOADS[name]
+    rows = min(w.rows, 300 if w.cols <= 4096 else 24)
+    x = workloads.make(w.scaled(rows=rows), device="cuda")
+    _check(st, x, w.dtype, path, f"{name} x{rows} rows, {path}")
+
+
+@pytest.mark.parametrize("name", SOFTMAX_WORKLOADS)
+def test_workload_full_size_sampled(st, name):
+    """Full-size input, the launch the benchmark times; oracle on sampled rows,
+    row sums and ranges on every row, and a bit-identical second run."""
+    w = workloads.WORKLOADS[name]
+    x = workloads.make(w, device="cuda")
+    y = st.softmax(x)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(w.seed)
+    sample = np.unique(np.concatenate([[0, w.rows - 1], rng.choice(w.rows, 48, replace=False)]))
+    xs = x[torch.from_numpy(sample).cuda()].double().cpu().numpy()
+    ys = y[torch.from_numpy(sample).cuda()].double().cpu().numpy()
+    assert_softmax_close(xs, ys, oracle.softmax(xs), w.dtype, f"{name} sampled rows")
+    sums = y.double().sum(dim=1)
+    assert float((sums - 1).abs().max()) <= SUM_TOL[w.dtype]
+    assert float(y.min()) >= 0.0 and float(y.max()) <= 1.0
+    assert int(torch.isnan(y).sum()) == 0
+    if name.startswith("causal"):  # rows r with r % 128 == 0 have one finite entry
+        assert torch.all(y[::128, 0] == 1.0) and torch.all(y[::128, 1:] == 0)
+    y2 = st.softmax(x)
+    assert torch.equal(y, y2), "two runs on the same input differ"
+
+
+def test_edge_rows(st):
+    n = 4099
+    rows = []
+    for pos in (0, 1, 2047, n - 1):
+        r = np.full(n, -np.inf)
+        r[pos] = 3.0
+        rows.append(r)                              # all but one -inf
+    r = np.linspace(-5, 5, n)
+    r[:100] = -np.inf
+    rows.append(r)                                  # -inf first, then increasing
+    r = np.random.default_rng(1).normal(size=n) * 3
+    r[[3, 900, 2000, 4098]] = 40.0
+    rows.append(r)                                  # four exact spikes
+    rows.append(np.full(n, -7.25))                  # constant
+    r = np.random.default_rng(2).normal(size=n)
+    r[10] = 1e30
+    r[11] = -1e30
+    rows.append(r)                                  # huge magnitudes
+    rows.append(np.arange(n, dtype=np.float64) * 1e-3)  # strictly increasing
+    x64 = np.stack(rows)
+    for dtype in ("f32", "bf16"):
+        x = torch.tensor(x64).to(DT[dtype]).cuda()
+        for path in PATHS:
+            try:
+                y = st.softmax(x, path=path)
+            except st.OsError as e:
+                assert e.name == "OS_ERR_PATH"
+                continue
+            torch.cuda.synchronize()
+            xx = x.double().cpu().numpy()
+            assert_softmax_close(xx, y.double().cpu().numpy(), oracle.softmax(xx), dtype,
+                                 f"edge rows {dtype} {path}")
+
+
+def test_single_column_and_spike_ties(st):
+    x = torch.randn(1000, 1, device="cuda")
+    assert torch.all(st.softmax(x) == 1.0)
+    w = workloads.WORKLOADS["softmax_8192x128256_bf16"].scaled(rows=8)
+    x = workloads.make(w, device="cuda")
+    y = st.softmax(x).float()
+    spikes = x.float() == 40.0
+    per_row = y.masked_fill(~spikes, 0)
+    for r in range(8):
+        vals = per_row[r][spikes[r]]
+        assert vals.numel() == 4 and torch.all(vals == vals[0]), vals
+
+
+def test_all_neg_inf_row_does_not_disturb_others(st):
+    x = torch.randn(6, 3000, device="cuda")
+    x[2] = -np.inf
+    y = st.softmax(x)
+    torch.cuda.synchronize()
+    keep = [0, 1, 3, 4, 5]
+    xx = x[keep].double().cpu().numpy()
+    assert_softmax_close(xx, y[keep].double().cpu().numpy(), oracle.softmax(xx), "f32", "others")
+
+
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+@pytest.mark.parametrize("cols", [100, 4096, 30000, 100000])
+def test_misaligned_pointers(st, pair, cols):
+    """Buffers starting 1 element past a 16-byte boundary take the element-wise path."""
+    rows = 4
+    xin, xout = DT[pair[0]], DT[pair[1]]
+    xbuf = torch.empty(rows * cols + 8, dtype=xin, device="cuda")
+    ybuf = torch.zeros(rows * cols + 8, dtype=xout, device="cuda")
+    x = xbuf[1:1 + rows * cols].view(rows, cols)
+    x.copy_(_inputs(rows, cols, pair[0], seed=5))
+    y = ybuf[1:1 + rows * cols].view(rows, cols)
+    in_code = 0 if pair[0] == "f32" else 1
+    out_code = 0 if pair[1] == "f32" else 1
+    st.os_softmax_fwd(x.data_ptr(), y.data_ptr(), rows, cols, in_code, out_code,
+                      torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    xx = x.double().cpu().numpy()
+    assert_softmax_close(xx, y.double().cpu().numpy(), oracle.softmax(xx), pair[1], "misaligned")
+    assert float(ybuf[0]) == 0.0 and torch.all(ybuf[1 + rows * cols:] == 0)
+
+
+@pytest.mark.parametrize("cols", [128, 1024, 4096, 32000, 128256, 300000])
+def test_output_guard_bands_untouched(st, cols):
+    rows = 7
+    guard = 4096
+    x = _inputs(rows, cols, "f32", seed=9)
+    buf = torch.full((2 * guard + rows * cols,), 12345.0, device="cuda")
+    y = buf[guard:guard + rows * cols].view(rows, cols)
+    st.softmax(x, out=y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:guard] == 12345.0) and torch.all(buf[guard + rows * cols:] == 12345.0)
+    xx = x.double().cpu().numpy()
+    assert_softmax_close(xx, y.double().cpu().numpy(), oracle.softmax(xx), "f32", "guarded")
+
+
+def test_side_stream(st):
+    s = torch.cuda.Stream()
+    x = _inputs(64, 32000, "f32", seed=3)
+    with torch.cuda.stream(s):
+        y = st.softmax(x)
+    s.synchronize()
+    xx = x.double().cpu().numpy()
+    assert_softmax_close(xx, y.double().cpu().numpy(), oracle.softmax(xx), "f32", "side stream")
+
+
+def test_plans_of_the_workloads(st):
+    p = st.plan((4096, 32000), st.OS_F32)
+    assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 2
+    p = st.plan((8192, 128256), st.OS_BF16)
+    assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 8
+    p = st.plan((1048576, 128), st.OS_F32)
+    assert p["path"] == st.OS_PATH_WARP and p["lanes_per_row"] == 8
+    p = st.plan((65536, 4096), st.OS_F32)
+    assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 1 and p["threads"] == 128
+    with pytest.raises(st.OsError):
+        st.plan((10, 5000), st.OS_F32, path="warp")
+
+
+def test_bad_calls_raise(st):
+    x = torch.randn(4, 100, device="cuda")
+    with pytest.raises(st.OsError) as e:
+        st.os_softmax_fwd(x.data_ptr(), x.data_ptr(), 4, 100, 0, 0, None)
+    assert e.value.name == "OS_ERR_ALIAS"
+    with pytest.raises(st.OsError) as e:
+        st.softmax(torch.randn(2, 5000, device="cuda"), path="warp")
+    assert e.value.name == "OS_ERR_PATH"

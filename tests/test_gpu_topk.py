@@ -1,0 +1,134 @@
+"""Fused softmax+TopK parity on the GPU against the float64 oracle.
+
+Indices must match bit for bit (ties go to the lower column index); values
+within 1e-5 relative (values below FLT_MIN: in [0, FLT_MIN]).  Shapes cross
+the tile and cluster capacities, rows start at every 4-byte offset inside a
+16-byte vector, and crafted inputs drive the candidate-overflow path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._compare import assert_topk_equal
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def st():
+    import softmax_topk_gb300
+    return softmax_topk_gb300
+
+
+def _run(st, x, K, label):
+    vals, idx = st.softmax_topk(x, K)
+    torch.cuda.synchronize()
+    rv, ri = oracle.topk(x.double().cpu().numpy(), K)
+    assert_topk_equal(vals.cpu().numpy(), idx.cpu().numpy(), rv, ri, label)
+
+
+def _rand(rows, cols, seed, scale=4.0):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randn(rows, cols, generator=g, device="cuda") * scale
+
+
+COLS = [1, 2, 3, 5, 8, 63, 64, 65, 100, 1000, 4097, 8191, 8192, 8193, 16387, 32771, 50257,
+        65539, 100003, 300007]
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("K", [1, 2, 7, 8, 33, 64])
+def test_shapes(st, cols, K):
+    if K > cols:
+        pytest.skip("K > cols")
+    rows = 3 if cols > 100000 else 9     # 9 rows: every start offset mod 16 bytes occurs
+    _run(st, _rand(rows, cols, seed=cols * 131 + K), K, f"cols={cols} K={K}")
+
+
+@pytest.mark.parametrize("K", [8, 64])
+def test_workload_full_size(st, K):
+    w = workloads.WORKLOADS["topk_256x50257_f32"]
+    x = workloads.make(w, device="cuda")
+    _run(st, x, K, f"{w.name} K={K}")
+
+
+@pytest.mark.parametrize("K", [8, 64])
+def test_workload_with_planted_ties(st, K):
+    w = workloads.WORKLOADS["topk_256x50257_f32"]
+    x = workloads.plant_ties(workloads.make(w.scaled(rows=64), device="cuda"), per_row=K // 2 + 3)
+    _run(st, x, K, f"ties K={K}")
+
+
+@pytest.mark.parametrize("cols", [100, 5000, 50257])
+def test_coarse_values_many_ties(st, cols):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cols)
+    x = torch.randint(0, 4, (6, cols), generator=g, device="cuda").float()
+    for K in (1, 8, 64):
+        if K <= cols:
+            _run(st, x, K, f"values in 0..3, cols={cols} K={K}")
+
+
+@pytest.mark.parametrize("cols", [70, 9000, 50257, 200000])
+def test_constant_rows_overflow_path(st, cols):
+    """Every entry ties: the threshold admits far more than the candidate
+    buffer holds, so the kernel merges in several passes."""
+    x = torch.full((3, cols), 2.5, device="cuda")
+    for K in (8, 64):
+        _run(st, x, K, f"constant cols={cols} K={K}")
+
+
+def test_fewer_finite_than_k(st):
+    x = torch.full((4, 5000), -np.inf, device="cuda")
+    x[0, 4999] = 1.0
+    x[1, [0, 17, 4000]] = torch.tensor([0.5, 0.5, -2.0], device="cuda")
+    x[2, 100:110] = torch.arange(10, dtype=torch.float32, device="cuda")
+    x[3, 1] = 3.0
+    _run(st, x, 64, "few finite entries")
+
+
+def test_increasing_and_decreasing_rows(st):
+    up = torch.arange(60000, dtype=torch.float32, device="cuda")[None, :] * 1e-3
+    x = torch.cat([up, up.flip(1), -up]).contiguous()
+    for K in (8, 64):
+        _run(st, x, K, f"monotone K={K}")
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_base(st, offset):
+    rows, cols, K = 5, 50257, 64
+    buf = torch.empty(rows * cols + 8, device="cuda")
+    x = buf[offset:offset + rows * cols].view(rows, cols)
+    x.copy_(_rand(rows, cols, seed=offset))
+    vals = torch.empty(rows, K, device="cuda")
+    idx = torch.empty(rows, K, dtype=torch.int32, device="cuda")
+    st.os_softmax_topk(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, cols, K,
+                       torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    rv, ri = oracle.topk(x.double().cpu().numpy(), K)
+    assert_topk_equal(vals.cpu().numpy(), idx.cpu().numpy(), rv, ri, f"offset {offset}")
+
+
+def test_many_rows_short(st):
+    _run(st, _rand(5000, 40, seed=3), 16, "5000 x 40")
+
+
+def test_values_equal_softmax_output(st):
+    x = _rand(16, 32000, seed=11)
+    vals, idx = st.softmax_topk(x, 64)
+    y = st.softmax(x)
+    picked = torch.gather(y, 1, idx.long())
+    rel = ((picked.double() - vals.double()).abs() / vals.double()).max()
+    assert float(rel) <= 2e-5
+
+
+def test_bad_k_raises(st):
+    x = _rand(2, 100, seed=1)
+    with pytest.raises(st.OsError) as e:
+        st.softmax_topk(x, 65)
+    assert e.value.name == "OS_ERR_K"
+    with pytest.raises(st.OsError):
+        st.softmax_topk(_rand(2, 10, seed=1), 11)
