@@ -16,8 +16,8 @@ OK, NULL, SHAPE, DTYPE, KERR, ALIAS, CUDA, TIMEOUT, PATH, ALIGN = range(10)
 
 
 def _ensure_built():
-    from softmax_topk_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._builder().build()
 
 
 @pytest.fixture(scope="module")
