@@ -464,6 +464,43 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_only(args):
+    """One workload, optionally on fewer rows: a small, self-contained case for
+    profilers (prints a short JSON line; not a benchmark result)."""
+    import softmax_topk_gb300 as st
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.only]
+    if args.rows:
+        w = w.scaled(rows=args.rows)
+    x = workloads.make(w, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    if w.op == "softmax":
+        y = torch.empty_like(x)
+        fn = lambda: st.softmax(x, out=y, path=args.path)  # noqa: E731
+        nbytes = softmax_bytes(w)
+    else:
+        vals = torch.empty(w.rows, args.K, device=dev)
+        idx = torch.empty(w.rows, args.K, dtype=torch.int32, device=dev)
+        fn = lambda: st.softmax_topk(x, args.K, vals=vals, idx=idx)  # noqa: E731
+        nbytes = topk_bytes(w, args.K)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    print(json.dumps({"only": w.name, "rows": w.rows, "cols": w.cols, "path": args.path,
+                      "K": args.K if w.op == "topk" else None, "ms": round(ms, 5),
+                      "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "note": "inputs not rotated: L2-resident when small"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -473,10 +510,16 @@ def main():
     ap.add_argument("--extra", action="store_true", help="also time the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--only", default=None, help="time one workload by name (profiling case)")
+    ap.add_argument("--rows", type=int, default=0, help="with --only: number of rows")
+    ap.add_argument("--K", type=int, default=64, help="with --only on the TopK workload")
+    ap.add_argument("--path", default="auto", help="with --only: softmax kernel family")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.only:
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
