@@ -305,7 +305,10 @@ def kernel_of(st, label: str) -> str:
     p = st.plan((w.rows, w.cols), code)
     fam = {st.OS_PATH_WARP: "warp_rows_kernel", st.OS_PATH_ONCHIP: "onchip_rows_kernel",
            st.OS_PATH_STREAM: "stream_rows_kernel"}[p["path"]]
-    return f"{fam}<{w.dtype},{w.dtype},threads={p['threads']},cluster={p['cluster']}>"
+    if p["path"] == st.OS_PATH_ONCHIP and p["stages"] > 0:
+        fam = "tma_rows_kernel"
+    return (f"{fam}<{w.dtype},{w.dtype},threads={p['threads']},cluster={p['cluster']},"
+            f"stages={p['stages']}>")
 
 
 def run_e2e(st, dev, args):

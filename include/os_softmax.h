@@ -57,7 +57,7 @@ typedef enum {
     OS_ERR_K = 4,       /* K outside [1, min(cols, 64)] */
     OS_ERR_ALIAS = 5,   /* an output overlaps an input or another output */
     OS_ERR_CUDA = 6,    /* the CUDA runtime reported an error (launch or device query) */
-    OS_ERR_TIMEOUT = 7, /* reserved: a device-side bounded wait gave up */
+    OS_ERR_TIMEOUT = 7, /* a device-side bounded wait gave up (os_device_status) */
     OS_ERR_PATH = 8,    /* the requested kernel family cannot run this shape */
     OS_ERR_ALIGN = 9    /* a pointer is not aligned to its element size */
 } os_status;
@@ -79,7 +79,8 @@ typedef struct {
     int32_t vectors_per_thread; /* 16-byte input vectors held per thread (per chunk for STREAM) */
     int32_t cluster;            /* CTAs per row (thread-block cluster size), 1 if none */
     int32_t lanes_per_row;      /* WARP path: lanes that share one row; else 0 */
-    int32_t reserved;
+    int32_t stages;             /* ONCHIP path with bulk-copy staging: row slices
+                                   prefetched in shared memory; 0 = registers only */
     int64_t grid;               /* CTAs launched */
 } os_plan;
 
@@ -128,7 +129,8 @@ os_status os_softmax_fwd_path(const void *x, void *y, int64_t rows, int64_t cols
 /*
  * The launch configuration os_softmax_fwd_path would use for this shape on the
  * current device, written to *plan; nothing is launched.  Same argument
- * checks as the launching call, minus the pointer checks.
+ * checks as the launching call, minus the pointer checks; x and y are assumed
+ * 16-byte aligned (the choice can differ for other pointers).
  */
 os_status os_softmax_plan(int64_t rows, int64_t cols, os_dtype in_dtype, os_dtype out_dtype,
                           os_path path, os_plan *plan);
@@ -146,6 +148,31 @@ os_status os_topk_plan(int64_t rows, int64_t cols, int32_t K, os_plan *plan);
  *   z, out  device pointers to n fp32 values (may be the same buffer).
  */
 os_status os_exp_f32(const float *z, float *out, int64_t n, os_stream_t stream);
+
+/*
+ * Device-side waits.  Kernels that stage rows in shared memory wait on
+ * hardware barriers for their bulk copies; every such wait is bounded (by
+ * default 1 s).  A wait that gives up does not hang or fault the GPU: the
+ * kernel finishes with garbage in the affected outputs and records the event
+ * in a per-device status word.
+ *
+ * os_device_status synchronises `stream`, then returns OS_ERR_TIMEOUT if any
+ * kernel of this library on the current device gave up a wait since the
+ * previous call (and clears the word), OS_OK otherwise.
+ */
+os_status os_device_status(os_stream_t stream);
+
+/*
+ * Testing controls, process-wide, read at every launch.
+ *   os_set_wait_timeout_ns: bound of each device-side wait, 1 us .. 10 s
+ *     (OS_ERR_SHAPE outside that range).
+ *   os_set_fault_injection: 0 = off (default); 1 = in every following launch
+ *     the first CTA never issues its first bulk copy, so its wait must run out
+ *     (exercises the bounded-wait path; the outputs of that launch are
+ *     garbage).  Other values: OS_ERR_SHAPE.
+ */
+os_status os_set_wait_timeout_ns(uint64_t ns);
+os_status os_set_fault_injection(int32_t mode);
 
 #ifdef __cplusplus
 }

@@ -2,7 +2,8 @@
 
 The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
 ``os_softmax_fwd``, ``os_softmax_topk``, ``os_softmax_fwd_path``,
-``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_status_string``.  They take raw
+``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_device_status``,
+``os_set_wait_timeout_ns``, ``os_set_fault_injection``, ``os_status_string``.  They take raw
 device pointers (ints) and a raw stream handle, exactly like the C functions,
 and raise ``OsError`` on a non-OK status.
 
@@ -42,11 +43,11 @@ class OsError(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("vectors_per_thread", ctypes.c_int32), ("cluster", ctypes.c_int32),
-                ("lanes_per_row", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("lanes_per_row", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("grid", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 def _load() -> ctypes.CDLL:
@@ -63,10 +64,14 @@ def _load() -> ctypes.CDLL:
     lib.os_softmax_plan.argtypes = [i64, i64, st, st, st, ctypes.POINTER(Plan)]
     lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
     lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
+    lib.os_device_status.argtypes = [vp]
+    lib.os_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.os_set_fault_injection.argtypes = [i32]
     lib.os_status_string.argtypes = [st]
     lib.os_status_string.restype = ctypes.c_char_p
     for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_softmax_plan",
-                 "os_topk_plan", "os_exp_f32"):
+                 "os_topk_plan", "os_exp_f32", "os_device_status", "os_set_wait_timeout_ns",
+                 "os_set_fault_injection"):
         getattr(lib, name).restype = st
     return lib
 
@@ -102,6 +107,20 @@ def os_softmax_topk(x: int, vals: int, idx: int, rows: int, cols: int, K: int,
 
 def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
     _check(_lib.os_exp_f32(z, out, n, stream), "os_exp_f32")
+
+
+def os_device_status(stream: int | None) -> None:
+    """Synchronise `stream`; raise OsError(OS_ERR_TIMEOUT) if a device-side
+    wait gave up since the last call."""
+    _check(_lib.os_device_status(stream), "os_device_status")
+
+
+def os_set_wait_timeout_ns(ns: int) -> None:
+    _check(_lib.os_set_wait_timeout_ns(int(ns)), "os_set_wait_timeout_ns")
+
+
+def os_set_fault_injection(mode: int) -> None:
+    _check(_lib.os_set_fault_injection(int(mode)), "os_set_fault_injection")
 
 
 def os_softmax_plan(rows: int, cols: int, in_dtype: int, out_dtype: int, path: int = 0) -> dict:

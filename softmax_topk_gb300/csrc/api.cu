@@ -1,16 +1,52 @@
 // api.cu -- the C ABI declared in include/os_softmax.h: argument checks, kernel
 // choice per dtype pair, launch on the caller's stream.  No allocation, no
 // synchronisation, no host fallback.
+#include <atomic>
 #include <cstdint>
 
 #include "host_common.h"
 #include "internal.h"
 
+// Device status word (one per device the library runs on): kernels OR in
+// os::kErrWaitTimeout when a bounded wait gives up.  Read and cleared by
+// os_device_status.
+__device__ unsigned int os_device_status_word;
+
 namespace {
 
-using PlanFn = os_status (*)(int64_t, int64_t, os_path, os_plan*);
+std::atomic<unsigned long long> g_timeout_ns{1000000000ull};  // 1 s per wait
+std::atomic<int> g_fault{0};
+
+// Address of this device's status word (host code cannot use the symbol
+// itself as a device pointer), looked up once per device.
+unsigned int* status_word() {
+    constexpr int kMaxDevices = 64;
+    static unsigned int* cache[kMaxDevices] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, os_device_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cache[dev] = static_cast<unsigned int*>(p);
+    }
+    return cache[dev];
+}
+
+bool make_ctl(os::KernelCtl* ctl) {
+    ctl->err = status_word();
+    ctl->timeout_ns = g_timeout_ns.load();
+    ctl->fault = g_fault.load();
+    return ctl->err != nullptr;
+}
+
+using PlanFn = os_status (*)(int64_t, int64_t, os_path, bool, os_plan*);
 using LaunchFn = cudaError_t (*)(const os_plan&, const void*, void*, int64_t, int, bool,
-                                 cudaStream_t);
+                                 const os::KernelCtl&, cudaStream_t);
 
 struct Pair {
     PlanFn plan;
@@ -78,7 +114,7 @@ os_status os_softmax_plan(int64_t rows, int64_t cols, os_dtype in, os_dtype out,
     const os_status st = softmax_checks(rows, cols, in, out, path);
     if (st != OS_OK) return st;
     if (!plan) return OS_ERR_NULL;
-    return kPairs[in][out].plan(rows, cols, path, plan);
+    return kPairs[in][out].plan(rows, cols, path, true, plan);
 }
 
 os_status os_softmax_fwd_path(const void* x, void* y, int64_t rows, int64_t cols, os_dtype in,
@@ -92,14 +128,16 @@ os_status os_softmax_fwd_path(const void* x, void* y, int64_t rows, int64_t cols
         return OS_ERR_ALIGN;
     if (overlaps(x, rows * cols * elem_bytes(in), y, rows * cols * elem_bytes(out)))
         return OS_ERR_ALIAS;
+    const bool ptrs_aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                              reinterpret_cast<uintptr_t>(y) % 16 == 0;
     os_plan plan;
-    st = kPairs[in][out].plan(rows, cols, path, &plan);
+    st = kPairs[in][out].plan(rows, cols, path, ptrs_aligned, &plan);
     if (st != OS_OK) return st;
-    const bool aligned = cols % elems_per_vector(in) == 0 &&
-                         reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
-                         reinterpret_cast<uintptr_t>(y) % 16 == 0;
+    os::KernelCtl ctl;
+    if (!make_ctl(&ctl)) return OS_ERR_CUDA;
+    const bool aligned = ptrs_aligned && cols % elems_per_vector(in) == 0;
     const cudaError_t e = kPairs[in][out].launch(plan, x, y, rows, static_cast<int>(cols), aligned,
-                                                 reinterpret_cast<cudaStream_t>(stream));
+                                                 ctl, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
 }
 
@@ -130,8 +168,10 @@ os_status os_softmax_topk(const float* x, float* vals, int32_t* idx, int64_t row
     os_plan plan;
     st = os::plan_topk(rows, cols, K, &plan);
     if (st != OS_OK) return st;
+    os::KernelCtl ctl;
+    if (!make_ctl(&ctl)) return OS_ERR_CUDA;
     const cudaError_t e = os::launch_topk(plan, x, vals, idx, rows, static_cast<int>(cols), K,
-                                          reinterpret_cast<cudaStream_t>(stream));
+                                          ctl, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
 }
 
@@ -143,6 +183,32 @@ os_status os_exp_f32(const float* z, float* out, int64_t n, os_stream_t stream) 
         return OS_ERR_ALIGN;
     const cudaError_t e = os::launch_exp(z, out, n, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
+}
+
+os_status os_device_status(os_stream_t stream) {
+    unsigned int* word = status_word();
+    if (!word) return OS_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return OS_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return OS_ERR_CUDA;
+    if (v == 0) return OS_OK;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return OS_ERR_CUDA;
+    return (v & os::kErrWaitTimeout) ? OS_ERR_TIMEOUT : OS_ERR_CUDA;
+}
+
+os_status os_set_wait_timeout_ns(uint64_t ns) {
+    if (ns < 1000 || ns > 10000000000ull) return OS_ERR_SHAPE;
+    g_timeout_ns.store(ns);
+    return OS_OK;
+}
+
+os_status os_set_fault_injection(int32_t mode) {
+    if (mode != 0 && mode != os::kFaultSkipFirstLoad) return OS_ERR_SHAPE;
+    g_fault.store(mode);
+    return OS_OK;
 }
 
 }  // extern "C"

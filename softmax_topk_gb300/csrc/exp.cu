@@ -15,7 +15,7 @@ cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t strea
     const DeviceInfo* dev = device_info();
     if (!dev) return cudaErrorNoDevice;
     const int64_t grid = min64(ceil_div(n, 256), int64_t(dev->sms) * 8);
-    return launch_kernel(exp_kernel, grid, 256, 1, stream, z, out, n);
+    return launch_kernel(exp_kernel, grid, 256, 1, 0, stream, z, out, n);
 }
 
 }  // namespace os

@@ -38,11 +38,11 @@ inline const DeviceInfo* device_info() {
 // Launch `kernel` with `cluster` CTAs per thread-block cluster (1 = none).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), int64_t grid, int threads, int cluster,
-                          cudaStream_t stream, Args... args) {
+                          int smem, cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (cluster > 1) {
@@ -56,20 +56,33 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), int64_t grid, int threads, i
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// How many clusters of `cluster` CTAs of `kernel` can be resident at once on
-// the current device (0 if the size cannot be launched).  Cluster sizes above
-// 8 are opted into first (non-portable sizes).
+// Opt `kernel` into `smem` bytes of dynamic shared memory and, for cluster
+// sizes above 8, into non-portable cluster sizes.  Returns false on failure.
 template <typename... KArgs>
-int max_active_clusters(void (*kernel)(KArgs...), int threads, int cluster) {
-    if (cluster > 8 &&
-        cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+bool prepare_kernel(void (*kernel)(KArgs...), int cluster, int smem) {
+    const void* k = reinterpret_cast<const void*>(kernel);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
         cudaGetLastError();
-        return 0;
+        return false;
     }
+    if (cluster > 8 &&
+        cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
+// How many clusters of `cluster` CTAs of `kernel` can be resident at once on
+// the current device (0 if the size cannot be launched).
+template <typename... KArgs>
+int max_active_clusters(void (*kernel)(KArgs...), int threads, int cluster, int smem = 0) {
+    if (!prepare_kernel(kernel, cluster, smem)) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
@@ -87,10 +100,11 @@ int max_active_clusters(void (*kernel)(KArgs...), int threads, int cluster) {
 }
 
 template <typename... KArgs>
-int blocks_per_sm(void (*kernel)(KArgs...), int threads) {
+int blocks_per_sm(void (*kernel)(KArgs...), int threads, int smem = 0) {
     int n = 0;
+    if (!prepare_kernel(kernel, 1, smem)) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void*>(kernel),
-                                                      threads, 0) != cudaSuccess) {
+                                                      threads, smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

@@ -7,13 +7,16 @@
 #include <cstdint>
 
 #include "../../include/os_softmax.h"
+#include "ctl.h"
 
 namespace os {
 
 #define OS_DECLARE_SOFTMAX_PAIR(NAME)                                                          \
-    os_status plan_softmax_##NAME(int64_t rows, int64_t cols, os_path path, os_plan* p);       \
+    os_status plan_softmax_##NAME(int64_t rows, int64_t cols, os_path path, bool aligned,      \
+                                  os_plan* p);                                                 \
     cudaError_t launch_softmax_##NAME(const os_plan& p, const void* x, void* y, int64_t rows,  \
-                                      int cols, bool aligned, cudaStream_t stream);
+                                      int cols, bool aligned, const KernelCtl& ctl,            \
+                                      cudaStream_t stream);
 
 OS_DECLARE_SOFTMAX_PAIR(f32_f32)
 OS_DECLARE_SOFTMAX_PAIR(bf16_bf16)
@@ -22,7 +25,7 @@ OS_DECLARE_SOFTMAX_PAIR(bf16_f32)
 
 os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p);
 cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* idx,
-                        int64_t rows, int cols, int K, cudaStream_t stream);
+                        int64_t rows, int cols, int K, const KernelCtl& ctl, cudaStream_t stream);
 
 cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t stream);
 

@@ -178,14 +178,22 @@ struct RowMergeSmem {
     float2 slot[2][CLUSTER];
 };
 
-template <int THREADS, int CLUSTER>
+struct NoHook {
+    __device__ void operator()() const {}
+};
+
+// `after_barrier` runs right after the CTA-wide barrier that follows every
+// thread's contribution (the TMA kernel refills its stage there).
+template <int THREADS, int CLUSTER, bool HOOK = false, typename Hook = NoHook>
 __device__ __forceinline__ float2 merge_row_state(RowMergeSmem<THREADS, CLUSTER>& sm, float m,
-                                                  float d, int parity, uint32_t rank) {
+                                                  float d, int parity, uint32_t rank,
+                                                  Hook after_barrier = Hook()) {
     constexpr int NW = THREADS / 32;
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     group_merge<32>(m, d);
     if (lane == 0) sm.warp_state[warp] = make_float2(m, d);
     __syncthreads();
+    if (HOOK) after_barrier();
     if (warp == 0) {
         float2 s = lane < NW ? sm.warp_state[lane] : make_float2(kNegInf, 0.f);
         group_merge<32>(s.x, s.y);
@@ -251,6 +259,113 @@ onchip_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
             const int64_t v = v0 + int64_t(k) * THREADS;
             if (v < nv) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// tma_rows: persistent clusters with a ring of STAGES row slices in shared
+// memory, filled by bulk copies (cp.async.bulk) STAGES-1 rows ahead of the row
+// being computed, so HBM reads stay in flight while a row is reduced, merged
+// and written.  Cluster `c` of G processes rows c, c+G, c+2G, ...; CTA `rank`
+// of the cluster owns the contiguous slice [rank*S, rank*S + S) of every row
+// (S = ceil(cols / CLUSTER) rounded up to whole 16-byte vectors).  A thread
+// copies its EPT elements out of the stage into registers as e^(x - m_t)
+// (one exponential per element), the stage is refilled with the row STAGES
+// ahead, the (m, d) states are merged across the cluster, and the thread
+// writes y = e^(x - m_t) * e^(m_t - m)/d from registers.
+// Requires 16-byte aligned rows: x 16-byte aligned and cols*sizeof(TI) a
+// multiple of 16 (so every slice starts and ends on a vector boundary).
+template <typename TI, int THREADS, int EPT, int STAGES>
+struct TmaRing {
+    static constexpr int EPV = VecTraits<TI>::EPV;
+    static constexpr int VPT = EPT / EPV;
+    static constexpr int STAGE_BYTES = THREADS * EPT * int(sizeof(TI));
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES;
+};
+
+template <typename TI, typename TO, int THREADS, int EPT, int CLUSTER, int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+                KernelCtl ctl) {
+    using Ring = TmaRing<TI, THREADS, EPT, STAGES>;
+    constexpr int EPV = Ring::EPV, VPT = Ring::VPT;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[STAGES];
+    __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
+
+    const int tid = threadIdx.x;
+    const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
+    const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
+    const int slice = ((cols + CLUSTER - 1) / CLUSTER + EPV - 1) / EPV * EPV;
+    const int begin = int(rank) * slice;
+    const int len = max(0, min(cols - begin, slice));
+    const uint32_t bytes = uint32_t(len) * uint32_t(sizeof(TI));
+    const int nvec = len / EPV;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+    }
+    if (CLUSTER > 1) cluster_sync(); else __syncthreads();
+
+    // Producer (thread 0): loads issued into each stage.  After a wait gives
+    // up, a thread stops waiting (its data for the rest of the launch is
+    // garbage and the status word says so) and thread 0 stops issuing.
+    int issued[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+    bool failed = false;
+    auto issue = [&](int64_t local_row, int stage) {
+        const int64_t row = cluster_id + local_row * nclusters;
+        if (failed || row >= rows || bytes == 0) return;
+        if (ctl.fault == kFaultSkipFirstLoad && local_row == 0 && blockIdx.x == 0) return;
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        bulk_g2s(ring + stage * Ring::STAGE_BYTES, x + row * int64_t(cols) + begin, bytes,
+                 &full[stage]);
+        ++issued[stage];
+    };
+    if (tid == 0)
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) issue(s, s);
+
+    int parity = 0;
+    int64_t i = 0;
+    for (int64_t row = cluster_id; row < rows; row += nclusters, ++i, parity ^= 1) {
+        const int stage = int(i % STAGES);
+        if (!failed && bytes != 0)
+            failed = !mbar_wait_bounded(&full[stage], uint32_t((i / STAGES) & 1), ctl);
+
+        const unsigned char* src = ring + stage * Ring::STAGE_BYTES;
+        float e[EPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * THREADS;
+            if (v < nvec) {
+                unpack(ld_shared_v4(src + v * 16), e + k * EPV, TI());
+            } else {
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
+            }
+        }
+        const float m_t = max_of<EPT>(e);
+        const float d_t = exp_shift_sum<EPT>(e, m_t);
+        // merge_row_state's first barrier also marks the stage as consumed
+        const float2 md = merge_row_state<THREADS, CLUSTER, true>(
+            sm, m_t, d_t, parity, rank, [&] { if (tid == 0) issue(i + STAGES, stage); });
+        scale_all<EPT>(e, rescale(m_t, md.x) * (1.0f / md.y));
+        TO* yr = y + row * int64_t(cols) + begin;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * THREADS;
+            if (v < nvec) VecStore<TO, EPV>::run(yr + v * EPV, e + k * EPV);
+        }
+    }
+    // Loads can be left in flight only after a wait gave up: wait for each
+    // stage's last issued load (bounded) so nothing lands after the CTA exits.
+    if (tid == 0 && failed) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s)
+            if (issued[s] > 0) mbar_wait_bounded(&full[s], uint32_t((issued[s] - 1) & 1), ctl);
     }
 }
 

@@ -4,33 +4,37 @@
 // online normalizer with TopK: a single loop keeps (m, d) and the K best logits
 // u with their indices p, and only the winners are turned into probabilities
 // v_i = e^(u_i - m_V) / d_V at the end.  Selecting on logits is exact because
-// softmax is monotone.  The notes keep K+1 sorted slots per thread and insert
-// by one bubble pass; on a GPU this kernel keeps the same invariant (a sorted
-// list of the K best seen so far, per CTA) but fills it in batches:
+// softmax is monotone.  The notes keep K+1 sorted slots and insert by one
+// bubble pass per element; this kernel keeps the same invariant (a sorted list
+// of the K best seen so far, per CTA) but fills it in batches:
 //
-//   1. a CTA loads a tile of its row slice into registers and folds it into
-//      each thread's running (m, d) (chunked update, as in the softmax kernels);
-//   2. threshold: every thread takes its best element; each warp sorts its 32
-//      thread bests (bitonic network over shuffles); the worst of the warps'
-//      j*-th entries (j* = ceil(K / warps) - 1) is beaten or equalled by at
-//      least K elements of the tile, so nothing worse can be in the top K.  The
-//      running list's K-th entry is a second such bound; the better one is used;
-//   3. elements that are not worse than the threshold are appended to a
-//      shared-memory candidate buffer (few for random data: ~K + K ln(...));
-//   4. the new running list is the K best of (candidates U old list), found by
-//      ranking: rank(c) = number of entries that beat c.  If the buffer
-//      overflowed, the appended part is merged, the threshold is raised to the
-//      new K-th entry and the not-yet-appended elements are scanned again;
-//   5. the CTAs of the cluster send their lists and (m, d) states to CTA 0,
-//      which ranks the CLUSTER sorted lists against each other (binary search
-//      per list), folds the states with (+), and writes v = e^(u - m)/d and
-//      the indices in order.
+//   1. a cluster of CLUSTER CTAs owns a row; CTA `rank` stages its contiguous
+//      segment (a tile of up to TILE elements at a time) in shared memory with
+//      one bulk copy, and reads it twice: each thread's maximum over its
+//      elements of the tile, then their sum of e^(x - max); the tile's
+//      (max, sum) folds into the thread's running (m, d) (chunked update);
+//   2. threshold: each warp sorts its 32 thread maxima (bitonic network over
+//      shuffles).  The smallest of the warps' j*-th values (j* = ceil(K /
+//      warps) - 1) has at least K elements of the tile at or above it, so no
+//      element below it can be in the top K.  The running list's K-th value
+//      is a second such bound; the larger one is used;
+//   3. elements at or above the threshold are appended to a shared-memory
+//      candidate buffer (about K + K ln(n/K) for random data);
+//   4. the running list becomes the K best of (candidates U list), found by
+//      ranking: rank(c) = number of entries that beat c.  When the buffer
+//      would overflow (heavy ties at the threshold), an exact fallback finds
+//      the K-th largest key of the tile by bisection on the order-preserving
+//      bit pattern and admits the ties at it in index order;
+//   5. the CTAs send their lists and (m, d) states to CTA 0 of the cluster
+//      (distributed shared memory), which ranks the sorted lists against each
+//      other (binary search per list), folds the states with (+), and writes
+//      v = e^(u - m)/d and the indices, best first.
 //
 // Order ("beats"): larger logit first; equal logits, lower column index first.
 // Index INT32_MAX marks an empty slot and never beats a real element.
 //
-// Rows need only 4-byte alignment: vectors are taken in the 16-byte-aligned
-// frame of each row; the partial first and last vectors are read element-wise.
+// Rows only need 4-byte alignment: the bulk copy covers the 16-byte-aligned
+// interior of a tile; its first and last few elements are read one by one.
 #pragma once
 
 #include <climits>
@@ -52,23 +56,19 @@ __device__ __forceinline__ bool beats(float v1, int j1, float v2, int j2) {
 }
 __device__ __forceinline__ bool beats(const Cand& a, const Cand& b) { return beats(a.v, a.j, b.v, b.j); }
 
-// Sort (v, j) descending by `beats` across the 32 lanes of a warp.
-__device__ __forceinline__ void warp_bitonic_desc(float& v, int& j) {
+// Sort v descending across the 32 lanes of a warp.
+__device__ __forceinline__ float warp_sort_desc(float v) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float ov = __shfl_xor_sync(kFullMask, v, stride);
-            const int oj = __shfl_xor_sync(kFullMask, j, stride);
-            const bool keep_better = ((lane & stride) == 0) == ((lane & size) == 0);
-            const bool take = keep_better ? beats(ov, oj, v, j) : beats(v, j, ov, oj);
-            if (take) {
-                v = ov;
-                j = oj;
-            }
+            const float o = __shfl_xor_sync(kFullMask, v, stride);
+            const bool keep_larger = ((lane & stride) == 0) == ((lane & size) == 0);
+            v = keep_larger ? fmaxf(v, o) : fminf(v, o);
         }
     }
+    return v;
 }
 
 // Number of entries of the sorted list L[0..K) that beat c (they form a prefix).
@@ -81,129 +81,222 @@ __device__ __forceinline__ int count_beating(const Cand* L, int K, const Cand& c
     return lo;
 }
 
+// Order-preserving map float -> uint32 (larger float, larger key).
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+template <int THREADS>
+__device__ __forceinline__ int block_sum(int v, int* scratch) {
+    v = __reduce_add_sync(kFullMask, v);
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int total = 0;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) total += scratch[w];
+    __syncthreads();
+    return total;
+}
+
 template <int THREADS, int CLUSTER, int KMAX, int CAP>
 struct TopkSmem {
+    uint64_t bar;
     float2 warp_state[THREADS / 32];
-    Cand warp_thr[THREADS / 32];
+    float warp_thr[THREADS / 32];
+    int scratch[THREADS / 32];
+    int ncand;
+    int taken;
     Cand cand[CAP];
     Cand run[2][KMAX];
-    int ncand[2];
     float2 xstate[2][CLUSTER];
     Cand xlist[2][CLUSTER][KMAX];
 };
 
-template <int THREADS, int VPT, int CLUSTER, int KMAX, int CAP>
+// Dynamic shared memory of a launch: the tile frame (TILE + 8 floats).
+template <int TILE>
+constexpr int topk_frame_bytes() { return (TILE + 8) * 4; }
+
+template <int THREADS, int CLUSTER, int TILE, int KMAX, int CAP>
 __global__ void __launch_bounds__(THREADS)
 topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __restrict__ idx,
-                 int64_t rows, int cols, int K) {
-    constexpr int EPT = VPT * 4, NW = THREADS / 32, TILE = THREADS * VPT;
-    static_assert(EPT <= 32, "processed-element mask is 32 bits");
+                 int64_t rows, int cols, int K, KernelCtl ctl) {
+    constexpr int NW = THREADS / 32;
+    extern __shared__ __align__(128) float frame[];
     __shared__ TopkSmem<THREADS, CLUSTER, KMAX, CAP> sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
     const int jstar = min((K + NW - 1) / NW - 1, 31);
     const Cand pad{kNegInf, kNoIndex};
+    const int seg = (cols + CLUSTER - 1) / CLUSTER;
+    const int seg_begin = min(int(rank) * seg, cols);
+    const int seg_end = min(seg_begin + seg, cols);
 
-    if (tid < 2) sm.ncand[tid] = 0;
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        mbar_init_fence();
+        sm.ncand = 0;
+    }
     if (CLUSTER > 1) cluster_sync(); else __syncthreads();
 
-    int parity = 0, pass = 0;
+    // All threads count the bulk loads the CTA should have issued (the phases
+    // of sm.bar); thread 0 issues them.  After a wait gives up a thread stops
+    // waiting and thread 0 stops issuing (outputs are garbage, the status word
+    // says so); a load left in flight is waited for before the CTA exits.
+    uint32_t loads = 0, pending_parity = 0;
+    bool failed = false, pending = false;
+    int parity = 0;
     for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
         const float* xr = x + row * int64_t(cols);
-        const int s = int((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);  // row start inside its 16-B vector
-        const float* frame = xr - s;                                    // 16-byte aligned
-        const int64_t nvf = (int64_t(cols) + s + 3) / 4;
-        const int64_t per_cta = (nvf + CLUSTER - 1) / CLUSTER;
-        const int64_t begin = int64_t(rank) * per_cta;
-        const int64_t end = begin + per_cta < nvf ? begin + per_cta : nvf;
-
         int cur = 0;
         if (tid < KMAX) sm.run[0][tid] = pad;
         float m = kNegInf, d = 0.f;
 
-        for (int64_t tb = begin; tb < end; tb += TILE) {
-            // 1. load the tile; element (k, q) has column 4u - s + q
-            float v[EPT];
-            int64_t u0[VPT];
+        for (int tb = seg_begin; tb < seg_end; tb += TILE) {
+            const int len = min(TILE, seg_end - tb);
+            // ---- 1a. stage the tile: bulk copy of the aligned interior, element loads at the ends
+            const uintptr_t a = reinterpret_cast<uintptr_t>(xr + tb);
+            const uintptr_t a_floor = a & ~uintptr_t(15), a_ceil = (a + 15) & ~uintptr_t(15);
+            const uintptr_t a_end = a + uintptr_t(len) * 4, a_end_floor = a_end & ~uintptr_t(15);
+            const int head = int(a - a_floor) / 4;  // frame index of element 0
+            const bool bulk = a_end_floor > a_ceil;
+            const int plain_head = bulk ? int(a_ceil - a) / 4 : len;
+            const int tail_from = bulk ? int(a_end_floor - a) / 4 : len;
+            if (tid == 0 && bulk && !failed &&
+                !(ctl.fault == kFaultSkipFirstLoad && blockIdx.x == 0 && loads == 0)) {
+                mbar_arrive_expect_tx(&sm.bar, uint32_t(a_end_floor - a_ceil));
+                bulk_g2s(frame + (a_ceil - a_floor) / 4, reinterpret_cast<const void*>(a_ceil),
+                         uint32_t(a_end_floor - a_ceil), &sm.bar);
+                pending = true;
+                pending_parity = loads & 1u;
+            }
+            if (tid < plain_head) frame[head + tid] = xr[tb + tid];
+            if (tid >= 32 && tid - 32 < len - tail_from)
+                frame[head + tail_from + tid - 32] = xr[tb + tail_from + tid - 32];
+            if (bulk) {
+                if (!failed) {
+                    failed = !mbar_wait_bounded(&sm.bar, loads & 1u, ctl);
+                    if (!failed) pending = false;
+                }
+                ++loads;
+            }
+            __syncthreads();
+
+            // ---- 1b. thread maximum of the tile, then sum of e^(x - max): a
+            // second read of shared memory instead of a rescale per vector
+            const int nq = (head + len + 3) / 4;
+            auto load4 = [&](int q, float* v) {
+                const uint4 w = ld_shared_v4(frame + 4 * q);
+                v[0] = __uint_as_float(w.x);
+                v[1] = __uint_as_float(w.y);
+                v[2] = __uint_as_float(w.z);
+                v[3] = __uint_as_float(w.w);
+                if (4 * q < head || 4 * q + 4 - head > len) {
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int64_t u = tb + int64_t(k) * THREADS + tid;
-                u0[k] = u;
-                const int64_t j0 = 4 * u - s;
-                if (u < end && j0 >= 0 && j0 + 4 <= cols) {
-                    const uint4 w = ld_stream_v4(frame + 4 * u);
-                    v[4 * k] = __uint_as_float(w.x);
-                    v[4 * k + 1] = __uint_as_float(w.y);
-                    v[4 * k + 2] = __uint_as_float(w.z);
-                    v[4 * k + 3] = __uint_as_float(w.w);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int64_t j = j0 + q;
-                        v[4 * k + q] = (u < end && j >= 0 && j < cols) ? xr[j] : kNegInf;
+                    for (int l = 0; l < 4; ++l) {
+                        const int e = 4 * q + l - head;
+                        if (e < 0 || e >= len) v[l] = kNegInf;
                     }
                 }
-            }
-            auto col_of = [&](int k, int q) -> int {
-                const int64_t j = 4 * u0[k] - s + q;
-                return (u0[k] < end && j >= 0 && j < cols) ? int(j) : kNoIndex;
             };
-
-            // running (m, d): one rescale per tile
+            float tmax = kNegInf;
+            for (int q = tid; q < nq; q += THREADS) {
+                float v[4];
+                load4(q, v);
+                tmax = max3(tmax, fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+            }
+            float tsum = 0.f;
+            for (int q = tid; q < nq; q += THREADS) {
+                float v[4];
+                load4(q, v);
+                tsum += exp_sum<4>(v, tmax);
+            }
             {
-                const float m_new = fmaxf(m, max_of<EPT>(v));
-                d = d * rescale(m, m_new) + exp_sum<EPT>(v, m_new);
+                const float m_new = fmaxf(m, tmax);
+                d = d * rescale(m, m_new) + tsum * rescale(tmax, m_new);
                 m = m_new;
             }
 
-            // 2. threshold from the warps' sorted thread bests
-            float bv = kNegInf;
-            int bj = kNoIndex;
+            // ---- 2. threshold
+            const float sorted = warp_sort_desc(tmax);
+            if (lane == jstar) sm.warp_thr[warp] = sorted;
+            __syncthreads();
+            float T = sm.warp_thr[0];
 #pragma unroll
-            for (int k = 0; k < VPT; ++k)
+            for (int w = 1; w < NW; ++w) T = fminf(T, sm.warp_thr[w]);
+            T = fmaxf(T, sm.run[cur][K - 1].v);
+
+            // ---- 3. candidates at or above T
+            for (int q = tid; q < nq; q += THREADS) {
+                float v[4];
+                load4(q, v);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j = col_of(k, q);
-                    if (beats(v[4 * k + q], j, bv, bj)) {
-                        bv = v[4 * k + q];
-                        bj = j;
+                for (int l = 0; l < 4; ++l) {
+                    const int e = 4 * q + l - head;
+                    if (v[l] >= T && e >= 0 && e < len) {
+                        const int pos = atomicAdd(&sm.ncand, 1);
+                        if (pos < CAP) sm.cand[pos] = Cand{v[l], tb + e};
                     }
                 }
-            warp_bitonic_desc(bv, bj);
-            if (lane == jstar) sm.warp_thr[warp] = Cand{bv, bj};
+            }
             __syncthreads();
-            Cand T = sm.warp_thr[0];
-#pragma unroll
-            for (int w = 1; w < NW; ++w)
-                if (beats(T, sm.warp_thr[w])) T = sm.warp_thr[w];
-            if (beats(sm.run[cur][K - 1], T)) T = sm.run[cur][K - 1];
+            int n = sm.ncand;
+            __syncthreads();
+            if (tid == 0) sm.ncand = 0;
 
-            // 3-4. collect candidates not worse than T, merge into the running list
-            uint32_t done = 0;  // bit i: element i already appended
-            while (true) {
-                int* counter = &sm.ncand[pass & 1];
-#pragma unroll
-                for (int k = 0; k < VPT; ++k)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int i = 4 * k + q;
-                        const int j = col_of(k, q);
-                        if (j != kNoIndex && !(done >> i & 1u) && !beats(T.v, T.j, v[i], j)) {
-                            const int pos = atomicAdd(counter, 1);
-                            if (pos < CAP) {
-                                sm.cand[pos] = Cand{v[i], j};
-                                done |= 1u << i;
-                            }
-                        }
-                    }
+            if (n > CAP) {
+                // ---- 4b. exact fallback: K-th largest key of the tile by bisection
+                const int need = min(K, len);
+                uint32_t t = 0;
+                for (int bit = 31; bit >= 0; --bit) {
+                    const uint32_t probe = t | (1u << bit);
+                    int c = 0;
+                    for (int e = tid; e < len; e += THREADS) c += order_key(frame[head + e]) >= probe;
+                    if (block_sum<THREADS>(c, sm.scratch) >= need) t = probe;
+                }
+                // strictly above t: fewer than `need`; then ties at t in column order
+                if (tid == 0) {
+                    sm.ncand = 0;
+                    sm.taken = 0;
+                }
                 __syncthreads();
-                const int n_all = *counter;
-                const int n = min(n_all, CAP);
-                if (tid == 0) sm.ncand[(pass + 1) & 1] = 0;
+                for (int e = tid; e < len; e += THREADS) {
+                    const float v = frame[head + e];
+                    if (order_key(v) > t) sm.cand[atomicAdd(&sm.ncand, 1)] = Cand{v, tb + e};
+                }
+                __syncthreads();
+                const int above = sm.ncand;
+                for (int base = 0; base < len; base += THREADS) {
+                    const int e = base + tid;
+                    const bool tie = e < len && order_key(frame[head + e]) == t;
+                    const unsigned ballot = __ballot_sync(kFullMask, tie);
+                    if (lane == 0) sm.scratch[warp] = __popc(ballot);
+                    __syncthreads();
+                    int before = sm.taken;
+                    for (int w = 0; w < warp; ++w) before += sm.scratch[w];
+                    before += __popc(ballot & ((1u << lane) - 1u));
+                    if (tie && above + before < need)
+                        sm.cand[above + before] = Cand{frame[head + e], tb + e};
+                    __syncthreads();
+                    if (tid == 0) {
+                        int add = 0;
+                        for (int w = 0; w < NW; ++w) add += sm.scratch[w];
+                        sm.taken += add;
+                    }
+                    __syncthreads();
+                    if (above + sm.taken >= need) break;
+                }
+                n = need;
+                __syncthreads();
+                if (tid == 0) sm.ncand = 0;
+            }
+
+            // ---- 4. running list := K best of (candidates U list)
+            {
                 const Cand* R = sm.run[cur];
                 Cand* Rn = sm.run[cur ^ 1];
-                int real_in_R = count_beating(R, K, pad);  // entries of R that are not empty
+                const int real_in_R = count_beating(R, K, pad);
                 const int total = min(n + real_in_R, K);
                 for (int i = tid; i < n + K; i += THREADS) {
                     const Cand c = i < n ? sm.cand[i] : R[i - n];
@@ -215,13 +308,10 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 if (tid >= total && tid < K) Rn[tid] = pad;
                 __syncthreads();
                 cur ^= 1;
-                ++pass;
-                if (beats(sm.run[cur][K - 1], T)) T = sm.run[cur][K - 1];
-                if (n_all <= CAP) break;
             }
         }
 
-        // 5. CTA state and list to CTA 0 of the cluster
+        // ---- 5. CTA state and list to CTA 0 of the cluster
         {
             float mm = m, dd = d;
             group_merge<32>(mm, dd);
@@ -271,6 +361,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             }
         }
     }
+    if (tid == 0 && pending) mbar_wait_bounded(&sm.bar, pending_parity, ctl);
 }
 
 }  // namespace os

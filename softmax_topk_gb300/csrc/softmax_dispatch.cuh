@@ -4,11 +4,15 @@
 // Choice by row length, in 16-byte input vectors nv = ceil(cols / EPV):
 //   WARP    nv <= 256: L = 1..32 lanes per row with 4 vectors per lane, or 32
 //           lanes with 8 vectors (rows of up to 1024 fp32 / 2048 bf16).
-//   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV): one CTA
-//           of 128/256/512 threads per row, or a cluster of 2..16 CTAs of 512
-//           threads when one CTA cannot hold the row (rows of up to 262144
-//           fp32 / 524288 bf16; 16-CTA clusters only where the device can
-//           schedule them).
+//   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV).
+//           * rows longer than 8192 elements whose rows start on 16-byte
+//             boundaries: the persistent bulk-copy ring (tma_rows), one CTA
+//             or a cluster of 2..16 CTAs of 512 threads per row, with row
+//             slices prefetched STAGES-1 rows ahead in shared memory;
+//           * otherwise the register kernel (onchip_rows): one CTA of
+//             128/256/512 threads, or a cluster of 512-thread CTAs, per row.
+//           Rows of up to 262144 fp32 / 524288 bf16 (16-CTA clusters only
+//           where the device can schedule them).
 //   STREAM  anything longer: one CTA per row when there are enough rows to
 //           fill the GPU, else a cluster of 8 CTAs per row.
 // "5.2 CUDA Online Softmax" (sections 6.3 and 8.3) makes the same split on
@@ -26,13 +30,17 @@ constexpr int kOnchipThreadsMax = 512;
 constexpr int kOnchipElemsPerThread = 32;
 constexpr int kStreamThreads = 512;
 constexpr int kStreamUnroll = 4;
-constexpr int kMaxCluster = 16;
+constexpr int kTmaMinCols = 8192;
 
 template <typename TI, typename TO>
 struct SoftmaxFamily {
     using Kernel = void (*)(const TI*, TO*, int64_t, int, int);
+    using TmaKernel = void (*)(const TI*, TO*, int64_t, int, KernelCtl);
     static constexpr int EPV = VecTraits<TI>::EPV;
     static constexpr int VPT = kOnchipElemsPerThread / EPV;
+    // 192 KB of ring per CTA: 3 stages of 64 KB (fp32) or 6 of 32 KB (bf16)
+    static constexpr int TMA_STAGES = sizeof(TI) == 4 ? 3 : 6;
+    using Ring = TmaRing<TI, kOnchipThreadsMax, kOnchipElemsPerThread, TMA_STAGES>;
 
     static Kernel warp(int lanes, int vpt) {
         if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads>;
@@ -60,6 +68,16 @@ struct SoftmaxFamily {
             default: return onchip_rows_kernel<TI, TO, 512, VPT, 16>;
         }
     }
+    static TmaKernel tma(int cluster) {
+        constexpr int T = kOnchipThreadsMax, E = kOnchipElemsPerThread, S = TMA_STAGES;
+        switch (cluster) {
+            case 1: return tma_rows_kernel<TI, TO, T, E, 1, S>;
+            case 2: return tma_rows_kernel<TI, TO, T, E, 2, S>;
+            case 4: return tma_rows_kernel<TI, TO, T, E, 4, S>;
+            case 8: return tma_rows_kernel<TI, TO, T, E, 8, S>;
+            default: return tma_rows_kernel<TI, TO, T, E, 16, S>;
+        }
+    }
     static Kernel streaming(int cluster) {
         return cluster == 1 ? stream_rows_kernel<TI, TO, kStreamThreads, kStreamUnroll, 1>
                             : stream_rows_kernel<TI, TO, kStreamThreads, kStreamUnroll, 8>;
@@ -69,18 +87,42 @@ struct SoftmaxFamily {
     static int onchip_cluster_limit(const DeviceInfo& dev) {
         static int cache[64] = {0};
         int& c = cache[dev.device & 63];
-        if (c == 0) c = max_active_clusters(onchip(512, 16), 512, 16) > 0 ? 16 : 8;
+        if (c == 0) {
+            const bool reg16 = max_active_clusters(onchip(512, 16), 512, 16) > 0;
+            const bool tma16 = max_active_clusters(tma(16), 512, 16, Ring::SMEM_BYTES) > 0;
+            c = reg16 && tma16 ? 16 : 8;
+        }
         return c;
     }
 
-    static os_status plan(int64_t rows, int64_t cols, os_path path, os_plan* p) {
+    // Clusters of the bulk-copy ring kernel resident at once (its persistent grid).
+    static int tma_resident_clusters(const DeviceInfo& dev, int cluster) {
+        static int cache[64][5] = {{0}};
+        const int slot = cluster == 1 ? 0 : cluster == 2 ? 1 : cluster == 4 ? 2 : cluster == 8 ? 3 : 4;
+        int& c = cache[dev.device & 63][slot];
+        if (c == 0) {
+            if (cluster == 1) {
+                c = blocks_per_sm(tma(1), kOnchipThreadsMax, Ring::SMEM_BYTES) * dev.sms;
+            } else {
+                c = max_active_clusters(tma(cluster), kOnchipThreadsMax, cluster,
+                                        Ring::SMEM_BYTES);
+            }
+            if (c <= 0) c = -1;
+        }
+        return c;
+    }
+
+    // `aligned`: x and y 16-byte aligned (then rows are aligned iff cols is a
+    // multiple of the vector width).
+    static os_status plan(int64_t rows, int64_t cols, os_path path, bool aligned, os_plan* p) {
         const DeviceInfo* dev = device_info();
         if (!dev) return OS_ERR_CUDA;
         const int64_t nv = ceil_div(cols, EPV);
         const bool warp_ok = nv <= 256;
         const int64_t cta_cap = int64_t(kOnchipThreadsMax) * VPT;
         const bool onchip_ok = nv <= int64_t(onchip_cluster_limit(*dev)) * cta_cap;
-        if (path == OS_PATH_AUTO) path = warp_ok ? OS_PATH_WARP : onchip_ok ? OS_PATH_ONCHIP : OS_PATH_STREAM;
+        if (path == OS_PATH_AUTO)
+            path = warp_ok ? OS_PATH_WARP : onchip_ok ? OS_PATH_ONCHIP : OS_PATH_STREAM;
         os_plan q = {};
         q.path = path;
         switch (path) {
@@ -91,13 +133,25 @@ struct SoftmaxFamily {
                 q.threads = kWarpThreads;
                 q.cluster = 1;
                 const int64_t rows_per_cta = kWarpThreads / q.lanes_per_row;
-                const int occ = blocks_per_sm(warp(q.lanes_per_row, q.vectors_per_thread), kWarpThreads);
+                const int occ = blocks_per_sm(warp(q.lanes_per_row, q.vectors_per_thread),
+                                              kWarpThreads);
                 q.grid = min64(ceil_div(rows, rows_per_cta), int64_t(dev->sms) * (occ > 0 ? occ : 1));
                 break;
             }
             case OS_PATH_ONCHIP: {
                 if (!onchip_ok) return OS_ERR_PATH;
                 q.vectors_per_thread = VPT;
+                const bool rows_aligned = aligned && cols % EPV == 0;
+                if (rows_aligned && cols > kTmaMinCols) {
+                    q.threads = kOnchipThreadsMax;
+                    q.cluster = pow2_at_least(ceil_div(nv, cta_cap));
+                    const int resident = tma_resident_clusters(*dev, q.cluster);
+                    if (resident > 0) {
+                        q.stages = TMA_STAGES;
+                        q.grid = min64(rows, resident) * q.cluster;
+                        break;
+                    }
+                }
                 if (nv <= cta_cap) {
                     q.cluster = 1;
                     q.threads = nv <= 128 * VPT ? 128 : nv <= 256 * VPT ? 256 : 512;
@@ -123,22 +177,24 @@ struct SoftmaxFamily {
     }
 
     static cudaError_t launch(const os_plan& p, const void* x, void* y, int64_t rows, int cols,
-                              bool aligned, cudaStream_t stream) {
+                              bool aligned, const KernelCtl& ctl, cudaStream_t stream) {
         const TI* xi = static_cast<const TI*>(x);
         TO* yo = static_cast<TO*>(y);
-        const int al = aligned ? 1 : 0;
+        if (p.path == OS_PATH_ONCHIP && p.stages > 0) {
+            TmaKernel k = tma(p.cluster);
+            if (!prepare_kernel(k, p.cluster, Ring::SMEM_BYTES)) return cudaErrorInvalidValue;
+            return launch_kernel(k, p.grid, p.threads, p.cluster, Ring::SMEM_BYTES, stream, xi, yo,
+                                 rows, cols, ctl);
+        }
         Kernel k = nullptr;
         switch (p.path) {
             case OS_PATH_WARP: k = warp(p.lanes_per_row, p.vectors_per_thread); break;
             case OS_PATH_ONCHIP: k = onchip(p.threads, p.cluster); break;
             default: k = streaming(p.cluster); break;
         }
-        if (p.cluster > 8) {
-            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-        }
-        return launch_kernel(k, p.grid, p.threads, p.cluster, stream, xi, yo, rows, cols, al);
+        if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
+        return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, xi, yo, rows, cols,
+                             aligned ? 1 : 0);
     }
 };
 
@@ -147,11 +203,13 @@ struct SoftmaxFamily {
 // One translation unit per dtype pair defines these two entry points.
 #define OS_DEFINE_SOFTMAX_PAIR(NAME, TI, TO)                                                   \
     namespace os {                                                                             \
-    os_status plan_softmax_##NAME(int64_t rows, int64_t cols, os_path path, os_plan* p) {      \
-        return SoftmaxFamily<TI, TO>::plan(rows, cols, path, p);                               \
+    os_status plan_softmax_##NAME(int64_t rows, int64_t cols, os_path path, bool aligned,      \
+                                  os_plan* p) {                                                \
+        return SoftmaxFamily<TI, TO>::plan(rows, cols, path, aligned, p);                      \
     }                                                                                          \
     cudaError_t launch_softmax_##NAME(const os_plan& p, const void* x, void* y, int64_t rows,  \
-                                      int cols, bool aligned, cudaStream_t stream) {           \
-        return SoftmaxFamily<TI, TO>::launch(p, x, y, rows, cols, aligned, stream);           \
+                                      int cols, bool aligned, const KernelCtl& ctl,            \
+                                      cudaStream_t stream) {                                   \
+        return SoftmaxFamily<TI, TO>::launch(p, x, y, rows, cols, aligned, ctl, stream);      \
     }                                                                                          \
     }

@@ -114,6 +114,14 @@ def test_exp_argument_errors(lib):
     assert lib.os_exp_f32(None, None, 0, None) == OK
 
 
+def test_testing_controls_validate(lib):
+    assert lib.os_set_wait_timeout_ns(0) == SHAPE
+    assert lib.os_set_wait_timeout_ns(20 * 10 ** 9) == SHAPE
+    assert lib.os_set_wait_timeout_ns(10 ** 9) == OK
+    assert lib.os_set_fault_injection(5) == SHAPE
+    assert lib.os_set_fault_injection(0) == OK
+
+
 def test_tensor_helpers_refuse_host_tensors(lib):
     import torch
 
