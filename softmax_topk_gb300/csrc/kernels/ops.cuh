@@ -316,6 +316,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
                  : "memory");
 }
 
+// 8 bytes into the shared memory of a CTA of the cluster (`remote`, a
+// shared::cluster address from map_to_rank), completing `bytes` of the
+// transaction count of that CTA's barrier `remote_bar`.
+__device__ __forceinline__ void st_async_b64(uint32_t remote, uint32_t lo, uint32_t hi,
+                                             uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+                 :: "r"(remote), "r"(lo), "r"(hi), "r"(remote_bar) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

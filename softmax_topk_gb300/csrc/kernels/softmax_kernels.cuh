@@ -178,22 +178,14 @@ struct RowMergeSmem {
     float2 slot[2][CLUSTER];
 };
 
-struct NoHook {
-    __device__ void operator()() const {}
-};
-
-// `after_barrier` runs right after the CTA-wide barrier that follows every
-// thread's contribution (the TMA kernel refills its stage there).
-template <int THREADS, int CLUSTER, bool HOOK = false, typename Hook = NoHook>
+template <int THREADS, int CLUSTER>
 __device__ __forceinline__ float2 merge_row_state(RowMergeSmem<THREADS, CLUSTER>& sm, float m,
-                                                  float d, int parity, uint32_t rank,
-                                                  Hook after_barrier = Hook()) {
+                                                  float d, int parity, uint32_t rank) {
     constexpr int NW = THREADS / 32;
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     group_merge<32>(m, d);
     if (lane == 0) sm.warp_state[warp] = make_float2(m, d);
     __syncthreads();
-    if (HOOK) after_barrier();
     if (warp == 0) {
         float2 s = lane < NW ? sm.warp_state[lane] : make_float2(kNegInf, 0.f);
         group_merge<32>(s.x, s.y);
@@ -263,6 +255,50 @@ onchip_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
 }
 
 // ---------------------------------------------------------------------------
+// Exchange of CTA states inside a cluster without a cluster-wide barrier:
+// every CTA sends its (m, d) with st.async into slot[parity][rank] of each
+// CTA (itself included); each CTA's barrier bar[parity] expects CLUSTER x 8
+// bytes and completes when all have landed.  A CTA sends row r+2's state only
+// after its own barrier for row r+1 completed, which needed every peer's row
+// r+1 state, sent after that peer had read its row r slots: so the parity
+// double buffer is never overwritten while being read.
+template <int CLUSTER>
+struct ClusterExchange {
+    uint64_t bar[2];
+    float2 slot[2][CLUSTER];
+};
+
+template <int CLUSTER>
+__device__ __forceinline__ void exchange_init(ClusterExchange<CLUSTER>& cx) {
+    mbar_init(&cx.bar[0], 1);
+    mbar_init(&cx.bar[1], 1);
+}
+
+// Called by all 32 lanes of one warp holding the CTA state in every lane.
+template <int CLUSTER>
+__device__ __forceinline__ void exchange_send(ClusterExchange<CLUSTER>& cx, float2 s, int parity,
+                                              uint32_t rank) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) mbar_arrive_expect_tx(&cx.bar[parity], CLUSTER * 8);
+    __syncwarp();
+    if (lane < CLUSTER)
+        st_async_b64(map_to_rank(&cx.slot[parity][rank], lane), __float_as_uint(s.x),
+                     __float_as_uint(s.y), map_to_rank(&cx.bar[parity], lane));
+}
+
+// Waits for all CLUSTER states of this row (bounded), then folds them: lane l
+// of each warp takes slot l % CLUSTER and the lanes merge in groups of
+// CLUSTER, so every thread ends with the row's (m, d) after one exponential.
+template <int CLUSTER>
+__device__ __forceinline__ float2 exchange_receive(ClusterExchange<CLUSTER>& cx, int parity,
+                                                   uint32_t use, const KernelCtl& ctl) {
+    mbar_wait_bounded(&cx.bar[parity], use & 1u, ctl);
+    float2 s = cx.slot[parity][(threadIdx.x & 31) % CLUSTER];
+    group_merge<CLUSTER>(s.x, s.y);
+    return s;
+}
+
+// ---------------------------------------------------------------------------
 // tma_rows: persistent clusters with a ring of STAGES row slices in shared
 // memory, filled by bulk copies (cp.async.bulk) STAGES-1 rows ahead of the row
 // being computed, so HBM reads stay in flight while a row is reduced, merged
@@ -271,8 +307,9 @@ onchip_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
 // (S = ceil(cols / CLUSTER) rounded up to whole 16-byte vectors).  A thread
 // copies its EPT elements out of the stage into registers as e^(x - m_t)
 // (one exponential per element), the stage is refilled with the row STAGES
-// ahead, the (m, d) states are merged across the cluster, and the thread
-// writes y = e^(x - m_t) * e^(m_t - m)/d from registers.
+// ahead, the (m, d) states are merged (shuffles, shared memory, st.async
+// between the CTAs of the cluster), and the thread writes
+// y = e^(x - m_t) * e^(m_t - m)/d from registers.
 // Requires 16-byte aligned rows: x 16-byte aligned and cols*sizeof(TI) a
 // multiple of 16 (so every slice starts and ends on a vector boundary).
 template <typename TI, int THREADS, int EPT, int STAGES>
@@ -288,12 +325,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
                 KernelCtl ctl) {
     using Ring = TmaRing<TI, THREADS, EPT, STAGES>;
-    constexpr int EPV = Ring::EPV, VPT = Ring::VPT;
+    constexpr int EPV = Ring::EPV, VPT = Ring::VPT, NW = THREADS / 32;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[STAGES];
-    __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
+    __shared__ float2 warp_state[NW];
+    __shared__ float2 cta_state[2];
+    __shared__ __align__(8) ClusterExchange<CLUSTER> cx;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
     const int slice = ((cols + CLUSTER - 1) / CLUSTER + EPV - 1) / EPV * EPV;
@@ -304,13 +343,14 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        if (CLUSTER > 1) exchange_init(cx);
         mbar_init_fence();
     }
     if (CLUSTER > 1) cluster_sync(); else __syncthreads();
 
     // Producer (thread 0): loads issued into each stage.  After a wait gives
-    // up, a thread stops waiting (its data for the rest of the launch is
-    // garbage and the status word says so) and thread 0 stops issuing.
+    // up, a thread stops waiting on the ring (its data for the rest of the
+    // launch is garbage and the status word says so) and thread 0 stops issuing.
     int issued[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued[s] = 0;
@@ -348,10 +388,24 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
             }
         }
         const float m_t = max_of<EPT>(e);
-        const float d_t = exp_shift_sum<EPT>(e, m_t);
-        // merge_row_state's first barrier also marks the stage as consumed
-        const float2 md = merge_row_state<THREADS, CLUSTER, true>(
-            sm, m_t, d_t, parity, rank, [&] { if (tid == 0) issue(i + STAGES, stage); });
+        float m = m_t, d = exp_shift_sum<EPT>(e, m_t);
+        group_merge<32>(m, d);
+        if (lane == 0) warp_state[warp] = make_float2(m, d);
+        __syncthreads();                                   // stage consumed, warp states ready
+        if (tid == 0) issue(i + STAGES, stage);
+        float2 md;
+        if (warp == 0) {
+            float2 s = lane < NW ? warp_state[lane] : make_float2(kNegInf, 0.f);
+            group_merge<32>(s.x, s.y);
+            if (CLUSTER > 1) exchange_send(cx, s, parity, rank);
+            else if (lane == 0) cta_state[parity] = s;
+        }
+        if (CLUSTER > 1) {
+            md = exchange_receive(cx, parity, uint32_t(i >> 1), ctl);
+        } else {
+            __syncthreads();
+            md = cta_state[parity];
+        }
         scale_all<EPT>(e, rescale(m_t, md.x) * (1.0f / md.y));
         TO* yr = y + row * int64_t(cols) + begin;
 #pragma unroll
@@ -367,6 +421,7 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
         for (int s = 0; s < STAGES; ++s)
             if (issued[s] > 0) mbar_wait_bounded(&full[s], uint32_t((issued[s] - 1) & 1), ctl);
     }
+    if (CLUSTER > 1) cluster_sync();  // no CTA leaves while a peer may still address it
 }
 
 // ---------------------------------------------------------------------------

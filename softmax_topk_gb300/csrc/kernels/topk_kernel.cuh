@@ -10,9 +10,10 @@
 //
 //   1. a cluster of CLUSTER CTAs owns a row; CTA `rank` stages its contiguous
 //      segment (a tile of up to TILE elements at a time) in shared memory with
-//      one bulk copy, and reads it twice: each thread's maximum over its
-//      elements of the tile, then their sum of e^(x - max); the tile's
-//      (max, sum) folds into the thread's running (m, d) (chunked update);
+//      NCHUNK bulk copies, each on its own barrier.  As each chunk lands,
+//      every thread folds its elements of the chunk into its running (m, d)
+//      (chunk maximum, then the sum of e^(x - max): one rescale per chunk) and
+//      into its maximum over the tile;
 //   2. threshold: each warp sorts its 32 thread maxima (bitonic network over
 //      shuffles).  The smallest of the warps' j*-th values (j* = ceil(K /
 //      warps) - 1) has at least K elements of the tile at or above it, so no
@@ -21,19 +22,20 @@
 //   3. elements at or above the threshold are appended to a shared-memory
 //      candidate buffer (about K + K ln(n/K) for random data);
 //   4. the running list becomes the K best of (candidates U list), found by
-//      ranking: rank(c) = number of entries that beat c.  When the buffer
-//      would overflow (heavy ties at the threshold), an exact fallback finds
-//      the K-th largest key of the tile by bisection on the order-preserving
-//      bit pattern and admits the ties at it in index order;
-//   5. the CTAs send their lists and (m, d) states to CTA 0 of the cluster
-//      (distributed shared memory), which ranks the sorted lists against each
-//      other (binary search per list), folds the states with (+), and writes
-//      v = e^(u - m)/d and the indices, best first.
+//      ranking: rank(c) = number of entries that beat c, each count split over
+//      the 32 lanes of a warp.  When the buffer would overflow (heavy ties at
+//      the threshold), an exact fallback finds the K-th largest key of the
+//      tile by bisection on the order-preserving bit pattern and admits the
+//      ties at it in column order;
+//   5. every CTA pushes its (m, d) state and sorted list into CTA 0 of the
+//      cluster with st.async (completing CTA 0's barrier); CTA 0 ranks the
+//      lists against each other (binary search per list), folds the states
+//      with (+), and writes v = e^(u - m)/d and the indices, best first.
 //
 // Order ("beats"): larger logit first; equal logits, lower column index first.
 // Index INT32_MAX marks an empty slot and never beats a real element.
 //
-// Rows only need 4-byte alignment: the bulk copy covers the 16-byte-aligned
+// Rows only need 4-byte alignment: the bulk copies cover the 16-byte-aligned
 // interior of a tile; its first and last few elements are read one by one.
 #pragma once
 
@@ -99,9 +101,10 @@ __device__ __forceinline__ int block_sum(int v, int* scratch) {
     return total;
 }
 
-template <int THREADS, int CLUSTER, int KMAX, int CAP>
+template <int THREADS, int CLUSTER, int KMAX, int CAP, int NCHUNK>
 struct TopkSmem {
-    uint64_t bar;
+    uint64_t chunk_bar[NCHUNK];
+    uint64_t xbar[2];
     float2 warp_state[THREADS / 32];
     float warp_thr[THREADS / 32];
     int scratch[THREADS / 32];
@@ -113,17 +116,13 @@ struct TopkSmem {
     Cand xlist[2][CLUSTER][KMAX];
 };
 
-// Dynamic shared memory of a launch: the tile frame (TILE + 8 floats).
-template <int TILE>
-constexpr int topk_frame_bytes() { return (TILE + 8) * 4; }
-
-template <int THREADS, int CLUSTER, int TILE, int KMAX, int CAP>
+template <int THREADS, int CLUSTER, int TILE, int KMAX, int CAP, int NCHUNK>
 __global__ void __launch_bounds__(THREADS)
 topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __restrict__ idx,
                  int64_t rows, int cols, int K, KernelCtl ctl) {
     constexpr int NW = THREADS / 32;
     extern __shared__ __align__(128) float frame[];
-    __shared__ TopkSmem<THREADS, CLUSTER, KMAX, CAP> sm;
+    __shared__ __align__(8) TopkSmem<THREADS, CLUSTER, KMAX, CAP, NCHUNK> sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
@@ -134,28 +133,35 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
     const int seg_end = min(seg_begin + seg, cols);
 
     if (tid == 0) {
-        mbar_init(&sm.bar, 1);
+        for (int c = 0; c < NCHUNK; ++c) mbar_init(&sm.chunk_bar[c], 1);
+        mbar_init(&sm.xbar[0], 1);
+        mbar_init(&sm.xbar[1], 1);
         mbar_init_fence();
         sm.ncand = 0;
     }
     if (CLUSTER > 1) cluster_sync(); else __syncthreads();
 
-    // All threads count the bulk loads the CTA should have issued (the phases
-    // of sm.bar); thread 0 issues them.  After a wait gives up a thread stops
-    // waiting and thread 0 stops issuing (outputs are garbage, the status word
-    // says so); a load left in flight is waited for before the CTA exits.
-    uint32_t loads = 0, pending_parity = 0;
-    bool failed = false, pending = false;
+    // Every thread keeps the phase parity of each chunk barrier (bit c of
+    // `cpar`, flipped whenever chunk c of a tile is non-empty, which is the
+    // same in all threads); thread 0 issues the copies.  After a wait gives up
+    // a thread stops waiting and thread 0 stops issuing (outputs are garbage,
+    // the status word says so); copies left in flight are waited for before exit.
+    uint32_t tiles = 0, cpar = 0;
+    bool failed = false;
+    uint32_t pending = 0, pending_par = 0;  // thread 0: issued chunks not yet seen complete
     int parity = 0;
-    for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
+    int64_t local = 0;
+    for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1, ++local) {
+        // a second row of this cluster reuses CTA 0's exchange slots: keep lockstep
+        if (CLUSTER > 1 && local > 0) cluster_sync();
         const float* xr = x + row * int64_t(cols);
         int cur = 0;
         if (tid < KMAX) sm.run[0][tid] = pad;
         float m = kNegInf, d = 0.f;
 
-        for (int tb = seg_begin; tb < seg_end; tb += TILE) {
+        for (int tb = seg_begin; tb < seg_end; tb += TILE, ++tiles) {
             const int len = min(TILE, seg_end - tb);
-            // ---- 1a. stage the tile: bulk copy of the aligned interior, element loads at the ends
+            // ---- 1a. stage the tile: bulk copies of the aligned interior, element loads at the ends
             const uintptr_t a = reinterpret_cast<uintptr_t>(xr + tb);
             const uintptr_t a_floor = a & ~uintptr_t(15), a_ceil = (a + 15) & ~uintptr_t(15);
             const uintptr_t a_end = a + uintptr_t(len) * 4, a_end_floor = a_end & ~uintptr_t(15);
@@ -163,36 +169,64 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             const bool bulk = a_end_floor > a_ceil;
             const int plain_head = bulk ? int(a_ceil - a) / 4 : len;
             const int tail_from = bulk ? int(a_end_floor - a) / 4 : len;
+            const int q_bulk0 = int(a_ceil - a_floor) / 16;      // first vector of the bulk region
+            const int q_bulk1 = bulk ? int(a_end_floor - a_floor) / 16 : q_bulk0;
+            const int nq = (head + len + 3) / 4;
+            const int qs_per_chunk = (q_bulk1 - q_bulk0 + NCHUNK - 1) / NCHUNK;
             if (tid == 0 && bulk && !failed &&
-                !(ctl.fault == kFaultSkipFirstLoad && blockIdx.x == 0 && loads == 0)) {
-                mbar_arrive_expect_tx(&sm.bar, uint32_t(a_end_floor - a_ceil));
-                bulk_g2s(frame + (a_ceil - a_floor) / 4, reinterpret_cast<const void*>(a_ceil),
-                         uint32_t(a_end_floor - a_ceil), &sm.bar);
-                pending = true;
-                pending_parity = loads & 1u;
+                !(ctl.fault == kFaultSkipFirstLoad && blockIdx.x == 0 && tiles == 0)) {
+                for (int c = 0; c < NCHUNK; ++c) {
+                    const int q0 = q_bulk0 + c * qs_per_chunk;
+                    const int q1 = min(q0 + qs_per_chunk, q_bulk1);
+                    if (q1 <= q0) continue;
+                    const uint32_t bytes = uint32_t(q1 - q0) * 16;
+                    mbar_arrive_expect_tx(&sm.chunk_bar[c], bytes);
+                    bulk_g2s(frame + 4 * q0, reinterpret_cast<const void*>(a_floor + uintptr_t(q0) * 16),
+                             bytes, &sm.chunk_bar[c]);
+                    pending |= 1u << c;
+                    pending_par = (pending_par & ~(1u << c)) | (cpar & (1u << c));
+                }
             }
             if (tid < plain_head) frame[head + tid] = xr[tb + tid];
             if (tid >= 32 && tid - 32 < len - tail_from)
                 frame[head + tail_from + tid - 32] = xr[tb + tail_from + tid - 32];
-            if (bulk) {
-                if (!failed) {
-                    failed = !mbar_wait_bounded(&sm.bar, loads & 1u, ctl);
-                    if (!failed) pending = false;
-                }
-                ++loads;
-            }
-            __syncthreads();
 
-            // ---- 1b. thread maximum of the tile, then sum of e^(x - max): a
-            // second read of shared memory instead of a rescale per vector
-            const int nq = (head + len + 3) / 4;
+            // ---- 1b. per chunk: running (m, d) and the thread's maximum over the tile
+            float tmax = kNegInf;
+            for (int c = 0; c < NCHUNK; ++c) {
+                const int q0 = q_bulk0 + c * qs_per_chunk;
+                const int q1 = min(q0 + qs_per_chunk, q_bulk1);
+                if (q1 <= q0) continue;
+                if (!failed) {
+                    failed = !mbar_wait_bounded(&sm.chunk_bar[c], (cpar >> c) & 1u, ctl);
+                    if (!failed && tid == 0) pending &= ~(1u << c);
+                }
+                cpar ^= 1u << c;
+                float cmax = kNegInf;
+                for (int q = q0 + tid; q < q1; q += THREADS) {
+                    const float4 v = *reinterpret_cast<const float4*>(frame + 4 * q);
+                    cmax = max3(cmax, fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+                }
+                float csum = 0.f;
+                for (int q = q0 + tid; q < q1; q += THREADS) {
+                    const float4 v = *reinterpret_cast<const float4*>(frame + 4 * q);
+                    const float w[4] = {v.x, v.y, v.z, v.w};
+                    csum += exp_sum<4>(w, cmax);
+                }
+                const float m_new = fmaxf(m, cmax);
+                d = d * rescale(m, m_new) + csum * rescale(cmax, m_new);
+                m = m_new;
+                tmax = fmaxf(tmax, cmax);
+            }
+            __syncthreads();  // element-wise loads of the ends are visible
+            // the partial vectors at the ends (at most two) and tiles too short for a bulk copy
             auto load4 = [&](int q, float* v) {
-                const uint4 w = ld_shared_v4(frame + 4 * q);
-                v[0] = __uint_as_float(w.x);
-                v[1] = __uint_as_float(w.y);
-                v[2] = __uint_as_float(w.z);
-                v[3] = __uint_as_float(w.w);
-                if (4 * q < head || 4 * q + 4 - head > len) {
+                const float4 w = *reinterpret_cast<const float4*>(frame + 4 * q);
+                v[0] = w.x;
+                v[1] = w.y;
+                v[2] = w.z;
+                v[3] = w.w;
+                if (q < q_bulk0 || q >= q_bulk1) {
 #pragma unroll
                     for (int l = 0; l < 4; ++l) {
                         const int e = 4 * q + l - head;
@@ -200,22 +234,18 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                     }
                 }
             };
-            float tmax = kNegInf;
-            for (int q = tid; q < nq; q += THREADS) {
-                float v[4];
-                load4(q, v);
-                tmax = max3(tmax, fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-            }
-            float tsum = 0.f;
-            for (int q = tid; q < nq; q += THREADS) {
-                float v[4];
-                load4(q, v);
-                tsum += exp_sum<4>(v, tmax);
-            }
             {
-                const float m_new = fmaxf(m, tmax);
-                d = d * rescale(m, m_new) + tsum * rescale(tmax, m_new);
-                m = m_new;
+                const int nedge = q_bulk0 + (nq - q_bulk1);
+                if (tid < nedge) {
+                    const int q = tid < q_bulk0 ? tid : q_bulk1 + (tid - q_bulk0);
+                    float v[4];
+                    load4(q, v);
+                    const float emax = max3(fmaxf(v[0], v[1]), v[2], v[3]);
+                    const float m_new = fmaxf(m, emax);
+                    d = d * rescale(m, m_new) + exp_sum<4>(v, m_new);
+                    m = m_new;
+                    tmax = fmaxf(tmax, emax);
+                }
             }
 
             // ---- 2. threshold
@@ -231,12 +261,14 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             for (int q = tid; q < nq; q += THREADS) {
                 float v[4];
                 load4(q, v);
+                if (fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])) >= T) {
 #pragma unroll
-                for (int l = 0; l < 4; ++l) {
-                    const int e = 4 * q + l - head;
-                    if (v[l] >= T && e >= 0 && e < len) {
-                        const int pos = atomicAdd(&sm.ncand, 1);
-                        if (pos < CAP) sm.cand[pos] = Cand{v[l], tb + e};
+                    for (int l = 0; l < 4; ++l) {
+                        const int e = 4 * q + l - head;
+                        if (v[l] >= T && e >= 0 && e < len) {
+                            const int pos = atomicAdd(&sm.ncand, 1);
+                            if (pos < CAP) sm.cand[pos] = Cand{v[l], tb + e};
+                        }
                     }
                 }
             }
@@ -292,18 +324,21 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 if (tid == 0) sm.ncand = 0;
             }
 
-            // ---- 4. running list := K best of (candidates U list)
+            // ---- 4. running list := K best of (candidates U list); one warp per item,
+            // its lanes splitting the count of entries that beat it
             {
                 const Cand* R = sm.run[cur];
                 Cand* Rn = sm.run[cur ^ 1];
                 const int real_in_R = count_beating(R, K, pad);
-                const int total = min(n + real_in_R, K);
-                for (int i = tid; i < n + K; i += THREADS) {
+                const int items = n + real_in_R;
+                const int total = min(items, K);
+                for (int i = warp; i < items; i += NW) {
                     const Cand c = i < n ? sm.cand[i] : R[i - n];
-                    if (c.j == kNoIndex) continue;
-                    int r = i < n ? count_beating(R, K, c) : i - n;
-                    for (int q = 0; q < n; ++q) r += beats(sm.cand[q], c);
-                    if (r < K) Rn[r] = c;
+                    int r = 0;
+                    for (int q = lane; q < n; q += 32) r += beats(sm.cand[q], c);
+                    r = __reduce_add_sync(kFullMask, r);
+                    r += i < n ? count_beating(R, K, c) : i - n;
+                    if (lane == 0 && r < K) Rn[r] = c;
                 }
                 if (tid >= total && tid < K) Rn[tid] = pad;
                 __syncthreads();
@@ -311,31 +346,38 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             }
         }
 
-        // ---- 5. CTA state and list to CTA 0 of the cluster
+        // ---- 5. CTA state and list pushed into CTA 0
         {
             float mm = m, dd = d;
             group_merge<32>(mm, dd);
             if (lane == 0) sm.warp_state[warp] = make_float2(mm, dd);
             __syncthreads();
-            if (warp == 0) {
-                float2 st = lane < NW ? sm.warp_state[lane] : make_float2(kNegInf, 0.f);
-                group_merge<32>(st.x, st.y);
-                if (lane == 0) {
-                    if (CLUSTER == 1) sm.xstate[parity][0] = st;
-                    else st_cluster_f2(map_to_rank(&sm.xstate[parity][rank], 0), st);
+            if (CLUSTER == 1) {
+                if (warp == 0) {
+                    float2 st = lane < NW ? sm.warp_state[lane] : make_float2(kNegInf, 0.f);
+                    group_merge<32>(st.x, st.y);
+                    if (lane == 0) sm.xstate[parity][0] = st;
                 }
-            }
-            for (int i = tid; i < K; i += THREADS) {
-                const Cand c = sm.run[cur][i];
-                if (CLUSTER == 1) {
-                    sm.xlist[parity][0][i] = c;
-                } else {
-                    st_cluster_b64(map_to_rank(&sm.xlist[parity][rank][i], 0),
-                                   __float_as_uint(c.v), uint32_t(c.j));
+                for (int i = tid; i < K; i += THREADS) sm.xlist[parity][0][i] = sm.run[cur][i];
+                __syncthreads();
+            } else {
+                const uint32_t bar0 = map_to_rank(&sm.xbar[parity], 0);
+                if (rank == 0 && tid == 0) mbar_arrive_expect_tx(&sm.xbar[parity], CLUSTER * (K + 1) * 8);
+                if (warp == 0) {
+                    float2 st = lane < NW ? sm.warp_state[lane] : make_float2(kNegInf, 0.f);
+                    group_merge<32>(st.x, st.y);
+                    if (lane == 0)
+                        st_async_b64(map_to_rank(&sm.xstate[parity][rank], 0), __float_as_uint(st.x),
+                                     __float_as_uint(st.y), bar0);
                 }
+                for (int i = tid; i < K; i += THREADS) {
+                    const Cand c = sm.run[cur][i];
+                    st_async_b64(map_to_rank(&sm.xlist[parity][rank][i], 0), __float_as_uint(c.v),
+                                 uint32_t(c.j), bar0);
+                }
+                if (rank == 0) mbar_wait_bounded(&sm.xbar[parity], uint32_t(local >> 1) & 1u, ctl);
             }
         }
-        if (CLUSTER > 1) cluster_sync(); else __syncthreads();
 
         if (rank == 0) {
             float M = kNegInf;
@@ -361,7 +403,11 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             }
         }
     }
-    if (tid == 0 && pending) mbar_wait_bounded(&sm.bar, pending_parity, ctl);
+    if (tid == 0 && pending) {
+        for (int c = 0; c < NCHUNK; ++c)
+            if (pending >> c & 1u) mbar_wait_bounded(&sm.chunk_bar[c], (pending_par >> c) & 1u, ctl);
+    }
+    if (CLUSTER > 1) cluster_sync();  // CTA 0's slots stay valid until every push has landed
 }
 
 }  // namespace os

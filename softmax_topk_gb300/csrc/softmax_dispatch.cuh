@@ -7,8 +7,9 @@
 //   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV).
 //           * rows longer than 8192 elements whose rows start on 16-byte
 //             boundaries: the persistent bulk-copy ring (tma_rows), one CTA
-//             or a cluster of 2..16 CTAs of 512 threads per row, with row
-//             slices prefetched STAGES-1 rows ahead in shared memory;
+//             or a cluster of 2..16 CTAs of 512 threads per row (32 fp32 or
+//             64 bf16 elements per thread: a 64 KB slice per CTA), with row
+//             slices prefetched 2 rows ahead in shared memory;
 //           * otherwise the register kernel (onchip_rows): one CTA of
 //             128/256/512 threads, or a cluster of 512-thread CTAs, per row.
 //           Rows of up to 262144 fp32 / 524288 bf16 (16-CTA clusters only
@@ -31,6 +32,9 @@ constexpr int kOnchipElemsPerThread = 32;
 constexpr int kStreamThreads = 512;
 constexpr int kStreamUnroll = 4;
 constexpr int kTmaMinCols = 8192;
+// elements per thread of the bulk-copy ring kernel: 32 fp32 or 64 bf16, so a
+// CTA's slice is 64 KB of input either way (3 stages: 192 KB of ring)
+template <typename TI> constexpr int tma_ept() { return sizeof(TI) == 4 ? 32 : 64; }
 
 template <typename TI, typename TO>
 struct SoftmaxFamily {
@@ -38,9 +42,9 @@ struct SoftmaxFamily {
     using TmaKernel = void (*)(const TI*, TO*, int64_t, int, KernelCtl);
     static constexpr int EPV = VecTraits<TI>::EPV;
     static constexpr int VPT = kOnchipElemsPerThread / EPV;
-    // 192 KB of ring per CTA: 3 stages of 64 KB (fp32) or 6 of 32 KB (bf16)
-    static constexpr int TMA_STAGES = sizeof(TI) == 4 ? 3 : 6;
-    using Ring = TmaRing<TI, kOnchipThreadsMax, kOnchipElemsPerThread, TMA_STAGES>;
+    static constexpr int TMA_STAGES = 3;
+    static constexpr int TMA_EPT = tma_ept<TI>();
+    using Ring = TmaRing<TI, kOnchipThreadsMax, TMA_EPT, TMA_STAGES>;
 
     static Kernel warp(int lanes, int vpt) {
         if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads>;
@@ -69,7 +73,7 @@ struct SoftmaxFamily {
         }
     }
     static TmaKernel tma(int cluster) {
-        constexpr int T = kOnchipThreadsMax, E = kOnchipElemsPerThread, S = TMA_STAGES;
+        constexpr int T = kOnchipThreadsMax, E = TMA_EPT, S = TMA_STAGES;
         switch (cluster) {
             case 1: return tma_rows_kernel<TI, TO, T, E, 1, S>;
             case 2: return tma_rows_kernel<TI, TO, T, E, 2, S>;
@@ -142,9 +146,12 @@ struct SoftmaxFamily {
                 if (!onchip_ok) return OS_ERR_PATH;
                 q.vectors_per_thread = VPT;
                 const bool rows_aligned = aligned && cols % EPV == 0;
-                if (rows_aligned && cols > kTmaMinCols) {
+                const int64_t tma_cap = int64_t(kOnchipThreadsMax) * TMA_EPT / EPV;
+                if (rows_aligned && cols > kTmaMinCols &&
+                    nv <= int64_t(onchip_cluster_limit(*dev)) * tma_cap) {
                     q.threads = kOnchipThreadsMax;
-                    q.cluster = pow2_at_least(ceil_div(nv, cta_cap));
+                    q.vectors_per_thread = TMA_EPT / EPV;
+                    q.cluster = pow2_at_least(ceil_div(nv, tma_cap));
                     const int resident = tma_resident_clusters(*dev, q.cluster);
                     if (resident > 0) {
                         q.stages = TMA_STAGES;
@@ -152,6 +159,7 @@ struct SoftmaxFamily {
                         break;
                     }
                 }
+                q.vectors_per_thread = VPT;
                 if (nv <= cta_cap) {
                     q.cluster = 1;
                     q.threads = nv <= 128 * VPT ? 128 : nv <= 256 * VPT ? 256 : 512;
