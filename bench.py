@@ -498,10 +498,29 @@ def run_only(args):
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / args.steps
-    print(json.dumps({"only": w.name, "rows": w.rows, "cols": w.cols, "path": args.path,
-                      "K": args.K if w.op == "topk" else None, "ms": round(ms, 5),
-                      "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                      "note": "inputs not rotated: L2-resident when small"}), flush=True)
+    out = {"only": w.name, "rows": w.rows, "cols": w.cols, "path": args.path,
+           "K": args.K if w.op == "topk" else None, "ms": round(ms, 5),
+           "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+           "note": "inputs not rotated: L2-resident when small"}
+    if args.graph:  # the same launches replayed from a CUDA graph: no host time between them
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(args.steps):
+                    fn()
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        gms = a.elapsed_time(b) / args.steps
+        out["graph_ms"] = round(gms, 5)
+        out["graph_gbs"] = round(nbytes / (gms * 1e-3) / 1e9, 1)
+    print(json.dumps(out), flush=True)
 
 
 def main():
@@ -517,6 +536,7 @@ def main():
     ap.add_argument("--rows", type=int, default=0, help="with --only: number of rows")
     ap.add_argument("--K", type=int, default=64, help="with --only on the TopK workload")
     ap.add_argument("--path", default="auto", help="with --only: softmax kernel family")
+    ap.add_argument("--graph", action="store_true", help="with --only: also time a CUDA graph replay")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

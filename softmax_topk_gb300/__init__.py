@@ -151,6 +151,24 @@ def _stream_handle(x) -> int:
     return torch.cuda.current_stream(x.device).cuda_stream
 
 
+class _OnDevice:
+    """Make x's device current for the call (a no-op when it already is)."""
+
+    def __init__(self, device):
+        self.index = device.index
+
+    def __enter__(self):
+        import torch
+        self.prev = torch.cuda.current_device()
+        if self.prev != self.index:
+            torch.cuda.set_device(self.index)
+
+    def __exit__(self, *exc):
+        import torch
+        if self.prev != self.index:
+            torch.cuda.set_device(self.prev)
+
+
 def softmax(x, out_dtype=None, path: str | int = "auto", out=None):
     """Row-wise softmax of a 2-D CUDA tensor (fp32 or bf16) along its last dim."""
     import torch
@@ -162,7 +180,7 @@ def softmax(x, out_dtype=None, path: str | int = "auto", out=None):
     elif out.shape != x.shape or out.dtype != out_dtype or not out.is_contiguous():
         raise ValueError("out must be contiguous with x's shape and out_dtype")
     code = PATHS[path] if isinstance(path, str) else int(path)
-    with torch.cuda.device(x.device):
+    with _OnDevice(x.device):
         os_softmax_fwd_path(x.data_ptr(), out.data_ptr(), x.shape[0], x.shape[1],
                             _dtype_code(x.dtype), _dtype_code(out_dtype), code,
                             _stream_handle(x))
@@ -179,7 +197,7 @@ def softmax_topk(x, K: int, vals=None, idx=None):
         vals = torch.empty((rows, K), dtype=torch.float32, device=x.device)
     if idx is None:
         idx = torch.empty((rows, K), dtype=torch.int32, device=x.device)
-    with torch.cuda.device(x.device):
+    with _OnDevice(x.device):
         os_softmax_topk(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, x.shape[1], K,
                         _stream_handle(x))
     return vals, idx
@@ -191,7 +209,7 @@ def exp(z):
     if not z.is_cuda or z.dtype != torch.float32 or not z.is_contiguous():
         raise ValueError("z must be a contiguous float32 CUDA tensor")
     out = torch.empty_like(z)
-    with torch.cuda.device(z.device):
+    with _OnDevice(z.device):
         os_exp_f32(z.data_ptr(), out.data_ptr(), z.numel(), _stream_handle(z))
     return out
 

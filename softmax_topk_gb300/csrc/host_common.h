@@ -5,7 +5,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/os_softmax.h"
 
@@ -58,18 +60,32 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), int64_t grid, int threads, i
 
 // Opt `kernel` into `smem` bytes of dynamic shared memory and, for cluster
 // sizes above 8, into non-portable cluster sizes.  Returns false on failure.
+// Done once per (device, kernel): later calls are a table lookup, so launches
+// (and stream captures) do not repeat the attribute calls.
 template <typename... KArgs>
 bool prepare_kernel(void (*kernel)(KArgs...), int cluster, int smem) {
     const void* k = reinterpret_cast<const void*>(kernel);
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, std::pair<int, int>> done;  // smem, cluster
+    std::lock_guard<std::mutex> lock(mu);
+    auto& d = done[{dev, k}];
+    if (smem > 48 * 1024 && smem > d.first) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        d.first = smem;
     }
-    if (cluster > 8 &&
-        cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
+    if (cluster > 8 && d.second <= 8) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        d.second = cluster;
     }
     return true;
 }
@@ -99,8 +115,20 @@ int max_active_clusters(void (*kernel)(KArgs...), int threads, int cluster, int 
     return n;
 }
 
+// Resident CTAs per SM of `kernel` (cached per device, kernel, block and smem size).
 template <typename... KArgs>
 int blocks_per_sm(void (*kernel)(KArgs...), int threads, int smem = 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static std::mutex mu;
+    static std::map<std::pair<std::pair<int, const void*>, std::pair<int, int>>, int> cache;
+    const auto key = std::make_pair(std::make_pair(dev, reinterpret_cast<const void*>(kernel)),
+                                    std::make_pair(threads, smem));
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
     int n = 0;
     if (!prepare_kernel(kernel, 1, smem)) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void*>(kernel),
@@ -108,6 +136,8 @@ int blocks_per_sm(void (*kernel)(KArgs...), int threads, int smem = 0) {
         cudaGetLastError();
         return 0;
     }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
     return n;
 }
 
