@@ -281,12 +281,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 
+// One poll of phase `parity`: the thread may sleep in the instruction until
+// the phase completes or about kSuspendHintNs pass, so waiting warps issue
+// (almost) nothing while a copy is in flight.
+constexpr uint32_t kSuspendHintNs = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+                 : "memory");
     return done != 0;
 }
 
@@ -300,7 +306,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1; it < (1u << 24); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && global_ns() - t0 > ctl.timeout_ns) break;
+        if (global_ns() - t0 > ctl.timeout_ns) break;
     }
     atomicOr(ctl.err, kErrWaitTimeout);
     return false;

@@ -321,7 +321,7 @@ struct TmaRing {
 };
 
 template <typename TI, typename TO, int THREADS, int EPT, int CLUSTER, int STAGES>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 128))
 tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
                 KernelCtl ctl) {
     using Ring = TmaRing<TI, THREADS, EPT, STAGES>;

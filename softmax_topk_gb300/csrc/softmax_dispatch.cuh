@@ -7,9 +7,9 @@
 //   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV).
 //           * rows longer than 8192 elements whose rows start on 16-byte
 //             boundaries: the persistent bulk-copy ring (tma_rows), one CTA
-//             or a cluster of 2..16 CTAs of 512 threads per row (32 fp32 or
-//             64 bf16 elements per thread: a 64 KB slice per CTA), with row
-//             slices prefetched 2 rows ahead in shared memory;
+//             or a cluster of 2..16 CTAs of 256 threads per row (32 fp32 or
+//             64 bf16 elements per thread: a 32 KB slice per CTA, two CTAs per
+//             SM), with row slices prefetched 2 rows ahead in shared memory;
 //           * otherwise the register kernel (onchip_rows): one CTA of
 //             128/256/512 threads, or a cluster of 512-thread CTAs, per row.
 //           Rows of up to 262144 fp32 / 524288 bf16 (16-CTA clusters only
@@ -32,8 +32,11 @@ constexpr int kOnchipElemsPerThread = 32;
 constexpr int kStreamThreads = 512;
 constexpr int kStreamUnroll = 4;
 constexpr int kTmaMinCols = 8192;
-// elements per thread of the bulk-copy ring kernel: 32 fp32 or 64 bf16, so a
-// CTA's slice is 64 KB of input either way (3 stages: 192 KB of ring)
+// The bulk-copy ring kernel runs CTAs of 256 threads, two per SM, so one
+// CTA's reductions and exchange overlap the other's loads and arithmetic.
+// Elements per thread: 32 fp32 or 64 bf16, so a CTA's slice is 32 KB of input
+// either way and its 3-stage ring 96 KB.
+constexpr int kTmaThreads = 256;
 template <typename TI> constexpr int tma_ept() { return sizeof(TI) == 4 ? 32 : 64; }
 
 template <typename TI, typename TO>
@@ -44,7 +47,7 @@ struct SoftmaxFamily {
     static constexpr int VPT = kOnchipElemsPerThread / EPV;
     static constexpr int TMA_STAGES = 3;
     static constexpr int TMA_EPT = tma_ept<TI>();
-    using Ring = TmaRing<TI, kOnchipThreadsMax, TMA_EPT, TMA_STAGES>;
+    using Ring = TmaRing<TI, kTmaThreads, TMA_EPT, TMA_STAGES>;
 
     static Kernel warp(int lanes, int vpt) {
         if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads>;
@@ -73,7 +76,7 @@ struct SoftmaxFamily {
         }
     }
     static TmaKernel tma(int cluster) {
-        constexpr int T = kOnchipThreadsMax, E = TMA_EPT, S = TMA_STAGES;
+        constexpr int T = kTmaThreads, E = TMA_EPT, S = TMA_STAGES;
         switch (cluster) {
             case 1: return tma_rows_kernel<TI, TO, T, E, 1, S>;
             case 2: return tma_rows_kernel<TI, TO, T, E, 2, S>;
@@ -93,7 +96,7 @@ struct SoftmaxFamily {
         int& c = cache[dev.device & 63];
         if (c == 0) {
             const bool reg16 = max_active_clusters(onchip(512, 16), 512, 16) > 0;
-            const bool tma16 = max_active_clusters(tma(16), 512, 16, Ring::SMEM_BYTES) > 0;
+            const bool tma16 = max_active_clusters(tma(16), kTmaThreads, 16, Ring::SMEM_BYTES) > 0;
             c = reg16 && tma16 ? 16 : 8;
         }
         return c;
@@ -106,10 +109,9 @@ struct SoftmaxFamily {
         int& c = cache[dev.device & 63][slot];
         if (c == 0) {
             if (cluster == 1) {
-                c = blocks_per_sm(tma(1), kOnchipThreadsMax, Ring::SMEM_BYTES) * dev.sms;
+                c = blocks_per_sm(tma(1), kTmaThreads, Ring::SMEM_BYTES) * dev.sms;
             } else {
-                c = max_active_clusters(tma(cluster), kOnchipThreadsMax, cluster,
-                                        Ring::SMEM_BYTES);
+                c = max_active_clusters(tma(cluster), kTmaThreads, cluster, Ring::SMEM_BYTES);
             }
             if (c <= 0) c = -1;
         }
@@ -146,10 +148,10 @@ struct SoftmaxFamily {
                 if (!onchip_ok) return OS_ERR_PATH;
                 q.vectors_per_thread = VPT;
                 const bool rows_aligned = aligned && cols % EPV == 0;
-                const int64_t tma_cap = int64_t(kOnchipThreadsMax) * TMA_EPT / EPV;
+                const int64_t tma_cap = int64_t(kTmaThreads) * TMA_EPT / EPV;
                 if (rows_aligned && cols > kTmaMinCols &&
                     nv <= int64_t(onchip_cluster_limit(*dev)) * tma_cap) {
-                    q.threads = kOnchipThreadsMax;
+                    q.threads = kTmaThreads;
                     q.vectors_per_thread = TMA_EPT / EPV;
                     q.cluster = pow2_at_least(ceil_div(nv, tma_cap));
                     const int resident = tma_resident_clusters(*dev, q.cluster);
