@@ -114,6 +114,40 @@ __device__ __forceinline__ float2 exp2x(float2 z) {
     return mul2(p, make_float2(pow2_from_rounded(t.x), pow2_from_rounded(t.y)));
 }
 
+// Cheaper variant for results that are rounded to bf16 afterwards (relative
+// error ~3e-6 against bf16's 2^-9 = 2e-3 rounding): ln 2 reduction with one
+// constant and a degree-4 minimax polynomial (same fit, degree 4).
+namespace expc4 {
+constexpr float kLn2 = 0.693147182e+00f;  // fp32(ln 2)
+constexpr float c1 = 0.99996674f;
+constexpr float c2 = 0.5000302f;
+constexpr float c3 = 0.1678763f;
+constexpr float c4 = 0.041513626f;
+}  // namespace expc4
+
+__device__ __forceinline__ float2 exp2x_bf16out(float2 z) {
+    using expc::kFloor;
+    using expc::kLog2e;
+    using expc::kRound;
+    z.x = fmaxf(z.x, kFloor);
+    z.y = fmaxf(z.y, kFloor);
+    const float2 t = fma2(z, splat2(kLog2e), splat2(kRound));
+    const float2 n = add2(t, splat2(-kRound));
+    const float2 r = fma2(n, splat2(-expc4::kLn2), z);
+    float2 p = fma2(splat2(expc4::c4), r, splat2(expc4::c3));
+    p = fma2(p, r, splat2(expc4::c2));
+    p = fma2(p, r, splat2(expc4::c1));
+    p = fma2(p, r, splat2(1.0f));
+    return mul2(p, make_float2(pow2_from_rounded(t.x), pow2_from_rounded(t.y)));
+}
+
+// e^z of a pair, accurate (FAST = false) or for bf16 results (FAST = true).
+template <bool FAST>
+__device__ __forceinline__ float2 exp_pair(float2 z) {
+    if constexpr (FAST) return exp2x_bf16out(z);
+    else return exp2x(z);
+}
+
 __device__ __forceinline__ float exp1(float z) {
     using namespace expc;
     z = fmaxf(z, kFloor);
@@ -159,6 +193,26 @@ __device__ __forceinline__ void group_merge(float& m, float& d) {
 template <typename T> struct VecTraits;
 template <> struct VecTraits<float> { static constexpr int EPV = 4; };
 template <> struct VecTraits<__nv_bfloat16> { static constexpr int EPV = 8; };
+
+// L2 eviction policies for loads that will be read again soon (pass 1 of a
+// two-pass kernel) and for last reads (pass 2).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 ld_policy_v4(const void* p, uint64_t policy) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(policy));
+    return v;
+}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;

@@ -71,7 +71,7 @@ __device__ __forceinline__ void store_slot(TO* row, int64_t v, int cols, bool al
 }
 
 // e[i] := e^(e[i] - m) for all N entries, returning the sum (pairs on f32x2).
-template <int N>
+template <int N, bool FAST = false>
 __device__ __forceinline__ float exp_shift_sum(float* e, float m) {
     static_assert(N % 2 == 0, "pairs");
     float2 acc = make_float2(0.f, 0.f);
@@ -79,7 +79,7 @@ __device__ __forceinline__ float exp_shift_sum(float* e, float m) {
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
         float2 z = add2(make_float2(e[i], e[i + 1]), neg_m);
-        float2 p = exp2x(z);
+        float2 p = exp_pair<FAST>(z);
         e[i] = p.x;
         e[i + 1] = p.y;
         acc = add2(acc, p);
@@ -88,14 +88,24 @@ __device__ __forceinline__ float exp_shift_sum(float* e, float m) {
 }
 
 // sum of e^(e[i] - m) over N entries, leaving e unchanged.
-template <int N>
+template <int N, bool FAST = false>
 __device__ __forceinline__ float exp_sum(const float* e, float m) {
     static_assert(N % 2 == 0, "pairs");
     float2 acc = make_float2(0.f, 0.f);
     const float2 neg_m = splat2(-m);
 #pragma unroll
-    for (int i = 0; i < N; i += 2) acc = add2(acc, exp2x(add2(make_float2(e[i], e[i + 1]), neg_m)));
+    for (int i = 0; i < N; i += 2)
+        acc = add2(acc, exp_pair<FAST>(add2(make_float2(e[i], e[i + 1]), neg_m)));
     return acc.x + acc.y;
+}
+
+template <typename TO> constexpr bool fast_exp_for() { return sizeof(TO) == 2; }
+
+// Load vector slot v with an L2 eviction policy (aligned rows only).
+template <typename TI>
+__device__ __forceinline__ void load_slot_policy(const TI* row, int64_t v, uint64_t policy,
+                                                 float* out) {
+    unpack(ld_policy_v4(row + v * VecTraits<TI>::EPV, policy), out, TI());
 }
 
 template <int N>
@@ -425,13 +435,23 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
 }
 
 // ---------------------------------------------------------------------------
-// stream_rows: one cluster per row (persistent over rows); CTA `rank` owns a
-// contiguous range of vector slots; two passes over it.
+// stream_rows: one CTA (or a cluster) per row, persistent over rows; CTA
+// `rank` owns a contiguous range of vector slots and reads it twice.
+// Pass 1 keeps a running (m, d) per thread with one rescale per chunk of
+// UNROLL vectors; its loads ask L2 to keep the lines (evict_last) because
+// pass 2 reads them again right after the merge.  Pass 2 walks the chunks in
+// reverse order (the most recently read lines are the likeliest still in
+// L2), marks its loads evict_first (last use) and writes y = e^(x - m) / d
+// with streaming stores.  With one CTA per row there is no exchange between
+// SMs at all: each row costs one __syncthreads-level merge.
+// bf16 outputs use the cheaper degree-4 exponential (see ops.cuh).
 template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2)
 stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
                    int aligned) {
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV;
+    constexpr bool FAST = fast_exp_for<TO>();
+    constexpr int64_t STEP = int64_t(THREADS) * UNROLL;
     __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
@@ -439,7 +459,24 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
     const int64_t per_cta = (nv + CLUSTER - 1) / CLUSTER;
     const int64_t begin = int64_t(rank) * per_cta;
     const int64_t end = begin + per_cta < nv ? begin + per_cta : nv;
+    const int64_t nchunks = end > begin ? (end - begin + STEP - 1) / STEP : 0;
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     if (CLUSTER > 1) cluster_sync();
+
+    auto load_chunk = [&](const TI* xr, int64_t c, uint64_t policy, float* e) {
+        const int64_t v0 = begin + c * STEP + threadIdx.x;
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+            const int64_t v = v0 + int64_t(k) * THREADS;
+            if (v < end) {
+                if (aligned) load_slot_policy(xr, v, policy, e + k * EPV);
+                else load_slot(xr, v, cols, false, e + k * EPV);
+            } else {
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
+            }
+        }
+    };
 
     int parity = 0;
     for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
@@ -447,44 +484,27 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
         TO* yr = y + row * int64_t(cols);
         // pass 1: running (m, d), one rescale per chunk of UNROLL vectors
         float m = kNegInf, d = 0.f;
-        for (int64_t v = begin + threadIdx.x; v < end; v += int64_t(THREADS) * UNROLL) {
+        for (int64_t c = 0; c < nchunks; ++c) {
             float e[EPC];
-#pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
-                const int64_t vk = v + int64_t(k) * THREADS;
-                if (vk < end) {
-                    load_slot(xr, vk, cols, aligned, e + k * EPV);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
-                }
-            }
+            load_chunk(xr, c, keep, e);
             const float m_new = fmaxf(m, max_of<EPC>(e));
-            const float s = exp_shift_sum<EPC>(e, m_new);
+            const float s = exp_sum<EPC, FAST>(e, m_new);
             d = d * rescale(m, m_new) + s;
             m = m_new;
         }
         const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m, d, parity, rank);
         const float inv_d = 1.0f / md.y;
-        // pass 2: y = e^(x - m) / d
-        for (int64_t v = begin + threadIdx.x; v < end; v += int64_t(THREADS) * UNROLL) {
+        // pass 2, last chunk first: y = e^(x - m) / d
+        for (int64_t c = nchunks - 1; c >= 0; --c) {
             float e[EPC];
-#pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
-                const int64_t vk = v + int64_t(k) * THREADS;
-                if (vk < end) {
-                    load_slot(xr, vk, cols, aligned, e + k * EPV);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
-                }
-            }
-            exp_shift_sum<EPC>(e, md.x);
+            load_chunk(xr, c, drop, e);
+            exp_shift_sum<EPC, FAST>(e, md.x);
             scale_all<EPC>(e, inv_d);
+            const int64_t v0 = begin + c * STEP + threadIdx.x;
 #pragma unroll
             for (int k = 0; k < UNROLL; ++k) {
-                const int64_t vk = v + int64_t(k) * THREADS;
-                if (vk < end) store_slot<TI, TO>(yr, vk, cols, aligned, e + k * EPV);
+                const int64_t v = v0 + int64_t(k) * THREADS;
+                if (v < end) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
             }
         }
     }

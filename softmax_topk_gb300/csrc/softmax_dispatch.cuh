@@ -30,7 +30,8 @@ constexpr int kWarpThreads = 256;
 constexpr int kOnchipThreadsMax = 512;
 constexpr int kOnchipElemsPerThread = 32;
 constexpr int kStreamThreads = 512;
-constexpr int kStreamUnroll = 4;
+// 32 elements per thread per chunk: 8 fp32 vectors or 4 bf16 vectors
+template <typename TI> constexpr int stream_unroll() { return sizeof(TI) == 4 ? 8 : 4; }
 constexpr int kTmaMinCols = 8192;
 // The bulk-copy ring kernel runs CTAs of 256 threads, two per SM, so one
 // CTA's reductions and exchange overlap the other's loads and arithmetic.
@@ -85,9 +86,10 @@ struct SoftmaxFamily {
             default: return tma_rows_kernel<TI, TO, T, E, 16, S>;
         }
     }
+    static constexpr int STREAM_UNROLL = stream_unroll<TI>();
     static Kernel streaming(int cluster) {
-        return cluster == 1 ? stream_rows_kernel<TI, TO, kStreamThreads, kStreamUnroll, 1>
-                            : stream_rows_kernel<TI, TO, kStreamThreads, kStreamUnroll, 8>;
+        return cluster == 1 ? stream_rows_kernel<TI, TO, kStreamThreads, STREAM_UNROLL, 1>
+                            : stream_rows_kernel<TI, TO, kStreamThreads, STREAM_UNROLL, 8>;
     }
 
     // Largest cluster size of the ONCHIP family the current device can run.
@@ -174,9 +176,15 @@ struct SoftmaxFamily {
             }
             case OS_PATH_STREAM: {
                 q.threads = kStreamThreads;
-                q.vectors_per_thread = kStreamUnroll;
+                q.vectors_per_thread = STREAM_UNROLL;
                 q.cluster = rows >= 2 * int64_t(dev->sms) ? 1 : 8;
-                q.grid = min64(rows, kMaxClustersPerLaunch) * q.cluster;
+                {
+                    const int occ = blocks_per_sm(streaming(q.cluster), kStreamThreads);
+                    const int64_t resident = q.cluster == 1
+                        ? int64_t(dev->sms) * (occ > 0 ? occ : 1)
+                        : kMaxClustersPerLaunch;
+                    q.grid = min64(rows, resident) * q.cluster;
+                }
                 break;
             }
             default:
