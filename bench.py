@@ -307,8 +307,7 @@ def kernel_of(st, label: str) -> str:
            st.OS_PATH_STREAM: "stream_rows_kernel"}[p["path"]]
     if p["path"] == st.OS_PATH_ONCHIP and p["stages"] > 0:
         fam = "tma_rows_kernel"
-    return (f"{fam}<{w.dtype},{w.dtype},threads={p['threads']},cluster={p['cluster']},"
-            f"stages={p['stages']}>")
+    return f"{fam}<{w.dtype},{w.dtype},threads={p['threads']},cluster={p['cluster']}>"
 
 
 def run_e2e(st, dev, args):

@@ -1,7 +1,8 @@
 // softmax_dispatch.cuh -- kernel choice and launch for one (input, output) dtype
 // pair.  Included by one translation unit per pair, which instantiates it.
 //
-// Choice by row length, in 16-byte input vectors nv = ceil(cols / EPV):
+// Families by row length, in 16-byte input vectors nv = ceil(cols / EPV);
+// AUTO takes WARP for nv <= 256, ONCHIP for nv <= 4096, STREAM beyond:
 //   WARP    nv <= 256: L = 1..32 lanes per row with 4 vectors per lane, or 32
 //           lanes with 8 vectors (rows of up to 1024 fp32 / 2048 bf16).
 //   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV).
@@ -30,9 +31,13 @@ constexpr int kWarpThreads = 256;
 constexpr int kOnchipThreadsMax = 512;
 constexpr int kOnchipElemsPerThread = 32;
 constexpr int kStreamThreads = 512;
-// 32 elements per thread per chunk: 8 fp32 vectors or 4 bf16 vectors
-template <typename TI> constexpr int stream_unroll() { return sizeof(TI) == 4 ? 8 : 4; }
+// 4 vectors per thread per chunk (16 fp32 or 32 bf16 elements)
+template <typename TI> constexpr int stream_unroll() { return 4; }
 constexpr int kTmaMinCols = 8192;
+// AUTO sends rows longer than this many 16-byte vectors (16384 fp32, 32768
+// bf16 elements) to the two-pass streaming kernel: measured on GB300 it beats
+// both on-chip families there (no exchange between SMs, second read from L2).
+constexpr int64_t kAutoOnchipMaxVectors = 4096;
 // The bulk-copy ring kernel runs CTAs of 256 threads, two per SM, so one
 // CTA's reductions and exchange overlap the other's loads and arithmetic.
 // Elements per thread: 32 fp32 or 64 bf16, so a CTA's slice is 32 KB of input
@@ -130,7 +135,8 @@ struct SoftmaxFamily {
         const int64_t cta_cap = int64_t(kOnchipThreadsMax) * VPT;
         const bool onchip_ok = nv <= int64_t(onchip_cluster_limit(*dev)) * cta_cap;
         if (path == OS_PATH_AUTO)
-            path = warp_ok ? OS_PATH_WARP : onchip_ok ? OS_PATH_ONCHIP : OS_PATH_STREAM;
+            path = warp_ok ? OS_PATH_WARP
+                 : (nv <= kAutoOnchipMaxVectors && onchip_ok) ? OS_PATH_ONCHIP : OS_PATH_STREAM;
         os_plan q = {};
         q.path = path;
         switch (path) {

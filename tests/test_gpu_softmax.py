@@ -210,8 +210,10 @@ def test_side_stream(st):
 
 def test_plans_of_the_workloads(st):
     p = st.plan((4096, 32000), st.OS_F32)
-    assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 4 and p["stages"] == 3
+    assert p["path"] == st.OS_PATH_STREAM and p["cluster"] == 1
     p = st.plan((8192, 128256), st.OS_BF16)
+    assert p["path"] == st.OS_PATH_STREAM and p["cluster"] == 1
+    p = st.plan((8192, 128256), st.OS_BF16, path="onchip")
     assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 8 and p["stages"] == 3
     p = st.plan((1048576, 128), st.OS_F32)
     assert p["path"] == st.OS_PATH_WARP and p["lanes_per_row"] == 8
