@@ -366,6 +366,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// CTA-wide bounded wait: thread 0 polls (the other threads sleep in the CTA
+// barrier instead of spinning), then the result is shared through flag[which]
+// (a __shared__ int[2]); callers alternate `which` between consecutive waits
+// so a slow reader never sees the next wait's result.  Every thread of the
+// CTA must call it.
+__device__ __forceinline__ bool cta_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                 const KernelCtl& ctl, int* flag, int which) {
+    if (threadIdx.x == 0) flag[which] = mbar_wait_bounded(bar, parity, ctl) ? 1 : 0;
+    __syncthreads();
+    return flag[which] != 0;
+}
+
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,

@@ -296,13 +296,15 @@ __device__ __forceinline__ void exchange_send(ClusterExchange<CLUSTER>& cx, floa
                      __float_as_uint(s.y), map_to_rank(&cx.bar[parity], lane));
 }
 
-// Waits for all CLUSTER states of this row (bounded), then folds them: lane l
-// of each warp takes slot l % CLUSTER and the lanes merge in groups of
-// CLUSTER, so every thread ends with the row's (m, d) after one exponential.
+// Waits for all CLUSTER states of this row (bounded; thread 0 polls, the
+// others sleep in the CTA barrier), then folds them: lane l of each warp takes
+// slot l % CLUSTER and the lanes merge in groups of CLUSTER, so every thread
+// ends with the row's (m, d) after one exponential.
 template <int CLUSTER>
 __device__ __forceinline__ float2 exchange_receive(ClusterExchange<CLUSTER>& cx, int parity,
                                                    uint32_t use, const KernelCtl& ctl) {
-    mbar_wait_bounded(&cx.bar[parity], use & 1u, ctl);
+    if (threadIdx.x == 0) mbar_wait_bounded(&cx.bar[parity], use & 1u, ctl);
+    __syncthreads();
     float2 s = cx.slot[parity][(threadIdx.x & 31) % CLUSTER];
     group_merge<CLUSTER>(s.x, s.y);
     return s;
@@ -340,6 +342,7 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
     __shared__ __align__(8) uint64_t full[STAGES];
     __shared__ float2 warp_state[NW];
     __shared__ float2 cta_state[2];
+    __shared__ int wait_flag[2];
     __shared__ __align__(8) ClusterExchange<CLUSTER> cx;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -383,7 +386,8 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
     for (int64_t row = cluster_id; row < rows; row += nclusters, ++i, parity ^= 1) {
         const int stage = int(i % STAGES);
         if (!failed && bytes != 0)
-            failed = !mbar_wait_bounded(&full[stage], uint32_t((i / STAGES) & 1), ctl);
+            failed = !cta_wait_bounded(&full[stage], uint32_t((i / STAGES) & 1), ctl, wait_flag,
+                                       int(i & 1));
 
         const unsigned char* src = ring + stage * Ring::STAGE_BYTES;
         float e[EPT];

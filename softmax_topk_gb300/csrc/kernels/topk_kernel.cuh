@@ -110,6 +110,7 @@ struct TopkSmem {
     int scratch[THREADS / 32];
     int ncand;
     int taken;
+    int wait_flag[2];
     Cand cand[CAP];
     Cand run[2][KMAX];
     float2 xstate[2][CLUSTER];
@@ -198,7 +199,8 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 const int q1 = min(q0 + qs_per_chunk, q_bulk1);
                 if (q1 <= q0) continue;
                 if (!failed) {
-                    failed = !mbar_wait_bounded(&sm.chunk_bar[c], (cpar >> c) & 1u, ctl);
+                    failed = !cta_wait_bounded(&sm.chunk_bar[c], (cpar >> c) & 1u, ctl,
+                                               sm.wait_flag, c & 1);
                     if (!failed && tid == 0) pending &= ~(1u << c);
                 }
                 cpar ^= 1u << c;
@@ -375,7 +377,9 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                     st_async_b64(map_to_rank(&sm.xlist[parity][rank][i], 0), __float_as_uint(c.v),
                                  uint32_t(c.j), bar0);
                 }
-                if (rank == 0) mbar_wait_bounded(&sm.xbar[parity], uint32_t(local >> 1) & 1u, ctl);
+                if (rank == 0 && tid == 0)
+                    mbar_wait_bounded(&sm.xbar[parity], uint32_t(local >> 1) & 1u, ctl);
+                if (rank == 0) __syncthreads();
             }
         }
 

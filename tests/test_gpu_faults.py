@@ -31,13 +31,14 @@ def _stream():
                                          ((32, 128256), torch.bfloat16)])
 def test_softmax_wait_times_out_and_recovers(st, shape, dtype):
     x = (torch.randn(*shape, device="cuda") * 2).to(dtype)
-    assert st.plan(shape, st.OS_F32 if dtype == torch.float32 else st.OS_BF16)["stages"] > 0
+    code = st.OS_F32 if dtype == torch.float32 else st.OS_BF16
+    assert st.plan(shape, code, path="onchip")["stages"] > 0     # the bulk-copy ring kernel
     st.os_device_status(_stream())                      # clean slate
     st.os_set_wait_timeout_ns(20 * 10 ** 6)             # 20 ms
     st.os_set_fault_injection(1)
     try:
         t0 = time.time()
-        st.softmax(x)                                   # launch itself succeeds
+        st.softmax(x, path="onchip")                    # launch itself succeeds
         with pytest.raises(st.OsError) as e:
             st.os_device_status(_stream())
         assert e.value.name == "OS_ERR_TIMEOUT"
@@ -45,7 +46,7 @@ def test_softmax_wait_times_out_and_recovers(st, shape, dtype):
     finally:
         st.os_set_fault_injection(0)
         st.os_set_wait_timeout_ns(10 ** 9)
-    y = st.softmax(x)
+    y = st.softmax(x, path="onchip")
     st.os_device_status(_stream())                      # no error now
     xx = x.double().cpu().numpy()
     out = "f32" if dtype == torch.float32 else "bf16"
