@@ -1,9 +1,11 @@
 // Fused softmax + TopK: kernel choice and launch.
 //
-// A row is split over a cluster of CLUSTER CTAs of 512 threads, each thread
-// holding 8 vectors (32 fp32) of a tile in registers; CLUSTER is the smallest
-// power of two (up to 8) whose CTAs cover the row in one tile of 16384
-// elements each, and longer rows loop over several tiles per CTA.
+// A row is split over a cluster of CLUSTER CTAs of 512 threads; CLUSTER is
+// the smallest power of two (up to 8) whose segments are at most 26000
+// elements (two CTAs of about 100 KB of shared memory fit one SM), and rows
+// longer than 8 tiles of 32768 elements loop over several tiles per CTA.  The
+// tile frame is dynamic shared memory sized to the segment (at most one
+// tile), staged by four bulk copies.
 #include "host_common.h"
 #include "internal.h"
 #include "kernels/topk_kernel.cuh"
@@ -11,17 +13,18 @@
 namespace os {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkVpt = 8;
+constexpr int kTopkTile = 32768;
 constexpr int kTopkKmax = 64;
 constexpr int kTopkCap = 512;
+constexpr int kTopkChunks = 4;
 constexpr int kTopkMaxCluster = 8;
-constexpr int64_t kTopkTileElems = int64_t(kTopkThreads) * kTopkVpt * 4;
+constexpr int kTopkSegmentTarget = 26000;  // longest segment per CTA before adding CTAs
 
 using TopkKernel = void (*)(const float*, float*, int*, int64_t, int, int, KernelCtl);
 
 template <int C>
 constexpr TopkKernel topk_instance() {
-    return topk_rows_kernel<kTopkThreads, kTopkVpt, C, kTopkKmax, kTopkCap>;
+    return topk_rows_kernel<kTopkThreads, C, kTopkTile, kTopkKmax, kTopkCap, kTopkChunks>;
 }
 
 static TopkKernel topk_kernel_for(int cluster) {
@@ -33,15 +36,24 @@ static TopkKernel topk_kernel_for(int cluster) {
     }
 }
 
+static int frame_bytes(int64_t cols, int cluster) {
+    const int64_t seg = ceil_div(cols, cluster);
+    const int64_t tile = seg < kTopkTile ? seg : kTopkTile;
+    return static_cast<int>(((tile + 8) * 4 + 15) / 16 * 16);
+}
+
 os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
     (void)K;
     if (!device_info()) return OS_ERR_CUDA;
     os_plan q = {};
     q.path = OS_PATH_ONCHIP;
     q.threads = kTopkThreads;
-    q.vectors_per_thread = kTopkVpt;
-    q.cluster = pow2_at_least(ceil_div(cols + 3, kTopkTileElems));
+    q.cluster = pow2_at_least(ceil_div(cols, kTopkSegmentTarget));
     if (q.cluster > kTopkMaxCluster) q.cluster = kTopkMaxCluster;
+    const int64_t seg = ceil_div(cols, q.cluster);
+    q.vectors_per_thread = static_cast<int32_t>(ceil_div(seg < kTopkTile ? seg : kTopkTile,
+                                                         4 * kTopkThreads));
+    q.stages = kTopkChunks;
     q.grid = min64(rows, kMaxClustersPerLaunch) * q.cluster;
     *p = q;
     return OS_OK;
@@ -51,8 +63,9 @@ cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* 
                         int64_t rows, int cols, int K, const KernelCtl& ctl,
                         cudaStream_t stream) {
     TopkKernel k = topk_kernel_for(p.cluster);
-    if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
-    return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, x, vals,
+    const int smem = frame_bytes(cols, p.cluster);
+    if (!prepare_kernel(k, p.cluster, frame_bytes(kTopkTile, 1))) return cudaErrorInvalidValue;
+    return launch_kernel(k, p.grid, p.threads, p.cluster, smem, stream, x, vals,
                          reinterpret_cast<int*>(idx), rows, cols, K, ctl);
 }
 
