@@ -236,16 +236,13 @@ def run_ours(args):
     t1 = time.time()
     clock_info = clocks.stop(t0, t1) if clocks else None
 
-    total_ms = start.elapsed_time(end)
+    from softmax_topk_gb300 import multi
+    total_ms = multi.max_over_ranks(start.elapsed_time(end), device=dev)
     per_item_ms = [sum(evs[it][j].elapsed_time(evs[it][j + 1]) for it in range(args.steps))
                    / args.steps for j in range(n_items)]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     step_bytes = sum(u[1] for u in units)
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = multi.whole_job_rate(step_bytes, world, ms_per_step * 1e-3) / 1e9
 
     e2e = run_e2e(st, dev, args) if rank == 0 else None
     if world > 1:
