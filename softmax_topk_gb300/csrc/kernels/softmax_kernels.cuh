@@ -449,32 +449,43 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
 // with streaming stores.  With one CTA per row there is no exchange between
 // SMs at all: each row costs one __syncthreads-level merge.
 // bf16 outputs use the cheaper degree-4 exponential (see ops.cuh).
-template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER>
-__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2)
-stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
-                   int aligned) {
+// ALIGNED (rows start on 16-byte boundaries) selects 128-bit loads and stores;
+// otherwise the same register layout is filled element by element.  Chunks
+// lying wholly inside the CTA's range skip the per-vector range checks.
+template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER, bool ALIGNED>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
+stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols) {
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV;
     constexpr bool FAST = fast_exp_for<TO>();
-    constexpr int64_t STEP = int64_t(THREADS) * UNROLL;
+    constexpr int STEP = THREADS * UNROLL;  // vectors per chunk
     __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
-    const int64_t nv = (cols + EPV - 1) / EPV;
-    const int64_t per_cta = (nv + CLUSTER - 1) / CLUSTER;
-    const int64_t begin = int64_t(rank) * per_cta;
-    const int64_t end = begin + per_cta < nv ? begin + per_cta : nv;
-    const int64_t nchunks = end > begin ? (end - begin + STEP - 1) / STEP : 0;
+    const int nv = (cols + EPV - 1) / EPV;
+    const int per_cta = (nv + CLUSTER - 1) / CLUSTER;
+    const int begin = int(rank) * per_cta;
+    const int len = max(0, min(per_cta, nv - begin));  // vectors of this CTA
+    const int nchunks = (len + STEP - 1) / STEP;
     const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     if (CLUSTER > 1) cluster_sync();
 
-    auto load_chunk = [&](const TI* xr, int64_t c, uint64_t policy, float* e) {
-        const int64_t v0 = begin + c * STEP + threadIdx.x;
+    // vectors tid + k*THREADS (k < UNROLL) of chunk c, relative to `begin`
+    auto load_chunk = [&](const TI* xs, int c, uint64_t policy, float* e) {
+        const int v0 = c * STEP + int(threadIdx.x);
+        const bool full = c * STEP + STEP <= len;
 #pragma unroll
         for (int k = 0; k < UNROLL; ++k) {
-            const int64_t v = v0 + int64_t(k) * THREADS;
-            if (v < end) {
-                if (aligned) load_slot_policy(xr, v, policy, e + k * EPV);
-                else load_slot(xr, v, cols, false, e + k * EPV);
+            const int v = v0 + k * THREADS;
+            if (full || v < len) {
+                if constexpr (ALIGNED) {
+                    unpack(ld_policy_v4(xs + v * EPV, policy), e + k * EPV, TI());
+                } else {
+#pragma unroll
+                    for (int q = 0; q < EPV; ++q) {
+                        const int j = (begin + v) * EPV + q;
+                        e[k * EPV + q] = j < cols ? to_f32(xs[v * EPV + q]) : kNegInf;
+                    }
+                }
             } else {
 #pragma unroll
                 for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
@@ -484,13 +495,13 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
 
     int parity = 0;
     for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
-        const TI* xr = x + row * int64_t(cols);
-        TO* yr = y + row * int64_t(cols);
+        const TI* xs = x + row * int64_t(cols) + int64_t(begin) * EPV;
+        TO* ys = y + row * int64_t(cols) + int64_t(begin) * EPV;
         // pass 1: running (m, d), one rescale per chunk of UNROLL vectors
         float m = kNegInf, d = 0.f;
-        for (int64_t c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < nchunks; ++c) {
             float e[EPC];
-            load_chunk(xr, c, keep, e);
+            load_chunk(xs, c, keep, e);
             const float m_new = fmaxf(m, max_of<EPC>(e));
             const float s = exp_sum<EPC, FAST>(e, m_new);
             d = d * rescale(m, m_new) + s;
@@ -499,16 +510,27 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
         const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m, d, parity, rank);
         const float inv_d = 1.0f / md.y;
         // pass 2, last chunk first: y = e^(x - m) / d
-        for (int64_t c = nchunks - 1; c >= 0; --c) {
+        for (int c = nchunks - 1; c >= 0; --c) {
             float e[EPC];
-            load_chunk(xr, c, drop, e);
+            load_chunk(xs, c, drop, e);
             exp_shift_sum<EPC, FAST>(e, md.x);
             scale_all<EPC>(e, inv_d);
-            const int64_t v0 = begin + c * STEP + threadIdx.x;
+            const int v0 = c * STEP + int(threadIdx.x);
+            const bool full = c * STEP + STEP <= len;
 #pragma unroll
             for (int k = 0; k < UNROLL; ++k) {
-                const int64_t v = v0 + int64_t(k) * THREADS;
-                if (v < end) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
+                const int v = v0 + k * THREADS;
+                if (full || v < len) {
+                    if constexpr (ALIGNED) {
+                        VecStore<TO, EPV>::run(ys + v * EPV, e + k * EPV);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < EPV; ++q) {
+                            const int j = (begin + v) * EPV + q;
+                            if (j < cols) ys[v * EPV + q] = from_f32<TO>(e[k * EPV + q]);
+                        }
+                    }
+                }
             }
         }
     }

@@ -92,9 +92,14 @@ struct SoftmaxFamily {
         }
     }
     static constexpr int STREAM_UNROLL = stream_unroll<TI>();
-    static Kernel streaming(int cluster) {
-        return cluster == 1 ? stream_rows_kernel<TI, TO, kStreamThreads, STREAM_UNROLL, 1>
-                            : stream_rows_kernel<TI, TO, kStreamThreads, STREAM_UNROLL, 8>;
+    using StreamKernel = void (*)(const TI*, TO*, int64_t, int);
+    static StreamKernel streaming(int cluster, bool aligned) {
+        constexpr int T = kStreamThreads, U = STREAM_UNROLL;
+        if (aligned)
+            return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, true>
+                                : stream_rows_kernel<TI, TO, T, U, 8, true>;
+        return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, false>
+                            : stream_rows_kernel<TI, TO, T, U, 8, false>;
     }
 
     // Largest cluster size of the ONCHIP family the current device can run.
@@ -185,7 +190,7 @@ struct SoftmaxFamily {
                 q.vectors_per_thread = STREAM_UNROLL;
                 q.cluster = rows >= 2 * int64_t(dev->sms) ? 1 : 8;
                 {
-                    const int occ = blocks_per_sm(streaming(q.cluster), kStreamThreads);
+                    const int occ = blocks_per_sm(streaming(q.cluster, true), kStreamThreads);
                     const int64_t resident = q.cluster == 1
                         ? int64_t(dev->sms) * (occ > 0 ? occ : 1)
                         : kMaxClustersPerLaunch;
@@ -210,11 +215,15 @@ struct SoftmaxFamily {
             return launch_kernel(k, p.grid, p.threads, p.cluster, Ring::SMEM_BYTES, stream, xi, yo,
                                  rows, cols, ctl);
         }
+        if (p.path == OS_PATH_STREAM) {
+            StreamKernel k = streaming(p.cluster, aligned);
+            if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
+            return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, xi, yo, rows, cols);
+        }
         Kernel k = nullptr;
         switch (p.path) {
             case OS_PATH_WARP: k = warp(p.lanes_per_row, p.vectors_per_thread); break;
-            case OS_PATH_ONCHIP: k = onchip(p.threads, p.cluster); break;
-            default: k = streaming(p.cluster); break;
+            default: k = onchip(p.threads, p.cluster); break;
         }
         if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
         return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, xi, yo, rows, cols,
