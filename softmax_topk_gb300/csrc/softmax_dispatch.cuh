@@ -31,8 +31,8 @@ constexpr int kWarpThreads = 256;
 constexpr int kOnchipThreadsMax = 512;
 constexpr int kOnchipElemsPerThread = 32;
 constexpr int kStreamThreads = 512;
-// 4 vectors per thread per chunk (16 fp32 or 32 bf16 elements)
-template <typename TI> constexpr int stream_unroll() { return 4; }
+// vectors per thread per chunk: 8 fp32 or 4 bf16 (32 elements either way; measured best)
+template <typename TI> constexpr int stream_unroll() { return sizeof(TI) == 4 ? 8 : 4; }
 constexpr int kTmaMinCols = 8192;
 // AUTO sends rows longer than this many 16-byte vectors (16384 fp32, 32768
 // bf16 elements) to the two-pass streaming kernel: measured on GB300 it beats
