@@ -1,7 +1,7 @@
 // ops.cuh -- device building blocks shared by the softmax and TopK kernels.
 //
 //  * packed fp32 pair arithmetic (the sm_100-family f32x2 FMA/ADD/MUL forms),
-//  * the library's own fp32 exponential (no ex2.approx / MUFU),
+//  * exponentials: the library's own FMA-pipe fp32 exponential and the SFU's ex2,
 //  * the (m, d) online-normalizer state and its merge over lanes,
 //  * 128-bit vector loads/stores with bf16 <-> fp32 conversion,
 //  * thread-block-cluster helpers (rank, barrier, distributed shared memory).
@@ -65,7 +65,8 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 
 // ------------------------------------------------------------------ exp
-// e^z for z <= 88, in fp32, on the FMA pipe only.
+// e^z for z <= 88, in fp32, on the FMA pipe only: the library's accurate
+// exponential (os_exp_f32) and the rescale factors of the (m, d) merges.
 //
 //   z := max(z, -88)                      (-inf and NaN become -88: result 0)
 //   n  = rint(z log2 e)                   via the 1.5*2^23 rounding constant
@@ -93,59 +94,12 @@ constexpr float c6 = 0.0013843592f;
 
 // 2^n from t = kRound + n: the low bits of t's pattern hold n; shifting them
 // into the exponent field and adding the bias gives 2^n (n = -127 -> +0).
+// Written as one integer multiply-add (t_bits * 2^23 + bias, modulo 2^32),
+// which the FMA pipe executes, leaving the integer ALU pipe to other work.
 __device__ __forceinline__ float pow2_from_rounded(float t) {
-    return __uint_as_float((__float_as_uint(t) << 23) + 0x3f800000u);
-}
-
-__device__ __forceinline__ float2 exp2x(float2 z) {
-    using namespace expc;
-    z.x = fmaxf(z.x, kFloor);
-    z.y = fmaxf(z.y, kFloor);
-    const float2 t = fma2(z, splat2(kLog2e), splat2(kRound));
-    const float2 n = add2(t, splat2(-kRound));
-    float2 r = fma2(n, splat2(-kLn2Hi), z);
-    r = fma2(n, splat2(-kLn2Lo), r);
-    float2 p = fma2(splat2(c6), r, splat2(c5));
-    p = fma2(p, r, splat2(c4));
-    p = fma2(p, r, splat2(c3));
-    p = fma2(p, r, splat2(c2));
-    p = fma2(p, r, splat2(c1));
-    p = fma2(p, r, splat2(1.0f));
-    return mul2(p, make_float2(pow2_from_rounded(t.x), pow2_from_rounded(t.y)));
-}
-
-// Cheaper variant for results that are rounded to bf16 afterwards (relative
-// error ~3e-6 against bf16's 2^-9 = 2e-3 rounding): ln 2 reduction with one
-// constant and a degree-4 minimax polynomial (same fit, degree 4).
-namespace expc4 {
-constexpr float kLn2 = 0.693147182e+00f;  // fp32(ln 2)
-constexpr float c1 = 0.99996674f;
-constexpr float c2 = 0.5000302f;
-constexpr float c3 = 0.1678763f;
-constexpr float c4 = 0.041513626f;
-}  // namespace expc4
-
-__device__ __forceinline__ float2 exp2x_bf16out(float2 z) {
-    using expc::kFloor;
-    using expc::kLog2e;
-    using expc::kRound;
-    z.x = fmaxf(z.x, kFloor);
-    z.y = fmaxf(z.y, kFloor);
-    const float2 t = fma2(z, splat2(kLog2e), splat2(kRound));
-    const float2 n = add2(t, splat2(-kRound));
-    const float2 r = fma2(n, splat2(-expc4::kLn2), z);
-    float2 p = fma2(splat2(expc4::c4), r, splat2(expc4::c3));
-    p = fma2(p, r, splat2(expc4::c2));
-    p = fma2(p, r, splat2(expc4::c1));
-    p = fma2(p, r, splat2(1.0f));
-    return mul2(p, make_float2(pow2_from_rounded(t.x), pow2_from_rounded(t.y)));
-}
-
-// e^z of a pair, accurate (FAST = false) or for bf16 results (FAST = true).
-template <bool FAST>
-__device__ __forceinline__ float2 exp_pair(float2 z) {
-    if constexpr (FAST) return exp2x_bf16out(z);
-    else return exp2x(z);
+    uint32_t b;
+    asm("mad.lo.u32 %0, %1, 8388608, 1065353216;" : "=r"(b) : "r"(__float_as_uint(t)));
+    return __uint_as_float(b);
 }
 
 __device__ __forceinline__ float exp1(float z) {
@@ -162,6 +116,44 @@ __device__ __forceinline__ float exp1(float z) {
     p = fmaf(p, r, c1);
     p = fmaf(p, r, 1.0f);
     return p * pow2_from_rounded(t);
+}
+
+// ------------------------------------------------------------------ exp (SFU)
+// The streaming loops take e^z as 2^(z log2 e) with the special-function
+// unit's base-2 exponential (PTX ex2.approx.ftz.f32): one SFU instruction
+// per element and two FMA-pipe operations per pair, against the dozen of the
+// polynomial above.  Blackwell Ultra doubled the SFU's ex2 rate for exactly
+// this use, which leaves these kernels bound by HBM instead of by issue.
+// ex2 maps -inf to +0, NaN to NaN, and flushes results below 2^-126 to +0.
+// Error of e^z: the product t = z log2 e is rounded once (relative error of
+// the result <= 2^-24 |z|); the accurate form splits log2 e into two fp32
+// constants so that the constant's own rounding adds nothing; ex2 adds a few
+// ulp.  The softmax tests bound the result over z in [-87, 0].
+__device__ __forceinline__ float ex2_sfu(float t) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
+namespace expc {
+constexpr float kLog2eLo = 1.925963034e-08f;  // log2 e - kLog2e
+}  // namespace expc
+
+// e^z of a pair: accurate (FAST = false, fp32 results) or with log2 e rounded
+// to fp32 (FAST = true, for results rounded to bf16 afterwards).
+template <bool FAST>
+__device__ __forceinline__ float2 exp_pair(float2 z) {
+    float2 t;
+    if constexpr (FAST) t = mul2(z, splat2(expc::kLog2e));
+    else t = fma2(z, splat2(expc::kLog2e), mul2(z, splat2(expc::kLog2eLo)));
+    return make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
+}
+
+// e^z / d of a pair for bf16 results, folded into one exponent:
+// 2^(z log2 e - log2 d), with neg_log2_d = -log2 d.
+__device__ __forceinline__ float2 exp_pair_div(float2 z, float neg_log2_d) {
+    const float2 t = fma2(z, splat2(expc::kLog2e), splat2(neg_log2_d));
+    return make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
 }
 
 // ------------------------------------------------------------------ (m, d)
@@ -242,6 +234,27 @@ __device__ __forceinline__ void unpack(const uint4& v, float* out, __nv_bfloat16
         out[2 * i] = __uint_as_float(w[i] << 16);
         out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
+}
+
+// (lo - m, hi - m) of a word holding two bf16 values, widened exactly and
+// subtracted in one mixed-precision instruction each (no separate unpack).
+__device__ __forceinline__ float2 sub_bf16x2(uint32_t w, float m) {
+    float2 z;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(z.x), "=f"(z.y) : "r"(w), "f"(m));
+    return z;
+}
+
+// Lane-wise maximum of two words of two bf16 values each.
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float bf16x2_max_to_f32(uint32_t w) {
+    return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -70,12 +70,16 @@ __device__ __forceinline__ void store_slot(TO* row, int64_t v, int cols, bool al
     }
 }
 
+// The shift used for e^(x - m): m itself, or 0 where m = -inf (every x seen
+// so far is -inf, so every term is e^-inf = 0, the identity state's d).
+__device__ __forceinline__ float finite_shift(float m) { return m > kNegInf ? m : 0.f; }
+
 // e[i] := e^(e[i] - m) for all N entries, returning the sum (pairs on f32x2).
 template <int N, bool FAST = false>
 __device__ __forceinline__ float exp_shift_sum(float* e, float m) {
     static_assert(N % 2 == 0, "pairs");
     float2 acc = make_float2(0.f, 0.f);
-    const float2 neg_m = splat2(-m);
+    const float2 neg_m = splat2(-finite_shift(m));
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
         float2 z = add2(make_float2(e[i], e[i + 1]), neg_m);
@@ -92,7 +96,7 @@ template <int N, bool FAST = false>
 __device__ __forceinline__ float exp_sum(const float* e, float m) {
     static_assert(N % 2 == 0, "pairs");
     float2 acc = make_float2(0.f, 0.f);
-    const float2 neg_m = splat2(-m);
+    const float2 neg_m = splat2(-finite_shift(m));
 #pragma unroll
     for (int i = 0; i < N; i += 2)
         acc = add2(acc, exp_pair<FAST>(add2(make_float2(e[i], e[i + 1]), neg_m)));
@@ -439,6 +443,74 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
 }
 
 // ---------------------------------------------------------------------------
+// Chunk arithmetic of the streaming kernel.  A chunk is UNROLL 16-byte
+// vectors per thread, kept as raw words: bf16 inputs are never unpacked by
+// shifts -- their maximum is taken on packed pairs (max.bf16x2) and x - m is
+// formed by mixed-precision subtraction straight from the halves.
+template <typename TI, int UNROLL>
+struct Chunk {
+    uint4 raw[UNROLL];
+    static constexpr int EPV = VecTraits<TI>::EPV;
+
+    __device__ __forceinline__ float max() const {
+        if constexpr (sizeof(TI) == 2) {
+            uint32_t w = raw[0].x;
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+                if (k > 0) w = max_bf16x2(w, raw[k].x);
+                w = max_bf16x2(w, raw[k].y);
+                w = max_bf16x2(w, raw[k].z);
+                w = max_bf16x2(w, raw[k].w);
+            }
+            return bf16x2_max_to_f32(w);
+        } else {
+            float m = __uint_as_float(raw[0].x);
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+                m = max3(m, __uint_as_float(raw[k].x), __uint_as_float(raw[k].y));
+                m = max3(m, __uint_as_float(raw[k].z), __uint_as_float(raw[k].w));
+            }
+            return m;
+        }
+    }
+
+    // e[i] = x_i - m for the UNROLL * EPV elements (m = -inf: x_i itself)
+    __device__ __forceinline__ void shifted(float m, float* e) const {
+        m = finite_shift(m);
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+            const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+            if constexpr (sizeof(TI) == 2) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 z = sub_bf16x2(w[i], m);
+                    e[k * 8 + 2 * i] = z.x;
+                    e[k * 8 + 2 * i + 1] = z.y;
+                }
+            } else {
+                const float2 a = add2(make_float2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                      splat2(-m));
+                const float2 b = add2(make_float2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                      splat2(-m));
+                e[k * 4] = a.x;
+                e[k * 4 + 1] = a.y;
+                e[k * 4 + 2] = b.x;
+                e[k * 4 + 3] = b.y;
+            }
+        }
+    }
+};
+
+// sum over N entries of e^(z_i), z given
+template <int N, bool FAST>
+__device__ __forceinline__ float exp_sum_z(const float* z) {
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) acc = add2(acc, exp_pair<FAST>(make_float2(z[i], z[i + 1])));
+    return acc.x + acc.y;
+}
+
+// ---------------------------------------------------------------------------
 // stream_rows: one CTA (or a cluster) per row, persistent over rows; CTA
 // `rank` owns a contiguous range of vector slots and reads it twice.
 // Pass 1 keeps a running (m, d) per thread with one rescale per chunk of
@@ -448,7 +520,7 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
 // L2), marks its loads evict_first (last use) and writes y = e^(x - m) / d
 // with streaming stores.  With one CTA per row there is no exchange between
 // SMs at all: each row costs one __syncthreads-level merge.
-// bf16 outputs use the cheaper degree-4 exponential (see ops.cuh).
+// bf16 outputs fold 1/d into the exponent (one FMA and one ex2 per element).
 // ALIGNED (rows start on 16-byte boundaries) selects 128-bit loads and stores;
 // otherwise the same register layout is filled element by element.  Chunks
 // lying wholly inside the CTA's range skip the per-vector range checks.
@@ -469,26 +541,29 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
     const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     if (CLUSTER > 1) cluster_sync();
 
-    // vectors tid + k*THREADS (k < UNROLL) of chunk c, relative to `begin`
-    auto load_chunk = [&](const TI* xs, int c, uint64_t policy, float* e) {
+    // vectors tid + k*THREADS (k < UNROLL) of chunk c, relative to `begin`;
+    // slots past the end (and, unaligned, columns past `cols`) read as -inf
+    auto load_chunk = [&](const TI* xs, int c, uint64_t policy, Chunk<TI, UNROLL>& ch) {
         const int v0 = c * STEP + int(threadIdx.x);
         const bool full = c * STEP + STEP <= len;
+        const uint32_t neg_inf_word = sizeof(TI) == 2 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
         for (int k = 0; k < UNROLL; ++k) {
             const int v = v0 + k * THREADS;
             if (full || v < len) {
                 if constexpr (ALIGNED) {
-                    unpack(ld_policy_v4(xs + v * EPV, policy), e + k * EPV, TI());
+                    ch.raw[k] = ld_policy_v4(xs + v * EPV, policy);
                 } else {
+                    TI tmp[EPV];
 #pragma unroll
                     for (int q = 0; q < EPV; ++q) {
                         const int j = (begin + v) * EPV + q;
-                        e[k * EPV + q] = j < cols ? to_f32(xs[v * EPV + q]) : kNegInf;
+                        tmp[q] = j < cols ? xs[v * EPV + q] : from_f32<TI>(kNegInf);
                     }
+                    ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
                 }
             } else {
-#pragma unroll
-                for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
+                ch.raw[k] = make_uint4(neg_inf_word, neg_inf_word, neg_inf_word, neg_inf_word);
             }
         }
     };
@@ -500,21 +575,31 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
         // pass 1: running (m, d), one rescale per chunk of UNROLL vectors
         float m = kNegInf, d = 0.f;
         for (int c = 0; c < nchunks; ++c) {
-            float e[EPC];
-            load_chunk(xs, c, keep, e);
-            const float m_new = fmaxf(m, max_of<EPC>(e));
-            const float s = exp_sum<EPC, FAST>(e, m_new);
-            d = d * rescale(m, m_new) + s;
+            Chunk<TI, UNROLL> ch;
+            load_chunk(xs, c, keep, ch);
+            const float m_new = fmaxf(m, ch.max());
+            float z[EPC];
+            ch.shifted(m_new, z);
+            d = d * rescale(m, m_new) + exp_sum_z<EPC, FAST>(z);
             m = m_new;
         }
         const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m, d, parity, rank);
-        const float inv_d = 1.0f / md.y;
+        const float2 inv_d = splat2(1.0f / md.y);
+        const float neg_log2_d = -__log2f(md.y);  // bf16 results: 2^(z log2 e - log2 d)
         // pass 2, last chunk first: y = e^(x - m) / d
         for (int c = nchunks - 1; c >= 0; --c) {
+            Chunk<TI, UNROLL> ch;
+            load_chunk(xs, c, drop, ch);
             float e[EPC];
-            load_chunk(xs, c, drop, e);
-            exp_shift_sum<EPC, FAST>(e, md.x);
-            scale_all<EPC>(e, inv_d);
+            ch.shifted(md.x, e);
+#pragma unroll
+            for (int i = 0; i < EPC; i += 2) {
+                const float2 z = make_float2(e[i], e[i + 1]);
+                const float2 p = FAST ? exp_pair_div(z, neg_log2_d)
+                                      : mul2(exp_pair<false>(z), inv_d);
+                e[i] = p.x;
+                e[i + 1] = p.y;
+            }
             const int v0 = c * STEP + int(threadIdx.x);
             const bool full = c * STEP + STEP <= len;
 #pragma unroll

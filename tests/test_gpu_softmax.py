@@ -163,6 +163,24 @@ def test_all_neg_inf_row_does_not_disturb_others(st):
     assert_softmax_close(xx, y[keep].double().cpu().numpy(), oracle.softmax(xx), "f32", "others")
 
 
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+def test_wide_exponent_range(st, pair, path):
+    """One entry at the row maximum and the rest spread over [max - 87.3, max - 20],
+    so that d stays close to 1 and e^(x - m) / d sweeps the normal fp32 range
+    down to FLT_MIN: the exponential's error grows with |x - m|, and this is
+    where it is largest.  Row offsets from -300 to +300 make x - m a rounded
+    difference for fp32 inputs."""
+    rows, cols = 12, 20000
+    rng = np.random.default_rng(17)
+    x64 = rng.uniform(-87.3, -20.0, size=(rows, cols))
+    x64[:, 4321] = 0.0
+    x64 += np.linspace(-300.0, 300.0, rows)[:, None]
+    x = torch.tensor(x64, dtype=torch.float64).to(DT[pair[0]]).cuda()
+    e = _check(st, x, pair[1], path, f"wide range {pair} {path}")
+    assert e["max_rel"] <= {"f32": 1e-5, "bf16": 8e-3}[pair[1]]
+
+
 @pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
 @pytest.mark.parametrize("cols", [100, 4096, 30000, 100000])
 def test_misaligned_pointers(st, pair, cols):
