@@ -167,9 +167,12 @@ os_status os_device_status(os_stream_t stream);
  *   os_set_wait_timeout_ns: bound of each device-side wait, 1 us .. 10 s
  *     (OS_ERR_SHAPE outside that range).
  *   os_set_fault_injection: 0 = off (default); 1 = in every following launch
- *     the first CTA never issues its first bulk copy, so its wait must run out
- *     (exercises the bounded-wait path; the outputs of that launch are
- *     garbage).  Other values: OS_ERR_SHAPE.
+ *     one CTA withholds data that another CTA waits for, so that wait must run
+ *     out (exercises the bounded-wait path; the outputs of that launch are
+ *     garbage): in the bulk-copy ring softmax (OS_PATH_ONCHIP rows held in
+ *     shared memory) the first CTA never issues its first copy; in the fused
+ *     TopK, when a row is split over a cluster, CTA 1 of the first cluster
+ *     never sends its list to CTA 0.  Other values: OS_ERR_SHAPE.
  */
 os_status os_set_wait_timeout_ns(uint64_t ns);
 os_status os_set_fault_injection(int32_t mode);

@@ -1,11 +1,9 @@
 // Fused softmax + TopK: kernel choice and launch.
 //
-// A row is split over a cluster of CLUSTER CTAs of 512 threads; CLUSTER is
-// the smallest power of two (up to 8) whose segments are at most 26000
-// elements (two CTAs of about 100 KB of shared memory fit one SM), and rows
-// longer than 8 tiles of 32768 elements loop over several tiles per CTA.  The
-// tile frame is dynamic shared memory sized to the segment (at most one
-// tile), staged by four bulk copies.
+// Persistent CTAs of 512 threads, two per SM, each taking whole rows in
+// chunks of 8 16-byte blocks per thread (16384 fp32); with fewer rows than
+// resident CTAs a row is split over a cluster of S CTAs (S <= 8, and no more
+// CTAs than the row has chunks) that merge through distributed shared memory.
 #include "host_common.h"
 #include "internal.h"
 #include "kernels/topk_kernel.cuh"
@@ -13,48 +11,38 @@
 namespace os {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkTile = 32768;
+constexpr int kTopkVpt = 8;  // 16-byte blocks per thread per chunk
 constexpr int kTopkKmax = 64;
-constexpr int kTopkCap = 512;
-constexpr int kTopkChunks = 4;
-constexpr int kTopkMaxCluster = 8;
-constexpr int kTopkSegmentTarget = 26000;  // longest segment per CTA before adding CTAs
+constexpr int kTopkCap = 2048;
 
-using TopkKernel = void (*)(const float*, float*, int*, int64_t, int, int, KernelCtl);
-
-template <int C>
-constexpr TopkKernel topk_instance() {
-    return topk_rows_kernel<kTopkThreads, C, kTopkTile, kTopkKmax, kTopkCap, kTopkChunks>;
-}
-
-static TopkKernel topk_kernel_for(int cluster) {
-    switch (cluster) {
-        case 1: return topk_instance<1>();
-        case 2: return topk_instance<2>();
-        case 4: return topk_instance<4>();
-        default: return topk_instance<8>();
-    }
-}
-
-static int frame_bytes(int64_t cols, int cluster) {
-    const int64_t seg = ceil_div(cols, cluster);
-    const int64_t tile = seg < kTopkTile ? seg : kTopkTile;
-    return static_cast<int>(((tile + 8) * 4 + 15) / 16 * 16);
+static auto topk_kernel() {
+    return topk_rows_kernel<kTopkThreads, kTopkVpt, kTopkKmax, kTopkCap>;
 }
 
 os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
     (void)K;
-    if (!device_info()) return OS_ERR_CUDA;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return OS_ERR_CUDA;
+    const int per_sm = blocks_per_sm(topk_kernel(), kTopkThreads);
+    if (per_sm <= 0) return OS_ERR_CUDA;
+    const int64_t resident = int64_t(dev->sms) * per_sm;
+    const int64_t blocks = (cols + 3) / 4 + 1;  // upper bound over the 4 possible row offsets
+    const int64_t chunks = ceil_div(blocks, int64_t(kTopkThreads) * kTopkVpt);
+    int64_t S = rows >= resident ? 1 : resident / rows;
+    if (S > kTopkMaxCluster) S = kTopkMaxCluster;
+    if (S > chunks) S = chunks;
+    if (S < 1) S = 1;
+    int64_t clusters = resident / S;
+    if (clusters > rows) clusters = rows;
+    if (clusters > kMaxClustersPerLaunch) clusters = kMaxClustersPerLaunch;
     os_plan q = {};
-    q.path = OS_PATH_ONCHIP;
+    q.path = OS_PATH_STREAM;
     q.threads = kTopkThreads;
-    q.cluster = pow2_at_least(ceil_div(cols, kTopkSegmentTarget));
-    if (q.cluster > kTopkMaxCluster) q.cluster = kTopkMaxCluster;
-    const int64_t seg = ceil_div(cols, q.cluster);
-    q.vectors_per_thread = static_cast<int32_t>(ceil_div(seg < kTopkTile ? seg : kTopkTile,
-                                                         4 * kTopkThreads));
-    q.stages = kTopkChunks;
-    q.grid = min64(rows, kMaxClustersPerLaunch) * q.cluster;
+    q.vectors_per_thread = kTopkVpt;
+    q.cluster = static_cast<int32_t>(S);
+    q.lanes_per_row = 0;
+    q.stages = 0;
+    q.grid = clusters * S;
     *p = q;
     return OS_OK;
 }
@@ -62,11 +50,10 @@ os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
 cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* idx,
                         int64_t rows, int cols, int K, const KernelCtl& ctl,
                         cudaStream_t stream) {
-    TopkKernel k = topk_kernel_for(p.cluster);
-    const int smem = frame_bytes(cols, p.cluster);
-    if (!prepare_kernel(k, p.cluster, frame_bytes(kTopkTile, 1))) return cudaErrorInvalidValue;
-    return launch_kernel(k, p.grid, p.threads, p.cluster, smem, stream, x, vals,
-                         reinterpret_cast<int*>(idx), rows, cols, K, ctl);
+    auto k = topk_kernel();
+    if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
+    return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, x, vals,
+                         reinterpret_cast<int*>(idx), rows, cols, K, p.cluster, ctl);
 }
 
 }  // namespace os

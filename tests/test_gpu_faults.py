@@ -1,5 +1,6 @@
-"""Bounded device-side waits: a bulk copy that never arrives (injected on the
-host: the first CTA skips issuing it) makes the wait run out after the
+"""Bounded device-side waits: data that never arrives (injected on the host: in
+the softmax ring kernel the first CTA skips its first bulk copy, in the fused
+TopK one CTA of a cluster never sends its list) makes the wait run out after the
 configured time; the kernel finishes, the status call reports OS_ERR_TIMEOUT,
 and the context stays usable for correct work afterwards.  Nothing traps or
 hangs."""
@@ -55,6 +56,7 @@ def test_softmax_wait_times_out_and_recovers(st, shape, dtype):
 
 def test_topk_wait_times_out_and_recovers(st):
     x = torch.randn(16, 50257, device="cuda") * 4
+    assert st.os_topk_plan(16, 50257, 8)["cluster"] > 1    # rows split over a cluster
     st.os_device_status(_stream())
     st.os_set_wait_timeout_ns(20 * 10 ** 6)
     st.os_set_fault_injection(1)
