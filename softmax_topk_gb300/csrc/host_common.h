@@ -71,7 +71,9 @@ bool prepare_kernel(void (*kernel)(KArgs...), int cluster, int smem) {
     static std::map<std::pair<int, const void*>, std::pair<int, int>> done;  // smem, cluster
     std::lock_guard<std::mutex> lock(mu);
     auto& d = done[{dev, k}];
-    if (smem > 48 * 1024 && smem > d.first) {
+    // static plus dynamic shared memory above 48 KB needs the opt-in, so the
+    // limit is raised for any dynamic size (a no-op below it)
+    if (smem > d.first) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess) {
             cudaGetLastError();

@@ -1,4 +1,5 @@
-// topk_kernel.cuh -- fused softmax + TopK: one read of x, K probabilities out.
+// topk_kernel.cuh -- fused softmax + TopK: one read of x from HBM, K
+// probabilities out.
 //
 // "Online normalizer calculation for softmax" (notes), section 4, fuses the
 // online normalizer with TopK: one pass keeps (m, d) and the K best logits u
@@ -6,30 +7,31 @@
 // v_i = e^(u_i - m_V) / d_V at the end (selecting on logits is exact because
 // softmax is monotone).  The notes insert every element into a sorted list
 // behind a rejection test against the list's last entry.  Here the rejection
-// threshold comes from the data itself and the list is built once, from the
-// few survivors:
+// threshold comes from the data itself, and only the few survivors are ever
+// compared with one another:
 //
-//   * a CTA streams its segment of the row (the whole row, or one of S <= 8
-//     segments of a thread-block cluster when rows are too few to fill the
-//     GPU) in chunks of U 16-byte blocks per thread.  Every thread folds each
-//     chunk into its running (m, d) (chunk maximum, then the sum of e^(x - max)
-//     on the SFU: one rescale per chunk) and into its running maximum;
-//   * threshold: each warp sorts its 32 thread maxima (bitonic network over
+//   pass 1 (HBM): a CTA streams its segment of the row (the whole row, or one
+//     of S <= 8 segments of a thread-block cluster when rows are too few to
+//     fill the GPU) in chunks of U 16-byte blocks per thread.  Every thread
+//     folds each chunk into its running (m, d) (chunk maximum, then the sum of
+//     e^(x - max) on the SFU: one FMA and one ex2 per element, one rescale
+//     per chunk) and into its running maximum, and keeps each block's maximum
+//     as a rounded-up 16-bit key in shared memory;
+//   threshold: each warp sorts its 32 thread maxima (bitonic network over
 //     shuffles); the smallest of the warps' j*-th largest (j* = ceil(K /
 //     warps) - 1) has at least K elements of the segment at or above it (that
 //     many threads of every warp hold one), so nothing below it can be in the
-//     top K.  T0, taken after the first chunk, filters every chunk as it
-//     streams by: elements at or above T0 go to a shared-memory candidate
-//     buffer, a warp reserving its slots with one atomic.  T, taken the same
-//     way over the whole segment at its end, is higher (more elements behind
-//     each thread maximum) and decides which candidates are ranked;
-//   * selection: every candidate at or above T gets its rank, the number of
-//     candidates that beat it (one warp per candidate, the lanes splitting the
-//     count); rank r < K puts it in slot r of the list.  If the candidates
-//     overflow the buffer (heavy ties, or rows whose first chunk is far below
-//     the rest), an exact path finds the K-th largest key of the segment by
-//     bisection and admits the ties at it in column order;
-//   * output: the CTA's (m, d) is the (+)-fold of its threads' states.  With
+//     top K;
+//   pass 2 (L2): only the blocks whose key reaches the threshold's are read
+//     again (about one in a hundred for random data), and their elements at
+//     or above it become the candidates, a warp reserving its slots in the
+//     shared-memory buffer with one atomic;
+//   selection: each candidate's rank is the number of candidates that beat it
+//     (one warp per candidate, the lanes splitting the count); rank r < K puts
+//     it in slot r of the list.  If the candidates overflow the buffer (heavy
+//     ties at the threshold), an exact path finds the K-th largest key of the
+//     segment by bisection and admits the ties at it in column order;
+//   output: the CTA's (m, d) is the (+)-fold of its threads' states.  With
 //     S = 1 the CTA writes v = e^(u - m)/d and the indices, best first.  With
 //     S > 1 every CTA pushes its state and list into CTA 0 of the cluster with
 //     st.async (completing CTA 0's barrier), and CTA 0 ranks the lists against
@@ -46,12 +48,13 @@
 #pragma once
 
 #include <climits>
-#include <type_traits>
 
 #include "ops.cuh"
 #include "softmax_kernels.cuh"
 
 namespace os {
+
+constexpr float kLn2f = 0.693147182f;  // fp32(ln 2)
 
 struct Cand {
     float v;
@@ -138,11 +141,11 @@ constexpr int kTopkMaxCluster = 8;
 template <int THREADS, int KMAX, int CAP>
 struct TopkSmem {
     uint64_t xbar[2];
-    float warp_thr0[THREADS / 32];  // first-chunk bound
-    float warp_thr[THREADS / 32];   // whole-segment bound
+    float warp_thr[THREADS / 32];
     float2 warp_state[THREADS / 32];
     int scratch[THREADS / 32];
     int ncand[2];  // candidate counters of alternate rows
+    int nflag[2];  // listed-block counters of alternate rows
     int flag;
     Cand cand[CAP];
     Cand list[KMAX];
@@ -150,14 +153,20 @@ struct TopkSmem {
     Cand xlist[2][kTopkMaxCluster][KMAX];
 };
 
-// The U blocks of a chunk that one thread owns: element l of block k, and
-// bit 4k + l of `live` set where that element is a column of the segment
-// (other elements hold -inf).
-template <int U>
-struct TopkChunk {
-    float v[U][4];
-    uint32_t live;
+// Dynamic shared memory: per thread and block slot the maximum of the block
+// (as a 16-bit key rounded up, see block_key) for each group of chunks, and
+// the list of the blocks that pass 2 reads again.
+template <int THREADS, int U, int GROUPS, int FCAP>
+struct TopkDynSmem {
+    uint16_t bkey[GROUPS][U][THREADS];
+    int flagged[FCAP];
 };
+
+// Upper 16 bits of the order-preserving key, rounded up: block_key(x) >=
+// threshold_key(t) whenever x >= t, so a block whose key is below the
+// threshold's holds nothing at or above it.
+__device__ __forceinline__ uint32_t block_key(float x) { return (order_key(x) + 0xffffu) >> 16; }
+__device__ __forceinline__ uint32_t threshold_key(float t) { return order_key(t) >> 16; }
 
 // A CTA's segment of one row.
 struct TopkSegment {
@@ -167,60 +176,31 @@ struct TopkSegment {
     int b0, b1;            // the CTA's blocks of the row
 };
 
-template <int THREADS, int U, int KMAX, int CAP>
+template <int THREADS, int U, int KMAX, int CAP, int GROUPS, int FCAP>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2)
 topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __restrict__ idx,
                  int64_t rows, int cols, int K, int S, KernelCtl ctl) {
     constexpr int NW = THREADS / 32;
     constexpr int CHUNK = THREADS * U;  // 16-byte blocks per chunk
-    static_assert(U * 4 <= 32, "one mask bit per element of a chunk");
-    static_assert(CAP >= 128 && KMAX <= THREADS, "buffer sizes");
+    static_assert(CAP % 32 == 0 && CAP >= 128 && KMAX <= THREADS, "buffer sizes");
     __shared__ __align__(16) TopkSmem<THREADS, KMAX, CAP> sm;
+    extern __shared__ __align__(16) unsigned char dyn_raw[];
+    auto& dyn = *reinterpret_cast<TopkDynSmem<THREADS, U, GROUPS, FCAP>*>(dyn_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = S > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / S, nclusters = gridDim.x / S;
     const int jstar = min((K + NW - 1) / NW - 1, 31);
     const Cand pad{kNegInf, kNoIndex};
-    const uint64_t policy = l2_policy_evict_first();  // every element is read once
+    const uint64_t policy = l2_policy_evict_first();
 
     if (tid == 0) {
         mbar_init(&sm.xbar[0], 1);
         mbar_init(&sm.xbar[1], 1);
         mbar_init_fence();
         sm.ncand[0] = sm.ncand[1] = 0;
+        sm.nflag[0] = sm.nflag[1] = 0;
     }
     if (S > 1) cluster_sync(); else __syncthreads();
-
-    // the thread's blocks k0 .. k0 + NB - 1 of chunk c
-    auto load = [&](auto nb_tag, const TopkSegment& g, int c, int k0, uint64_t policy) {
-        constexpr int NB = decltype(nb_tag)::value;
-        TopkChunk<NB> ch;
-        uint32_t live = 0;
-        const float* xb = g.xr - g.head;  // 16-byte aligned; dereferenced only inside the row
-#pragma unroll
-        for (int k = 0; k < NB; ++k) {
-            const int b = g.b0 + c * CHUNK + (k0 + k) * THREADS + tid;
-            if (b < g.b1 && b >= g.full_lo && b < g.full_hi) {
-                const uint4 w = ld_policy_v4(xb + 4 * int64_t(b), policy);
-                ch.v[k][0] = __uint_as_float(w.x);
-                ch.v[k][1] = __uint_as_float(w.y);
-                ch.v[k][2] = __uint_as_float(w.z);
-                ch.v[k][3] = __uint_as_float(w.w);
-                live |= 0xfu << (4 * k);
-            } else {
-#pragma unroll
-                for (int l = 0; l < 4; ++l) {
-                    const int64_t col = 4 * int64_t(b) + l - g.head;
-                    const bool in = b < g.b1 && col >= 0 && col < cols;
-                    ch.v[k][l] = in ? g.xr[col] : kNegInf;
-                    live |= uint32_t(in) << (4 * k + l);
-                }
-            }
-        }
-        ch.live = live;
-        return ch;
-    };
-    using AllBlocks = std::integral_constant<int, U>;
 
     bool failed = false;  // a wait gave up: outputs are garbage, the status word says so
     int parity = 0;
@@ -240,72 +220,80 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             g.b0 = min(int(rank) * per, nb);
             g.b1 = min(g.b0 + per, nb);
         }
+        const float* xb = g.xr - g.head;  // 16-byte aligned; dereferenced only inside the row
         const int nchunks = (g.b1 - g.b0 + CHUNK - 1) / CHUNK;
+        const int G = max(1, (nchunks + GROUPS - 1) / GROUPS);  // chunks per group
+        const int ngroups = (nchunks + G - 1) / G;
         int* counter = &sm.ncand[parity];
-        if (tid == 0) *counter = 0;  // last used two rows ago
+        int* nflag = &sm.nflag[parity];
+        if (tid == 0) {  // last used two rows ago
+            *counter = 0;
+            *nflag = 0;
+        }
         if (tid < K) sm.list[tid] = pad;
 
-        // ---- one pass: running (m, d) and maximum; candidates >= T0
-        float m = kNegInf, d = 0.f, tmax = kNegInf, T0 = kNegInf;
+        // ---- pass 1 (HBM): running (m, d) and maximum; block maxima kept as keys
+        float m = kNegInf, d = 0.f, tmax = kNegInf;
         for (int c = 0; c < nchunks; ++c) {
-            const TopkChunk<U> ch = load(AllBlocks{}, g, c, 0, policy);
-            const auto& v = ch.v;
-            float cmax = kNegInf;
-#pragma unroll
-            for (int k = 0; k < U; ++k) cmax = max3(cmax, fmaxf(v[k][0], v[k][1]), fmaxf(v[k][2], v[k][3]));
-            float2 acc = make_float2(0.f, 0.f);
-            const float2 neg_m = splat2(-finite_shift(cmax));
+            float v[U][4];
 #pragma unroll
             for (int k = 0; k < U; ++k) {
-                acc = add2(acc, exp_pair<false>(add2(make_float2(v[k][0], v[k][1]), neg_m)));
-                acc = add2(acc, exp_pair<false>(add2(make_float2(v[k][2], v[k][3]), neg_m)));
-            }
-            const float m_new = fmaxf(m, cmax);
-            d = d * rescale(m, m_new) + (acc.x + acc.y) * rescale(cmax, m_new);
-            m = m_new;
-            tmax = fmaxf(tmax, cmax);
-            if (c == 0) {
-                const float sorted = warp_sort_desc(tmax);
-                if (lane == jstar) sm.warp_thr0[warp] = sorted;
-                __syncthreads();
-                T0 = sm.warp_thr0[0];
-#pragma unroll
-                for (int w = 1; w < NW; ++w) T0 = fminf(T0, sm.warp_thr0[w]);
-            }
-            // candidates of this chunk: one atomic per warp reserves the slots
-            int cnt = 0;
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                if (max3(fmaxf(v[k][0], v[k][1]), v[k][2], v[k][3]) >= T0) {
-#pragma unroll
-                    for (int l = 0; l < 4; ++l) cnt += v[k][l] >= T0 && ((ch.live >> (4 * k + l)) & 1u);
-                }
-            }
-            int incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(kFullMask, incl, o);
-                if (lane >= o) incl += t;
-            }
-            int base = 0;
-            if (lane == 31 && incl > 0) base = atomicAdd(counter, incl);
-            int pos = __shfl_sync(kFullMask, base, 31) + incl - cnt;
-            if (cnt > 0) {
-#pragma unroll
-                for (int k = 0; k < U; ++k)
+                const int b = g.b0 + c * CHUNK + k * THREADS + tid;
+                if (b < g.b1 && b >= g.full_lo && b < g.full_hi) {
+                    const uint4 w = ld_policy_v4(xb + 4 * int64_t(b), policy);
+                    v[k][0] = __uint_as_float(w.x);
+                    v[k][1] = __uint_as_float(w.y);
+                    v[k][2] = __uint_as_float(w.z);
+                    v[k][3] = __uint_as_float(w.w);
+                } else {
 #pragma unroll
                     for (int l = 0; l < 4; ++l) {
-                        if (v[k][l] >= T0 && ((ch.live >> (4 * k + l)) & 1u)) {
-                            const int col = int(4u * uint32_t(g.b0 + c * CHUNK + k * THREADS + tid) +
-                                                uint32_t(l) - uint32_t(g.head));
-                            if (pos < CAP) sm.cand[pos] = Cand{v[k][l], col};
-                            ++pos;
-                        }
+                        const int64_t col = 4 * int64_t(b) + l - g.head;
+                        v[k][l] = (b < g.b1 && col >= 0 && col < cols) ? g.xr[col] : kNegInf;
                     }
+                }
+            }
+            float bm[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) bm[k] = fmaxf(max3(v[k][0], v[k][1], v[k][2]), v[k][3]);
+            float cmax = bm[0];
+#pragma unroll
+            for (int k = 1; k < U; k += 2) cmax = max3(cmax, bm[k], bm[k + 1 < U ? k + 1 : k]);
+            // (m, d) against the new running maximum m': e^(x - m') is taken as
+            // 2^(x log2e - M_hi) (2^(-M_lo)), where M_hi + M_lo = m' log2e exactly
+            // (the residual of an FMA): one FMA and one SFU ex2 per element.
+            // Dropping log2e's own rounding costs 1.3e-8 |x - m'| relative per term.
+            {
+                const float m_new = fmaxf(m, cmax);
+                const float ms = finite_shift(m_new);
+                const float M_hi = ms * expc::kLog2e;
+                const float M_lo = fmaf(ms, expc::kLog2e, -M_hi);
+                const float2 L2 = splat2(expc::kLog2e), nM = splat2(-M_hi);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const float2 t0 = fma2(make_float2(v[k][0], v[k][1]), L2, nM);
+                    const float2 t1 = fma2(make_float2(v[k][2], v[k][3]), L2, nM);
+                    acc = add2(acc, make_float2(ex2_sfu(t0.x), ex2_sfu(t0.y)));
+                    acc = add2(acc, make_float2(ex2_sfu(t1.x), ex2_sfu(t1.y)));
+                }
+                const float keep = m == m_new ? 1.0f : ex2_sfu((m - m_new) * expc::kLog2e);
+                d = fmaf(d, keep, (acc.x + acc.y) * fmaf(-M_lo, kLn2f, 1.0f));
+                m = m_new;
+            }
+            tmax = fmaxf(tmax, cmax);
+            // block keys (thread-private slots): a group's first chunk writes, later ones raise
+            const int grp = c / G;
+            const bool first_of_group = c == grp * G;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                uint32_t key = block_key(bm[k]);
+                if (!first_of_group) key = max(key, uint32_t(dyn.bkey[grp][k][tid]));
+                dyn.bkey[grp][k][tid] = uint16_t(key);
             }
         }
 
-        // ---- T over the whole segment (>= T0): the candidates below it drop out
+        // ---- threshold T over the whole segment: at least K elements are >= T
         {
             const float sorted = warp_sort_desc(tmax);
             if (lane == jstar) sm.warp_thr[warp] = sorted;
@@ -314,7 +302,96 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
         float T = sm.warp_thr[0];
 #pragma unroll
         for (int w = 1; w < NW; ++w) T = fminf(T, sm.warp_thr[w]);
-        int n = *counter;
+        const uint32_t tk = threshold_key(T);
+
+        // ---- the blocks whose key reaches T's, listed (one atomic per warp)
+        {
+            int mine = 0;
+            for (int q = 0; q < ngroups; ++q) {
+                const int c_end = min(nchunks, (q + 1) * G);
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (dyn.bkey[q][k][tid] >= tk)
+                        for (int c = q * G; c < c_end; ++c)
+                            mine += g.b0 + c * CHUNK + k * THREADS + tid < g.b1;
+            }
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(kFullMask, incl, o);
+                if (lane >= o) incl += t;
+            }
+            int base = 0;
+            if (lane == 31 && incl > 0) base = atomicAdd(nflag, incl);
+            int pos = __shfl_sync(kFullMask, base, 31) + incl - mine;
+            if (mine > 0) {
+                for (int q = 0; q < ngroups; ++q) {
+                    const int c_end = min(nchunks, (q + 1) * G);
+#pragma unroll
+                    for (int k = 0; k < U; ++k)
+                        if (dyn.bkey[q][k][tid] >= tk)
+                            for (int c = q * G; c < c_end; ++c) {
+                                const int b = g.b0 + c * CHUNK + k * THREADS + tid;
+                                if (b < g.b1) {
+                                    if (pos < FCAP) dyn.flagged[pos] = b;
+                                    ++pos;
+                                }
+                            }
+                }
+            }
+        }
+        __syncthreads();
+        const int nf = *nflag;
+
+        // ---- pass 2 (L2): the listed blocks again; their elements >= T are the candidates
+        if (nf <= FCAP) {
+            for (int i0 = 0; i0 < nf; i0 += THREADS) {  // uniform
+                const int i = i0 + tid;
+                float v[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+                int b = 0;
+                if (i < nf) {
+                    b = dyn.flagged[i];
+                    if (b >= g.full_lo && b < g.full_hi) {
+                        const uint4 w = ld_policy_v4(xb + 4 * int64_t(b), policy);
+                        v[0] = __uint_as_float(w.x);
+                        v[1] = __uint_as_float(w.y);
+                        v[2] = __uint_as_float(w.z);
+                        v[3] = __uint_as_float(w.w);
+                    } else {
+#pragma unroll
+                        for (int l = 0; l < 4; ++l) {
+                            const int64_t col = 4 * int64_t(b) + l - g.head;
+                            if (col >= 0 && col < cols) v[l] = g.xr[col];
+                        }
+                    }
+                }
+                uint32_t hit = 0;  // bit l: element l is a candidate
+#pragma unroll
+                for (int l = 0; l < 4; ++l) {
+                    const int64_t col = 4 * int64_t(b) + l - g.head;
+                    hit |= uint32_t(i < nf && v[l] >= T && col >= 0 && col < cols) << l;
+                }
+                const int cnt = __popc(hit);
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(kFullMask, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                int base = 0;
+                if (lane == 31 && incl > 0) base = atomicAdd(counter, incl);
+                int pos = __shfl_sync(kFullMask, base, 31) + incl - cnt;
+#pragma unroll
+                for (int l = 0; l < 4; ++l) {
+                    if ((hit >> l) & 1u) {
+                        if (pos < CAP) sm.cand[pos] = Cand{v[l], int(4u * uint32_t(b) + uint32_t(l) - uint32_t(g.head))};
+                        ++pos;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        int n = nf <= FCAP ? *counter : CAP + 1;
 
         if (n > CAP) {
             // ---- exact path (heavy ties at T; rare): the K-th largest key of the
@@ -349,18 +426,18 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 admitted += round_total;
             }
             n = need;
-            T = kNegInf;  // all of them are ranked
             __syncthreads();
         }
 
-        // ---- selection: list[r] = the candidate >= T that r candidates beat (r < K)
+        // ---- selection: list[r] = the candidate that r candidates beat (r < K);
+        // one warp per candidate, the lanes splitting the count (the first 128
+        // candidates held in registers)
         {
             Cand reg[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) reg[j] = lane + 32 * j < n ? sm.cand[lane + 32 * j] : pad;
             for (int i = warp; i < n; i += NW) {
                 const Cand c = sm.cand[i];
-                if (c.v < T) continue;  // uniform over the warp
                 int r = 0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) r += beats(reg[j], c);

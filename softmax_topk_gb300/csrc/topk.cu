@@ -11,19 +11,23 @@
 namespace os {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkVpt = 8;  // 16-byte blocks per thread per chunk
+constexpr int kTopkVpt = 8;      // 16-byte blocks per thread per chunk
 constexpr int kTopkKmax = 64;
-constexpr int kTopkCap = 2048;
+constexpr int kTopkCap = 2048;   // candidates
+constexpr int kTopkGroups = 4;   // block keys kept per thread slot (groups of chunks)
+constexpr int kTopkFcap = 2048;  // blocks read again in pass 2
+constexpr int kTopkDynBytes =
+    int(sizeof(TopkDynSmem<kTopkThreads, kTopkVpt, kTopkGroups, kTopkFcap>));
 
 static auto topk_kernel() {
-    return topk_rows_kernel<kTopkThreads, kTopkVpt, kTopkKmax, kTopkCap>;
+    return topk_rows_kernel<kTopkThreads, kTopkVpt, kTopkKmax, kTopkCap, kTopkGroups, kTopkFcap>;
 }
 
 os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
     (void)K;
     const DeviceInfo* dev = device_info();
     if (!dev) return OS_ERR_CUDA;
-    const int per_sm = blocks_per_sm(topk_kernel(), kTopkThreads);
+    const int per_sm = blocks_per_sm(topk_kernel(), kTopkThreads, kTopkDynBytes);
     if (per_sm <= 0) return OS_ERR_CUDA;
     const int64_t resident = int64_t(dev->sms) * per_sm;
     const int64_t blocks = (cols + 3) / 4 + 1;  // upper bound over the 4 possible row offsets
@@ -51,8 +55,8 @@ cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* 
                         int64_t rows, int cols, int K, const KernelCtl& ctl,
                         cudaStream_t stream) {
     auto k = topk_kernel();
-    if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
-    return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, x, vals,
+    if (!prepare_kernel(k, p.cluster, kTopkDynBytes)) return cudaErrorInvalidValue;
+    return launch_kernel(k, p.grid, p.threads, p.cluster, kTopkDynBytes, stream, x, vals,
                          reinterpret_cast<int*>(idx), rows, cols, K, p.cluster, ctl);
 }
 
