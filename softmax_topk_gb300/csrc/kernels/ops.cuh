@@ -391,18 +391,6 @@ __device__ __forceinline__ bool cta_wait_bounded(uint64_t* bar, uint32_t parity,
     return flag[which] != 0;
 }
 
-// 16 bytes global -> shared memory by the calling thread, asynchronously
-// (L2 only, with an L2 eviction policy); completes in the thread's current
-// commit group.  Both addresses 16-byte aligned.
-__device__ __forceinline__ void cp_async_16(void* dst_smem, const void* src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-                 :: "r"(smem_addr(dst_smem)), "l"(src), "l"(policy) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most N of the thread's commit groups are still in flight.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,

@@ -153,12 +153,13 @@ struct TopkSmem {
     Cand xlist[2][kTopkMaxCluster][KMAX];
 };
 
-// Dynamic shared memory: per thread and block slot the maximum of the block
-// (as a 16-bit key rounded up, see block_key) for each group of chunks, and
-// the list of the blocks that pass 2 reads again.
+// Dynamic shared memory: per group of chunks and thread, the maximum of each
+// of the thread's U block slots (as a 16-bit key rounded up, see block_key;
+// U = 4 keys in 8 bytes), and the list of the blocks that pass 2 reads again.
 template <int THREADS, int U, int GROUPS, int FCAP>
 struct TopkDynSmem {
-    uint16_t bkey[GROUPS][U][THREADS];
+    static_assert(U == 4, "four 16-bit keys per 8-byte slot");
+    uint2 bkey[GROUPS][THREADS];
     int flagged[FCAP];
 };
 
@@ -282,21 +283,25 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 m = m_new;
             }
             tmax = fmaxf(tmax, cmax);
-            // block keys (thread-private slots): a group's first chunk writes, later ones raise
+            // block keys (thread-private slot): a group's first chunk writes, later ones raise
             const int grp = c / G;
-            const bool first_of_group = c == grp * G;
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                uint32_t key = block_key(bm[k]);
-                if (!first_of_group) key = max(key, uint32_t(dyn.bkey[grp][k][tid]));
-                dyn.bkey[grp][k][tid] = uint16_t(key);
+            uint2 key = make_uint2(block_key(bm[0]) | (block_key(bm[1]) << 16),
+                                   block_key(bm[2]) | (block_key(bm[3]) << 16));
+            if (c != grp * G) {
+                const uint2 old = dyn.bkey[grp][tid];
+                key = make_uint2(__vmaxu2(key.x, old.x), __vmaxu2(key.y, old.y));
             }
+            dyn.bkey[grp][tid] = key;
         }
 
-        // ---- threshold T over the whole segment: at least K elements are >= T
+        // ---- threshold T over the whole segment (at least K elements are >= T);
+        // the same barrier publishes each warp's (m, d)
         {
             const float sorted = warp_sort_desc(tmax);
             if (lane == jstar) sm.warp_thr[warp] = sorted;
+            float mm = m, dd = d;
+            group_merge<32>(mm, dd);
+            if (lane == 0) sm.warp_state[warp] = make_float2(mm, dd);
         }
         __syncthreads();
         float T = sm.warp_thr[0];
@@ -304,16 +309,26 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
         for (int w = 1; w < NW; ++w) T = fminf(T, sm.warp_thr[w]);
         const uint32_t tk = threshold_key(T);
 
-        // ---- the blocks whose key reaches T's, listed (one atomic per warp)
+        // ---- the blocks whose key reaches T's, listed (one atomic per warp).
+        // The keys are read in one batch: shared-memory round trips are slow
+        // while the SM's other CTA streams.
         {
-            int mine = 0;
-            for (int q = 0; q < ngroups; ++q) {
-                const int c_end = min(nchunks, (q + 1) * G);
+            uint32_t hit = 0;  // bit q * U + k: slot k of group q reaches the threshold
 #pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (dyn.bkey[q][k][tid] >= tk)
-                        for (int c = q * G; c < c_end; ++c)
-                            mine += g.b0 + c * CHUNK + k * THREADS + tid < g.b1;
+            for (int q = 0; q < GROUPS; ++q) {
+                if (q < ngroups) {
+                    const uint2 kk = dyn.bkey[q][tid];
+                    hit |= uint32_t((kk.x & 0xffffu) >= tk) << (q * U);
+                    hit |= uint32_t((kk.x >> 16) >= tk) << (q * U + 1);
+                    hit |= uint32_t((kk.y & 0xffffu) >= tk) << (q * U + 2);
+                    hit |= uint32_t((kk.y >> 16) >= tk) << (q * U + 3);
+                }
+            }
+            int mine = 0;
+            for (uint32_t h = hit; h != 0; h &= h - 1) {
+                const int s = __ffs(h) - 1, q = s / U, k = s % U;
+                const int c_end = min(nchunks, (q + 1) * G);
+                for (int c = q * G; c < c_end; ++c) mine += g.b0 + c * CHUNK + k * THREADS + tid < g.b1;
             }
             int incl = mine;
 #pragma unroll
@@ -324,31 +339,29 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             int base = 0;
             if (lane == 31 && incl > 0) base = atomicAdd(nflag, incl);
             int pos = __shfl_sync(kFullMask, base, 31) + incl - mine;
-            if (mine > 0) {
-                for (int q = 0; q < ngroups; ++q) {
-                    const int c_end = min(nchunks, (q + 1) * G);
-#pragma unroll
-                    for (int k = 0; k < U; ++k)
-                        if (dyn.bkey[q][k][tid] >= tk)
-                            for (int c = q * G; c < c_end; ++c) {
-                                const int b = g.b0 + c * CHUNK + k * THREADS + tid;
-                                if (b < g.b1) {
-                                    if (pos < FCAP) dyn.flagged[pos] = b;
-                                    ++pos;
-                                }
-                            }
+            for (uint32_t h = hit; h != 0; h &= h - 1) {
+                const int s = __ffs(h) - 1, q = s / U, k = s % U;
+                const int c_end = min(nchunks, (q + 1) * G);
+                for (int c = q * G; c < c_end; ++c) {
+                    const int b = g.b0 + c * CHUNK + k * THREADS + tid;
+                    if (b < g.b1) {
+                        if (pos < FCAP) dyn.flagged[pos] = b;
+                        ++pos;
+                    }
                 }
             }
         }
         __syncthreads();
         const int nf = *nflag;
 
-        // ---- pass 2 (L2): the listed blocks again; their elements >= T are the candidates
+        // ---- pass 2 (L2): the listed blocks again, one per thread; their
+        // elements >= T are the candidates
         if (nf <= FCAP) {
             for (int i0 = 0; i0 < nf; i0 += THREADS) {  // uniform
                 const int i = i0 + tid;
                 float v[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
                 int b = 0;
+                uint32_t live = 0;
                 if (i < nf) {
                     b = dyn.flagged[i];
                     if (b >= g.full_lo && b < g.full_hi) {
@@ -357,21 +370,22 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                         v[1] = __uint_as_float(w.y);
                         v[2] = __uint_as_float(w.z);
                         v[3] = __uint_as_float(w.w);
+                        live = 0xfu;
                     } else {
 #pragma unroll
                         for (int l = 0; l < 4; ++l) {
                             const int64_t col = 4 * int64_t(b) + l - g.head;
-                            if (col >= 0 && col < cols) v[l] = g.xr[col];
+                            const bool in = col >= 0 && col < cols;
+                            if (in) v[l] = g.xr[col];
+                            live |= uint32_t(in) << l;
                         }
                     }
                 }
-                uint32_t hit = 0;  // bit l: element l is a candidate
+                uint32_t hitmask = 0;  // bit l: element l is a candidate
 #pragma unroll
-                for (int l = 0; l < 4; ++l) {
-                    const int64_t col = 4 * int64_t(b) + l - g.head;
-                    hit |= uint32_t(i < nf && v[l] >= T && col >= 0 && col < cols) << l;
-                }
-                const int cnt = __popc(hit);
+                for (int l = 0; l < 4; ++l) hitmask |= uint32_t(v[l] >= T) << l;
+                hitmask &= live;
+                const int cnt = __popc(hitmask);
                 int incl = cnt;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -383,7 +397,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 int pos = __shfl_sync(kFullMask, base, 31) + incl - cnt;
 #pragma unroll
                 for (int l = 0; l < 4; ++l) {
-                    if ((hit >> l) & 1u) {
+                    if ((hitmask >> l) & 1u) {
                         if (pos < CAP) sm.cand[pos] = Cand{v[l], int(4u * uint32_t(b) + uint32_t(l) - uint32_t(g.head))};
                         ++pos;
                     }
@@ -429,40 +443,49 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             __syncthreads();
         }
 
-        // ---- selection: list[r] = the candidate that r candidates beat (r < K);
-        // one warp per candidate, the lanes splitting the count (the first 128
-        // candidates held in registers)
+        // ---- selection: list[r] = the candidate that r candidates beat (r < K).
+        // One warp per candidate, the lanes splitting the count.  The first
+        // 32 * RC candidates are loaded into registers once (lane l holds l,
+        // l + 32, ...) and items are passed around by shuffles, not reread from
+        // shared memory (its round trips are slow while the SM's other CTA
+        // streams).
         {
-            Cand reg[4];
+            constexpr int RC = 8;
+            Cand reg[RC];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) reg[j] = lane + 32 * j < n ? sm.cand[lane + 32 * j] : pad;
+            for (int j = 0; j < RC; ++j) reg[j] = lane + 32 * j < n ? sm.cand[lane + 32 * j] : pad;
             for (int i = warp; i < n; i += NW) {
-                const Cand c = sm.cand[i];
+                Cand c;
+                if (i < 32 * RC) {
+                    const int slot = i >> 5;  // uniform over the warp
+                    Cand h = reg[0];
+#pragma unroll
+                    for (int j = 1; j < RC; ++j)
+                        if (slot == j) h = reg[j];
+                    c.v = __shfl_sync(kFullMask, h.v, i & 31);
+                    c.j = __shfl_sync(kFullMask, h.j, i & 31);
+                } else {
+                    c = sm.cand[i];
+                }
                 int r = 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) r += beats(reg[j], c);
-                for (int q = 128 + lane; q < n; q += 32) r += beats(sm.cand[q], c);
+                for (int j = 0; j < RC; ++j) r += beats(reg[j], c);
+                for (int q = 32 * RC + lane; q < n; q += 32) r += beats(sm.cand[q], c);
                 r = __reduce_add_sync(kFullMask, r);
                 if (lane == 0 && r < K) sm.list[r] = c;
             }
         }
 
-        // ---- the CTA's (m, d), then the outputs
-        {
-            float mm = m, dd = d;
-            group_merge<32>(mm, dd);
-            if (lane == 0) sm.warp_state[warp] = make_float2(mm, dd);
-        }
-        __syncthreads();
+        __syncthreads();  // the list is complete
+
+        // ---- the CTA's (m, d) (warp states published at the threshold barrier),
+        // then the outputs
         float2 st = make_float2(kNegInf, 0.f);
-        if (warp == 0) {
+        if (warp == 0 || (S == 1 && warp * 32 < K)) {  // every warp that writes outputs folds it
             st = lane < NW ? sm.warp_state[lane] : make_float2(kNegInf, 0.f);
             group_merge<32>(st.x, st.y);
         }
         if (S == 1) {
-            if (tid == 0) sm.xstate[parity][0] = st;
-            __syncthreads();
-            st = sm.xstate[parity][0];
             if (tid < K) {
                 const Cand c = sm.list[tid];
                 vals[row * K + tid] = exp1(c.v - st.x) * (1.0f / st.y);

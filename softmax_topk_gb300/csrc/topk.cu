@@ -1,7 +1,7 @@
 // Fused softmax + TopK: kernel choice and launch.
 //
 // Persistent CTAs of 512 threads, two per SM, each taking whole rows in
-// chunks of 8 16-byte blocks per thread (16384 fp32); with fewer rows than
+// chunks of 4 16-byte blocks per thread (8192 fp32); with fewer rows than
 // resident CTAs a row is split over a cluster of S CTAs (S <= 8, and no more
 // CTAs than the row has chunks) that merge through distributed shared memory.
 #include "host_common.h"
@@ -11,7 +11,7 @@
 namespace os {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkVpt = 8;      // 16-byte blocks per thread per chunk
+constexpr int kTopkVpt = 4;      // 16-byte blocks per thread per chunk
 constexpr int kTopkKmax = 64;
 constexpr int kTopkCap = 2048;   // candidates
 constexpr int kTopkGroups = 4;   // block keys kept per thread slot (groups of chunks)
