@@ -442,6 +442,12 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
     if (CLUSTER > 1) cluster_sync();  // no CTA leaves while a peer may still address it
 }
 
+// Chunks of a row that the streaming kernel keeps in shared memory between
+// its passes: as many as fit in kStreamKeptBytes (two CTAs share an SM).
+constexpr int kStreamKeptBytes = 96 * 1024;
+template <typename TI, int THREADS, int UNROLL>
+constexpr int stream_kept_chunks() { return kStreamKeptBytes / (THREADS * UNROLL * 16); }
+
 // ---------------------------------------------------------------------------
 // Chunk arithmetic of the streaming kernel.  A chunk is UNROLL 16-byte
 // vectors per thread, kept as raw words: bf16 inputs are never unpacked by
@@ -518,8 +524,11 @@ __device__ __forceinline__ float exp_sum_z(const float* z) {
 // pass 2 reads them again right after the merge.  Pass 2 walks the chunks in
 // reverse order (the most recently read lines are the likeliest still in
 // L2), marks its loads evict_first (last use) and writes y = e^(x - m) / d
-// with streaming stores.  With one CTA per row there is no exchange between
-// SMs at all: each row costs one __syncthreads-level merge.
+// with streaming stores.  The row's first NS chunks (the ones pass 1 read
+// longest ago, so the likeliest to have left L2) are also kept raw in shared
+// memory by the thread that loaded them, and pass 2 takes them from there.
+// With one CTA per row there is no exchange between SMs at all: each row
+// costs one __syncthreads-level merge.
 // bf16 outputs fold 1/d into the exponent (one FMA and one ex2 per element).
 // ALIGNED (rows start on 16-byte boundaries) selects 128-bit loads and stores;
 // otherwise the same register layout is filled element by element.  Chunks
@@ -530,7 +539,9 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV;
     constexpr bool FAST = fast_exp_for<TO>();
     constexpr int STEP = THREADS * UNROLL;  // vectors per chunk
+    constexpr int NS = stream_kept_chunks<TI, THREADS, UNROLL>();
     __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
+    extern __shared__ uint4 kept[];  // [NS][UNROLL][THREADS]: the row's first chunks, raw
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
     const int nv = (cols + EPV - 1) / EPV;
@@ -577,6 +588,10 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
         for (int c = 0; c < nchunks; ++c) {
             Chunk<TI, UNROLL> ch;
             load_chunk(xs, c, keep, ch);
+            if (c < NS) {  // kept on chip for pass 2 (thread-private slots)
+#pragma unroll
+                for (int k = 0; k < UNROLL; ++k) kept[(c * UNROLL + k) * THREADS + threadIdx.x] = ch.raw[k];
+            }
             const float m_new = fmaxf(m, ch.max());
             float z[EPC];
             ch.shifted(m_new, z);
@@ -589,7 +604,12 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
         // pass 2, last chunk first: y = e^(x - m) / d
         for (int c = nchunks - 1; c >= 0; --c) {
             Chunk<TI, UNROLL> ch;
-            load_chunk(xs, c, drop, ch);
+            if (c < NS) {
+#pragma unroll
+                for (int k = 0; k < UNROLL; ++k) ch.raw[k] = kept[(c * UNROLL + k) * THREADS + threadIdx.x];
+            } else {
+                load_chunk(xs, c, drop, ch);
+            }
             float e[EPC];
             ch.shifted(md.x, e);
 #pragma unroll

@@ -93,6 +93,10 @@ struct SoftmaxFamily {
     }
     static constexpr int STREAM_UNROLL = stream_unroll<TI>();
     using StreamKernel = void (*)(const TI*, TO*, int64_t, int);
+    static constexpr int stream_smem_bytes() {
+        return stream_kept_chunks<TI, kStreamThreads, STREAM_UNROLL>() * kStreamThreads *
+               STREAM_UNROLL * 16;
+    }
     static StreamKernel streaming(int cluster, bool aligned) {
         constexpr int T = kStreamThreads, U = STREAM_UNROLL;
         if (aligned)
@@ -190,7 +194,8 @@ struct SoftmaxFamily {
                 q.vectors_per_thread = STREAM_UNROLL;
                 q.cluster = rows >= 2 * int64_t(dev->sms) ? 1 : 8;
                 {
-                    const int occ = blocks_per_sm(streaming(q.cluster, true), kStreamThreads);
+                    const int occ = blocks_per_sm(streaming(q.cluster, true), kStreamThreads,
+                                                  stream_smem_bytes());
                     const int64_t resident = q.cluster == 1
                         ? int64_t(dev->sms) * (occ > 0 ? occ : 1)
                         : kMaxClustersPerLaunch;
@@ -217,8 +222,9 @@ struct SoftmaxFamily {
         }
         if (p.path == OS_PATH_STREAM) {
             StreamKernel k = streaming(p.cluster, aligned);
-            if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
-            return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, xi, yo, rows, cols);
+            const int smem = stream_smem_bytes();
+            if (!prepare_kernel(k, p.cluster, smem)) return cudaErrorInvalidValue;
+            return launch_kernel(k, p.grid, p.threads, p.cluster, smem, stream, xi, yo, rows, cols);
         }
         Kernel k = nullptr;
         switch (p.path) {
