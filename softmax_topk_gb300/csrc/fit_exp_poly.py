@@ -1,4 +1,5 @@
-"""Derivation of the polynomial used by the library's own fp32 exponential.
+"""Derivation of the polynomial used by the library's accurate fp32 exponential
+(exp1 in kernels/ops.cuh: os_exp_f32, merge rescale factors, TopK values).
 
 The kernels evaluate e^z as 2^n * p(r) with n = rint(z * log2 e) and
 r = z - n ln2 (Cody & Waite, "Software Manual for the Elementary Functions",
