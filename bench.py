@@ -287,6 +287,7 @@ def run_ours(args):
     }
     if args.extra:
         line["extra_workloads"] = run_extra(st, dev, args)
+        line["unfused_baselines"] = run_baselines(st, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -393,6 +394,63 @@ def run_extra(st, dev, args):
         out[n] = {"ms": round(ms, 5), "gbs": round(gbs, 1), "rows_per_s": round(w.rows / ms * 1e3),
                   "frac_of_measured_hbm": round(gbs / peak, 4), "input_copies": len(xs)}
         del xs, x, y
+    return out
+
+
+def _time_ms(fn, dev, steps):
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        fn(0)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for i in range(steps):
+        fn(i)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / steps
+
+
+def run_baselines(st, dev, args):
+    """The unfused pipelines the online normalizer and the fused TopK replace
+    ("Online normalizer calculation for softmax", sections 2 and 4): the
+    three-pass safe softmax against the two-pass online kernel, and softmax
+    followed by TopK of the probabilities against the fused kernel, on the
+    step's workloads.  Times per call (CUDA events), inputs larger than L2 or
+    rotated like the step's."""
+    out = {}
+    steps = max(20, min(args.steps, 200))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    for n in SOFTMAX_STEP:
+        w = workloads.WORKLOADS[n]
+        x = workloads.make(w, device=dev)
+        y = torch.empty_like(x)
+        t_online = _time_ms(lambda i: st.softmax(x, out=y), dev, steps)
+        t_safe = _time_ms(lambda i: st.softmax(x, out=y, path="safe"), dev, steps)
+        out[n] = {"online_ms": round(t_online, 5), "safe_three_pass_ms": round(t_safe, 5),
+                  "safe_over_online": round(t_safe / t_online, 3)}
+        del x, y
+    w = workloads.WORKLOADS[TOPK_NAME]
+    x = workloads.make(w, device=dev)
+    copies = max(1, -(-3 * l2 // (x.numel() * 4)) + 1)
+    xs = [x] + [x.clone() for _ in range(copies - 1)]
+    y = torch.empty_like(x)
+    for K in TOPK_KS:
+        vals = torch.empty(w.rows, K, device=dev)
+        idx = torch.empty(w.rows, K, dtype=torch.int32, device=dev)
+        t_fused = _time_ms(lambda i: st.softmax_topk(xs[i % copies], K, vals=vals, idx=idx), dev, steps)
+
+        def unfused(i, path):
+            st.softmax(xs[i % copies], out=y, path=path)
+            st.topk(y, K, vals=vals, idx=idx)
+        t_online = _time_ms(lambda i: unfused(i, "auto"), dev, steps)
+        t_safe = _time_ms(lambda i: unfused(i, "safe"), dev, steps)
+        out[f"{TOPK_NAME}_K{K}"] = {
+            "fused_ms": round(t_fused, 5), "online_softmax_then_topk_ms": round(t_online, 5),
+            "safe_softmax_then_topk_ms": round(t_safe, 5),
+            "unfused_online_over_fused": round(t_online / t_fused, 3),
+            "unfused_safe_over_fused": round(t_safe / t_fused, 3)}
     return out
 
 

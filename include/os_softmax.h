@@ -68,8 +68,13 @@ typedef enum {
     OS_PATH_WARP = 1,   /* 1..32 lanes per row, row held in registers; short rows */
     OS_PATH_ONCHIP = 2, /* one CTA or a thread-block cluster per row, row held
                            in registers across the cluster; one HBM read */
-    OS_PATH_STREAM = 3  /* two passes over the row (running (m, d), then
+    OS_PATH_STREAM = 3, /* two passes over the row (running (m, d), then
                            normalise); any row length */
+    OS_PATH_SAFE = 4    /* baseline: the three-pass safe softmax (maximum;
+                           sum of e^(x - m); normalise), each pass reading the
+                           row from memory ("Online normalizer calculation for
+                           softmax", section 2); any row length; never chosen
+                           by AUTO */
 } os_path;
 
 /* Launch configuration chosen for a call (see os_softmax_plan / os_topk_plan). */
@@ -111,6 +116,17 @@ os_status os_softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols,
  */
 os_status os_softmax_topk(const float *x, float *vals, int32_t *idx, int64_t rows,
                           int64_t cols, int32_t K, os_stream_t stream);
+
+/*
+ * TopK of x itself (no softmax): for each row the K largest values and their
+ * columns, best first, with the same order, ties rule, arguments, checks and
+ * kernel as os_softmax_topk; vals[r*K + k] = x[r, idx[r*K + k]] exactly.
+ * With y = softmax(x) from os_softmax_fwd it forms the unfused softmax-then-
+ * TopK pipeline that "Online normalizer calculation for softmax" (section 4)
+ * compares the fused kernel with; it is also a plain row TopK.
+ */
+os_status os_topk(const float *x, float *vals, int32_t *idx, int64_t rows, int64_t cols,
+                  int32_t K, os_stream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *os_status_string(os_status status);

@@ -1,13 +1,13 @@
 """Python binding of libos_softmax.so (row-wise online softmax, fused softmax+TopK).
 
 The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
-``os_softmax_fwd``, ``os_softmax_topk``, ``os_softmax_fwd_path``,
+``os_softmax_fwd``, ``os_softmax_topk``, ``os_topk``, ``os_softmax_fwd_path``,
 ``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_device_status``,
 ``os_set_wait_timeout_ns``, ``os_set_fault_injection``, ``os_status_string``.  They take raw
 device pointers (ints) and a raw stream handle, exactly like the C functions,
 and raise ``OsError`` on a non-OK status.
 
-``softmax`` and ``softmax_topk`` are the tensor-level conveniences: they take
+``softmax``, ``softmax_topk`` and ``topk`` are the tensor-level conveniences: they take
 torch CUDA tensors, allocate outputs with torch, pass the current torch
 stream, and call the same C entry points.  PyTorch only provides memory and
 streams; every step of the computation runs in the library's CUDA kernels.
@@ -23,9 +23,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libos_softmax.so")
 
 OS_F32, OS_BF16 = 0, 1
-OS_PATH_AUTO, OS_PATH_WARP, OS_PATH_ONCHIP, OS_PATH_STREAM = 0, 1, 2, 3
+OS_PATH_AUTO, OS_PATH_WARP, OS_PATH_ONCHIP, OS_PATH_STREAM, OS_PATH_SAFE = 0, 1, 2, 3, 4
 PATHS = {"auto": OS_PATH_AUTO, "warp": OS_PATH_WARP, "onchip": OS_PATH_ONCHIP,
-         "stream": OS_PATH_STREAM}
+         "stream": OS_PATH_STREAM, "safe": OS_PATH_SAFE}
 STATUS = ["OS_OK", "OS_ERR_NULL", "OS_ERR_SHAPE", "OS_ERR_DTYPE", "OS_ERR_K", "OS_ERR_ALIAS",
           "OS_ERR_CUDA", "OS_ERR_TIMEOUT", "OS_ERR_PATH", "OS_ERR_ALIGN"]
 KMAX = 64
@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
     lib.os_softmax_fwd.argtypes = [vp, vp, i64, i64, st, st, vp]
     lib.os_softmax_fwd_path.argtypes = [vp, vp, i64, i64, st, st, st, vp]
     lib.os_softmax_topk.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+    lib.os_topk.argtypes = [vp, vp, vp, i64, i64, i32, vp]
     lib.os_softmax_plan.argtypes = [i64, i64, st, st, st, ctypes.POINTER(Plan)]
     lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
     lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
@@ -69,7 +70,7 @@ def _load() -> ctypes.CDLL:
     lib.os_set_fault_injection.argtypes = [i32]
     lib.os_status_string.argtypes = [st]
     lib.os_status_string.restype = ctypes.c_char_p
-    for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_softmax_plan",
+    for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_topk", "os_softmax_plan",
                  "os_topk_plan", "os_exp_f32", "os_device_status", "os_set_wait_timeout_ns",
                  "os_set_fault_injection"):
         getattr(lib, name).restype = st
@@ -103,6 +104,11 @@ def os_softmax_fwd_path(x: int, y: int, rows: int, cols: int, in_dtype: int, out
 def os_softmax_topk(x: int, vals: int, idx: int, rows: int, cols: int, K: int,
                     stream: int | None) -> None:
     _check(_lib.os_softmax_topk(x, vals, idx, rows, cols, K, stream), "os_softmax_topk")
+
+
+def os_topk(x: int, vals: int, idx: int, rows: int, cols: int, K: int,
+            stream: int | None) -> None:
+    _check(_lib.os_topk(x, vals, idx, rows, cols, K, stream), "os_topk")
 
 
 def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
@@ -200,6 +206,23 @@ def softmax_topk(x, K: int, vals=None, idx=None):
     with _OnDevice(x.device):
         os_softmax_topk(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, x.shape[1], K,
                         _stream_handle(x))
+    return vals, idx
+
+
+def topk(x, K: int, vals=None, idx=None):
+    """(values fp32 [rows, K], column indices int32 [rows, K]) of each row's K largest
+    values of x itself (no softmax)."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous() or x.dtype != torch.float32:
+        raise ValueError("x must be a contiguous 2-D float32 CUDA tensor")
+    rows = x.shape[0]
+    if vals is None:
+        vals = torch.empty((rows, K), dtype=torch.float32, device=x.device)
+    if idx is None:
+        idx = torch.empty((rows, K), dtype=torch.int32, device=x.device)
+    with _OnDevice(x.device):
+        os_topk(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, x.shape[1], K,
+                _stream_handle(x))
     return vals, idx
 
 

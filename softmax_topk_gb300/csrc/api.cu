@@ -79,7 +79,7 @@ bool shape_ok(int64_t rows, int64_t cols) {
 os_status softmax_checks(int64_t rows, int64_t cols, os_dtype in, os_dtype out, os_path path) {
     if (!valid_dtype(in) || !valid_dtype(out)) return OS_ERR_DTYPE;
     if (!shape_ok(rows, cols)) return OS_ERR_SHAPE;
-    if (path < OS_PATH_AUTO || path > OS_PATH_STREAM) return OS_ERR_PATH;
+    if (path < OS_PATH_AUTO || path > OS_PATH_SAFE) return OS_ERR_PATH;
     return OS_OK;
 }
 
@@ -153,8 +153,8 @@ os_status os_topk_plan(int64_t rows, int64_t cols, int32_t K, os_plan* plan) {
     return os::plan_topk(rows, cols, K, plan);
 }
 
-os_status os_softmax_topk(const float* x, float* vals, int32_t* idx, int64_t rows, int64_t cols,
-                          int32_t K, os_stream_t stream) {
+os_status topk_entry(const float* x, float* vals, int32_t* idx, int64_t rows, int64_t cols,
+                     int32_t K, bool plain, os_stream_t stream) {
     os_status st = topk_checks(rows, cols, K);
     if (st != OS_OK) return st;
     if (rows == 0) return OS_OK;
@@ -170,9 +170,19 @@ os_status os_softmax_topk(const float* x, float* vals, int32_t* idx, int64_t row
     if (st != OS_OK) return st;
     os::KernelCtl ctl;
     if (!make_ctl(&ctl)) return OS_ERR_CUDA;
-    const cudaError_t e = os::launch_topk(plan, x, vals, idx, rows, static_cast<int>(cols), K,
+    const cudaError_t e = os::launch_topk(plan, x, vals, idx, rows, static_cast<int>(cols), K, plain,
                                           ctl, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
+}
+
+os_status os_softmax_topk(const float* x, float* vals, int32_t* idx, int64_t rows, int64_t cols,
+                          int32_t K, os_stream_t stream) {
+    return topk_entry(x, vals, idx, rows, cols, K, false, stream);
+}
+
+os_status os_topk(const float* x, float* vals, int32_t* idx, int64_t rows, int64_t cols, int32_t K,
+                  os_stream_t stream) {
+    return topk_entry(x, vals, idx, rows, cols, K, true, stream);
 }
 
 os_status os_exp_f32(const float* z, float* out, int64_t n, os_stream_t stream) {

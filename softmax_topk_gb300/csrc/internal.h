@@ -24,8 +24,10 @@ OS_DECLARE_SOFTMAX_PAIR(f32_bf16)
 OS_DECLARE_SOFTMAX_PAIR(bf16_f32)
 
 os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p);
+// plain: TopK of x itself (vals = the selected x) instead of softmax + TopK
 cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* idx,
-                        int64_t rows, int cols, int K, const KernelCtl& ctl, cudaStream_t stream);
+                        int64_t rows, int cols, int K, bool plain, const KernelCtl& ctl,
+                        cudaStream_t stream);
 
 cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t stream);
 

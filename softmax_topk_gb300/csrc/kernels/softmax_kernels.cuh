@@ -507,6 +507,61 @@ struct Chunk {
     }
 };
 
+// Vectors tid + k*THREADS (k < UNROLL) of chunk c of a range of `len`
+// vectors starting at vector `begin` of the row (xs points at that vector);
+// slots past the range (and, unaligned, columns past `cols`) read as -inf.
+template <typename TI, int THREADS, int UNROLL, bool ALIGNED>
+__device__ __forceinline__ void load_stream_chunk(const TI* xs, int c, int len, int begin, int cols,
+                                                  uint64_t policy, Chunk<TI, UNROLL>& ch) {
+    constexpr int EPV = VecTraits<TI>::EPV, STEP = THREADS * UNROLL;
+    const int v0 = c * STEP + int(threadIdx.x);
+    const bool full = c * STEP + STEP <= len;
+    const uint32_t neg_inf_word = sizeof(TI) == 2 ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+        const int v = v0 + k * THREADS;
+        if (full || v < len) {
+            if constexpr (ALIGNED) {
+                ch.raw[k] = ld_policy_v4(xs + v * EPV, policy);
+            } else {
+                TI tmp[EPV];
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) {
+                    const int j = (begin + v) * EPV + q;
+                    tmp[q] = j < cols ? xs[v * EPV + q] : from_f32<TI>(kNegInf);
+                }
+                ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
+            }
+        } else {
+            ch.raw[k] = make_uint4(neg_inf_word, neg_inf_word, neg_inf_word, neg_inf_word);
+        }
+    }
+}
+
+// Stores the UNROLL * EPV values e of chunk c (same slots as load_stream_chunk).
+template <typename TO, int THREADS, int UNROLL, int EPV, bool ALIGNED>
+__device__ __forceinline__ void store_stream_chunk(TO* ys, int c, int len, int begin, int cols,
+                                                   const float* e) {
+    constexpr int STEP = THREADS * UNROLL;
+    const int v0 = c * STEP + int(threadIdx.x);
+    const bool full = c * STEP + STEP <= len;
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+        const int v = v0 + k * THREADS;
+        if (full || v < len) {
+            if constexpr (ALIGNED) {
+                VecStore<TO, EPV>::run(ys + v * EPV, e + k * EPV);
+            } else {
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) {
+                    const int j = (begin + v) * EPV + q;
+                    if (j < cols) ys[v * EPV + q] = from_f32<TO>(e[k * EPV + q]);
+                }
+            }
+        }
+    }
+}
+
 // sum over N entries of e^(z_i), z given
 template <int N, bool FAST>
 __device__ __forceinline__ float exp_sum_z(const float* z) {
@@ -552,31 +607,8 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
     const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     if (CLUSTER > 1) cluster_sync();
 
-    // vectors tid + k*THREADS (k < UNROLL) of chunk c, relative to `begin`;
-    // slots past the end (and, unaligned, columns past `cols`) read as -inf
     auto load_chunk = [&](const TI* xs, int c, uint64_t policy, Chunk<TI, UNROLL>& ch) {
-        const int v0 = c * STEP + int(threadIdx.x);
-        const bool full = c * STEP + STEP <= len;
-        const uint32_t neg_inf_word = sizeof(TI) == 2 ? 0xff80ff80u : 0xff800000u;
-#pragma unroll
-        for (int k = 0; k < UNROLL; ++k) {
-            const int v = v0 + k * THREADS;
-            if (full || v < len) {
-                if constexpr (ALIGNED) {
-                    ch.raw[k] = ld_policy_v4(xs + v * EPV, policy);
-                } else {
-                    TI tmp[EPV];
-#pragma unroll
-                    for (int q = 0; q < EPV; ++q) {
-                        const int j = (begin + v) * EPV + q;
-                        tmp[q] = j < cols ? xs[v * EPV + q] : from_f32<TI>(kNegInf);
-                    }
-                    ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
-                }
-            } else {
-                ch.raw[k] = make_uint4(neg_inf_word, neg_inf_word, neg_inf_word, neg_inf_word);
-            }
-        }
+        load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, begin, cols, policy, ch);
     };
 
     int parity = 0;
@@ -620,23 +652,78 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
                 e[i] = p.x;
                 e[i + 1] = p.y;
             }
-            const int v0 = c * STEP + int(threadIdx.x);
-            const bool full = c * STEP + STEP <= len;
+            store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, len, begin, cols, e);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// safe_rows: the three-pass "safe softmax" that the online normalizer
+// replaces ("Online normalizer calculation for softmax" (notes), section 2;
+// "5.2 CUDA Online Softmax", section 1.1): pass 1 the row maximum m, pass 2
+// d = sum e^(x - m), pass 3 y = e^(x - m) / d, each pass reading the row from
+// global memory with ordinary (L2-allocating) loads.  A measurement baseline
+// (OS_PATH_SAFE), never chosen by AUTO.  One persistent CTA per row.
+template <typename TI, typename TO, int THREADS, int UNROLL, bool ALIGNED>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
+safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols) {
+    constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV, NW = THREADS / 32;
+    constexpr bool FAST = fast_exp_for<TO>();
+    constexpr int STEP = THREADS * UNROLL;
+    __shared__ float red[2][NW];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int len = (cols + EPV - 1) / EPV;
+    const int nchunks = (len + STEP - 1) / STEP;
+    const uint64_t normal = l2_policy_evict_normal();
+    int rb = 0;  // alternate reduction buffers: one barrier per reduction
+    auto block_reduce = [&](float v, bool is_max) {
 #pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
-                const int v = v0 + k * THREADS;
-                if (full || v < len) {
-                    if constexpr (ALIGNED) {
-                        VecStore<TO, EPV>::run(ys + v * EPV, e + k * EPV);
-                    } else {
+        for (int o = 16; o > 0; o >>= 1) {
+            const float t = __shfl_xor_sync(kFullMask, v, o);
+            v = is_max ? fmaxf(v, t) : v + t;
+        }
+        if (lane == 0) red[rb][warp] = v;
+        __syncthreads();
+        float r = red[rb][0];
 #pragma unroll
-                        for (int q = 0; q < EPV; ++q) {
-                            const int j = (begin + v) * EPV + q;
-                            if (j < cols) ys[v * EPV + q] = from_f32<TO>(e[k * EPV + q]);
-                        }
-                    }
-                }
+        for (int w = 1; w < NW; ++w) r = is_max ? fmaxf(r, red[rb][w]) : r + red[rb][w];
+        rb ^= 1;
+        return r;
+    };
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const TI* xs = x + row * int64_t(cols);
+        TO* ys = y + row * int64_t(cols);
+        float m = kNegInf;
+        for (int c = 0; c < nchunks; ++c) {  // pass 1: maximum
+            Chunk<TI, UNROLL> ch;
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, 0, cols, normal, ch);
+            m = fmaxf(m, ch.max());
+        }
+        m = block_reduce(m, true);
+        float d = 0.f;
+        for (int c = 0; c < nchunks; ++c) {  // pass 2: normalizer
+            Chunk<TI, UNROLL> ch;
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, 0, cols, normal, ch);
+            float z[EPC];
+            ch.shifted(m, z);
+            d += exp_sum_z<EPC, FAST>(z);
+        }
+        d = block_reduce(d, false);
+        const float2 inv_d = splat2(1.0f / d);
+        const float neg_log2_d = -__log2f(d);
+        for (int c = 0; c < nchunks; ++c) {  // pass 3: outputs
+            Chunk<TI, UNROLL> ch;
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, 0, cols, normal, ch);
+            float e[EPC];
+            ch.shifted(m, e);
+#pragma unroll
+            for (int i = 0; i < EPC; i += 2) {
+                const float2 z = make_float2(e[i], e[i + 1]);
+                const float2 p = FAST ? exp_pair_div(z, neg_log2_d) : mul2(exp_pair<false>(z), inv_d);
+                e[i] = p.x;
+                e[i + 1] = p.y;
             }
+            store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, len, 0, cols, e);
         }
     }
 }

@@ -177,7 +177,9 @@ struct TopkSegment {
     int b0, b1;            // the CTA's blocks of the row
 };
 
-template <int THREADS, int U, int KMAX, int CAP, int GROUPS, int FCAP>
+// PLAIN: the K largest values themselves (TopK of x, no softmax): no (m, d)
+// is formed and vals are the selected x.
+template <int THREADS, int U, int KMAX, int CAP, int GROUPS, int FCAP, bool PLAIN>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2)
 topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __restrict__ idx,
                  int64_t rows, int cols, int K, int S, KernelCtl ctl) {
@@ -264,7 +266,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             // 2^(x log2e - M_hi) (2^(-M_lo)), where M_hi + M_lo = m' log2e exactly
             // (the residual of an FMA): one FMA and one SFU ex2 per element.
             // Dropping log2e's own rounding costs 1.3e-8 |x - m'| relative per term.
-            {
+            if constexpr (!PLAIN) {
                 const float m_new = fmaxf(m, cmax);
                 const float ms = finite_shift(m_new);
                 const float M_hi = ms * expc::kLog2e;
@@ -488,7 +490,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
         if (S == 1) {
             if (tid < K) {
                 const Cand c = sm.list[tid];
-                vals[row * K + tid] = exp1(c.v - st.x) * (1.0f / st.y);
+                vals[row * K + tid] = PLAIN ? c.v : exp1(c.v - st.x) * (1.0f / st.y);
                 idx[row * K + tid] = c.j;
             }
             __syncthreads();  // list and warp states are rewritten by the next row
@@ -523,7 +525,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 for (int b = 0; b < S; ++b)
                     if (b != a) r += count_beating(sm.xlist[parity][b], K, c);
                 if (r < K) {
-                    vals[row * K + r] = exp1(c.v - M) * inv_d;
+                    vals[row * K + r] = PLAIN ? c.v : exp1(c.v - M) * inv_d;
                     idx[row * K + r] = c.j;
                 }
             }

@@ -17,6 +17,7 @@
 //           where the device can schedule them).
 //   STREAM  anything longer: one CTA per row when there are enough rows to
 //           fill the GPU, else a cluster of 8 CTAs per row.
+//   SAFE    the three-pass safe softmax, as a measurement baseline only.
 // "5.2 CUDA Online Softmax" (sections 6.3 and 8.3) makes the same split on
 // its hardware: the register-cached single read (V3) for short rows, the
 // two-pass kernel (V2/V4) beyond the register budget.
@@ -93,6 +94,10 @@ struct SoftmaxFamily {
     }
     static constexpr int STREAM_UNROLL = stream_unroll<TI>();
     using StreamKernel = void (*)(const TI*, TO*, int64_t, int);
+    static StreamKernel safe(bool aligned) {
+        constexpr int T = kStreamThreads, U = STREAM_UNROLL;
+        return aligned ? safe_rows_kernel<TI, TO, T, U, true> : safe_rows_kernel<TI, TO, T, U, false>;
+    }
     static constexpr int stream_smem_bytes() {
         return stream_kept_chunks<TI, kStreamThreads, STREAM_UNROLL>() * kStreamThreads *
                STREAM_UNROLL * 16;
@@ -203,6 +208,14 @@ struct SoftmaxFamily {
                 }
                 break;
             }
+            case OS_PATH_SAFE: {
+                q.threads = kStreamThreads;
+                q.vectors_per_thread = STREAM_UNROLL;
+                q.cluster = 1;
+                const int occ = blocks_per_sm(safe(true), kStreamThreads);
+                q.grid = min64(rows, int64_t(dev->sms) * (occ > 0 ? occ : 1));
+                break;
+            }
             default:
                 return OS_ERR_PATH;
         }
@@ -219,6 +232,11 @@ struct SoftmaxFamily {
             if (!prepare_kernel(k, p.cluster, Ring::SMEM_BYTES)) return cudaErrorInvalidValue;
             return launch_kernel(k, p.grid, p.threads, p.cluster, Ring::SMEM_BYTES, stream, xi, yo,
                                  rows, cols, ctl);
+        }
+        if (p.path == OS_PATH_SAFE) {
+            StreamKernel k = safe(aligned);
+            if (!prepare_kernel(k, 1, 0)) return cudaErrorInvalidValue;
+            return launch_kernel(k, p.grid, p.threads, 1, 0, stream, xi, yo, rows, cols);
         }
         if (p.path == OS_PATH_STREAM) {
             StreamKernel k = streaming(p.cluster, aligned);

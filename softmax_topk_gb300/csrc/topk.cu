@@ -19,15 +19,17 @@ constexpr int kTopkFcap = 2048;  // blocks read again in pass 2
 constexpr int kTopkDynBytes =
     int(sizeof(TopkDynSmem<kTopkThreads, kTopkVpt, kTopkGroups, kTopkFcap>));
 
+template <bool PLAIN>
 static auto topk_kernel() {
-    return topk_rows_kernel<kTopkThreads, kTopkVpt, kTopkKmax, kTopkCap, kTopkGroups, kTopkFcap>;
+    return topk_rows_kernel<kTopkThreads, kTopkVpt, kTopkKmax, kTopkCap, kTopkGroups, kTopkFcap,
+                            PLAIN>;
 }
 
 os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
     (void)K;
     const DeviceInfo* dev = device_info();
     if (!dev) return OS_ERR_CUDA;
-    const int per_sm = blocks_per_sm(topk_kernel(), kTopkThreads, kTopkDynBytes);
+    const int per_sm = blocks_per_sm(topk_kernel<false>(), kTopkThreads, kTopkDynBytes);
     if (per_sm <= 0) return OS_ERR_CUDA;
     const int64_t resident = int64_t(dev->sms) * per_sm;
     const int64_t blocks = (cols + 3) / 4 + 1;  // upper bound over the 4 possible row offsets
@@ -52,9 +54,9 @@ os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
 }
 
 cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* idx,
-                        int64_t rows, int cols, int K, const KernelCtl& ctl,
+                        int64_t rows, int cols, int K, bool plain, const KernelCtl& ctl,
                         cudaStream_t stream) {
-    auto k = topk_kernel();
+    auto k = plain ? topk_kernel<true>() : topk_kernel<false>();
     if (!prepare_kernel(k, p.cluster, kTopkDynBytes)) return cudaErrorInvalidValue;
     return launch_kernel(k, p.grid, p.threads, p.cluster, kTopkDynBytes, stream, x, vals,
                          reinterpret_cast<int*>(idx), rows, cols, K, p.cluster, ctl);

@@ -91,8 +91,9 @@ def test_softmax_without_device_fails_loudly(lib):
     assert lib.os_softmax_fwd(A, A + 4 * 32, 4, 8, F32, F32, None) == CUDA
 
 
-def test_topk_argument_errors(lib):
-    f = lib.os_softmax_topk
+@pytest.mark.parametrize("name", ["os_softmax_topk", "os_topk"])
+def test_topk_argument_errors(lib, name):
+    f = getattr(lib, name)
     assert f(A, B, C, 4, 100, 0, None) == KERR
     assert f(A, B, C, 4, 100, 65, None) == KERR
     assert f(A, B, C, 4, 5, 6, None) == KERR

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 PAIRS = [("f32", "f32"), ("bf16", "bf16"), ("f32", "bf16"), ("bf16", "f32")]
-PATHS = ["auto", "warp", "onchip", "stream"]
+PATHS = ["auto", "warp", "onchip", "stream", "safe"]
 COLS = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256,
         257, 511, 512, 513, 1023, 1024, 1025, 2047, 2048, 2049, 4095, 4096, 4097, 8191, 8192,
         8193, 16383, 16384, 16385, 32000, 32768, 32769, 50257, 65535, 65536, 65537, 128256,
@@ -63,7 +63,7 @@ def test_cols_sweep_auto(st, cols, pair):
 
 
 @pytest.mark.parametrize("cols", COLS)
-@pytest.mark.parametrize("path", ["warp", "onchip", "stream"])
+@pytest.mark.parametrize("path", ["warp", "onchip", "stream", "safe"])
 @pytest.mark.parametrize("pair", [("f32", "f32"), ("bf16", "bf16")], ids=lambda p: f"{p[0]}-{p[1]}")
 def test_cols_sweep_forced_path(st, cols, path, pair):
     rows = 3 if cols > 100000 else 6

@@ -132,3 +132,49 @@ def test_bad_k_raises(st):
     assert e.value.name == "OS_ERR_K"
     with pytest.raises(st.OsError):
         st.softmax_topk(_rand(2, 10, seed=1), 11)
+
+
+# ------------------------------------------------------------------ os_topk (TopK of x itself)
+def _run_plain(st, x, K, label):
+    vals, idx = st.topk(x, K)
+    torch.cuda.synchronize()
+    x64 = x.double().cpu().numpy()
+    _, ri = oracle.topk(x64, K)  # the oracle's order: value descending, then column ascending
+    idx = idx.cpu().numpy()
+    bad = np.argwhere(idx != ri)
+    assert bad.size == 0, f"{label}: {len(bad)} index mismatches, first at {bad[:3].tolist()}"
+    want = np.take_along_axis(x.cpu().numpy(), idx.astype(np.int64), axis=1)
+    assert np.array_equal(vals.cpu().numpy(), want), f"{label}: values are not the selected x"
+
+
+@pytest.mark.parametrize("cols", [1, 5, 64, 65, 1000, 8193, 50257, 300007])
+@pytest.mark.parametrize("K", [1, 8, 64])
+def test_plain_topk_shapes(st, cols, K):
+    if K > cols:
+        pytest.skip("K > cols")
+    rows = 3 if cols > 100000 else 9
+    _run_plain(st, _rand(rows, cols, seed=cols * 7 + K), K, f"plain cols={cols} K={K}")
+
+
+def test_plain_topk_ties_and_inf(st):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    x = torch.randint(0, 4, (6, 20000), generator=g, device="cuda").float()
+    x[1] = -np.inf
+    x[1, [3, 19999]] = 0.0
+    for K in (1, 8, 64):
+        _run_plain(st, x, K, f"plain ties K={K}")
+
+
+@pytest.mark.parametrize("K", [8, 64])
+def test_unfused_pipeline_matches_fused(st, K):
+    """softmax then TopK of the probabilities (the unfused pipeline) against the
+    oracle's TopK of those probabilities, and against the fused kernel's values."""
+    w = workloads.WORKLOADS["topk_256x50257_f32"]
+    x = workloads.make(w.scaled(rows=32), device="cuda")
+    y = st.softmax(x)
+    _run_plain(st, y, K, f"TopK of softmax(x) K={K}")
+    vals_u, _ = st.topk(y, K)
+    vals_f, _ = st.softmax_topk(x, K)
+    rel = ((vals_u.double() - vals_f.double()).abs() / vals_f.double()).max()
+    assert float(rel) <= 2e-5
