@@ -15,8 +15,8 @@
 //             128/256/512 threads, or a cluster of 512-thread CTAs, per row.
 //           Rows of up to 262144 fp32 / 524288 bf16 (16-CTA clusters only
 //           where the device can schedule them).
-//   STREAM  anything longer: one CTA per row when there are enough rows to
-//           fill the GPU, else a cluster of 8 CTAs per row.
+//   STREAM  anything longer: one CTA per row when there are at least as many
+//           rows as SMs, else a cluster of 8 CTAs per row.
 //   SAFE    the three-pass safe softmax, as a measurement baseline only.
 // "5.2 CUDA Online Softmax" (sections 6.3 and 8.3) makes the same split on
 // its hardware: the register-cached single read (V3) for short rows, the
@@ -197,7 +197,7 @@ struct SoftmaxFamily {
             case OS_PATH_STREAM: {
                 q.threads = kStreamThreads;
                 q.vectors_per_thread = STREAM_UNROLL;
-                q.cluster = rows >= 2 * int64_t(dev->sms) ? 1 : 8;
+                q.cluster = rows >= int64_t(dev->sms) ? 1 : 8;  // measured: 1 CTA per row wins from one row per SM up
                 {
                     const int occ = blocks_per_sm(streaming(q.cluster, true), kStreamThreads,
                                                   stream_smem_bytes());
