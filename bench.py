@@ -288,6 +288,7 @@ def run_ours(args):
     if args.extra:
         line["extra_workloads"] = run_extra(st, dev, args)
         line["unfused_baselines"] = run_baselines(st, dev, args)
+        line["stats_and_causal"] = run_stats_and_causal(st, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -451,6 +452,38 @@ def run_baselines(st, dev, args):
             "safe_softmax_then_topk_ms": round(t_safe, 5),
             "unfused_online_over_fused": round(t_online / t_fused, 3),
             "unfused_safe_over_fused": round(t_safe / t_fused, 3)}
+    return out
+
+
+def run_stats_and_causal(st, dev, args):
+    """Row statistics (one read per element, 12 bytes out per row) on the
+    step's softmax workloads, and the causal workload with the mask applied in
+    the kernel (masked columns never read) against reading the planted -inf."""
+    out = {}
+    steps = max(20, min(args.steps, 200))
+    peak, _ = measured_peaks()
+    for n in SOFTMAX_STEP:
+        w = workloads.WORKLOADS[n]
+        x = workloads.make(w, device=dev)
+        ms = _time_ms(lambda i: st.softmax_stats(x), dev, steps)
+        b = x.numel() * x.element_size() + w.rows * 12
+        out[f"stats_{n}"] = {"ms": round(ms, 5), "gbs": round(b / ms / 1e6, 1),
+                             "frac_of_measured_hbm": round(b / ms / 1e6 / peak, 4)}
+        del x
+    w = workloads.WORKLOADS["causal_1048576x128_f32"]
+    x = workloads.make(w, device=dev)
+    dense = torch.where(torch.isinf(x), torch.zeros_like(x), x)
+    y = torch.empty_like(x)
+    t_read = _time_ms(lambda i: st.softmax(x, out=y), dev, steps)
+    t_mask = _time_ms(lambda i: st.softmax_causal(dense, 128, 0, out=y), dev, steps)
+    # compulsory bytes with the mask in the kernel: the kept entries read, every entry written
+    kept = sum(min(w.cols, r % 128 + 1) for r in range(128)) * (w.rows // 128)
+    b_mask = kept * 4 + w.rows * w.cols * 4
+    out["causal_1048576x128_f32"] = {
+        "read_minus_inf_ms": round(t_read, 5), "in_kernel_mask_ms": round(t_mask, 5),
+        "read_over_mask": round(t_read / t_mask, 3),
+        "in_kernel_mask_gbs": round(b_mask / t_mask / 1e6, 1),
+        "in_kernel_mask_frac_of_measured_hbm": round(b_mask / t_mask / 1e6 / peak, 4)}
     return out
 
 

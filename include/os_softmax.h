@@ -128,6 +128,37 @@ os_status os_softmax_topk(const float *x, float *vals, int32_t *idx, int64_t row
 os_status os_topk(const float *x, float *vals, int32_t *idx, int64_t rows, int64_t cols,
                   int32_t K, os_stream_t stream);
 
+/*
+ * y = softmax(x) row by row under a causal mask applied inside the kernel:
+ * in row r the columns c > (r mod period) + offset are masked (treated as
+ * -inf, never read, written as exactly 0), the attention mask of a query at
+ * position r mod period over keys with `offset` extra leading positions
+ * ("6.2 FlashAttention V2": the causal mask applied while the row is
+ * processed rather than stored in the input).
+ *   period >= 1, offset >= 0 (so every row keeps at least column 0), else
+ *   OS_ERR_SHAPE.  Other arguments, checks and layout as os_softmax_fwd.
+ * Rows of up to 256 16-byte vectors run on the WARP family, longer ones on
+ * STREAM; masked columns cost no reads.
+ */
+os_status os_softmax_causal_fwd(const void *x, void *y, int64_t rows, int64_t cols,
+                                int64_t period, int64_t offset, os_dtype in_dtype,
+                                os_dtype out_dtype, os_stream_t stream);
+
+/*
+ * The online normalizer's state of every row, without normalising ("Online
+ * normalizer calculation for softmax", section 3): m[r] = max_j x[r, j],
+ * d[r] = sum_j e^(x[r, j] - m[r]) (so 1 <= d[r] <= the number of finite
+ * entries), and lse[r] = m[r] + ln d[r], the row's log-sum-exp ("6.2
+ * FlashAttention V2" keeps it per row for the backward pass).  One read of x.
+ *   x    device pointer, rows*cols of in_dtype (OS_F32 or OS_BF16).
+ *   m, d, lse  device pointers to rows fp32 each, written; any of them may be
+ *        NULL (not written) but not all three (OS_ERR_NULL).  They must not
+ *        overlap x or one another (OS_ERR_ALIAS).
+ * Rows that are all -inf give m = -inf, d = 0, lse = -inf.
+ */
+os_status os_softmax_stats(const void *x, float *m, float *d, float *lse, int64_t rows,
+                           int64_t cols, os_dtype in_dtype, os_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *os_status_string(os_status status);
 

@@ -12,8 +12,9 @@ ctypes/numpy.  Inputs of any real dtype are widened to float64 exactly
 Functions and the passages they follow are listed in ``oracle.c``'s header:
 ``softmax`` (three-pass safe softmax), ``row_stats`` ((m, d) by definition),
 ``online_stats`` (the single-pass recurrence), ``combine`` (the binary
-operator on (m, d) with identity (-inf, 0)) and ``topk`` (full sort by
-logit descending, index ascending; v = e^(u - m)/d).
+operator on (m, d) with identity (-inf, 0)), ``topk`` (full sort by
+logit descending, index ascending; v = e^(u - m)/d), ``lse`` (m + ln d) and
+``causal_mask`` / ``softmax_causal`` (the causal mask, then softmax).
 """
 from __future__ import annotations
 
@@ -65,6 +66,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.oracle_topk_f64.argtypes = [_dbl_p, _dbl_p, _i32_p, ctypes.c_int64, ctypes.c_int64,
                                     ctypes.c_int32]
     lib.oracle_topk_f64.restype = ctypes.c_int
+    lib.oracle_lse_f64.argtypes = [_dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64]
+    lib.oracle_causal_mask_f64.argtypes = [_dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_int64]
     return lib
 
 
@@ -141,3 +145,25 @@ def topk(x, K: int, lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, np.ndar
     if rc != 0:
         raise ValueError(f"oracle topk rejected K={K} for {cols} columns")
     return vals, idx
+
+
+def lse(x, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Per-row log-sum-exp, m + ln d (-inf for rows that are all -inf)."""
+    a = _as_rows(x)
+    out = np.empty(a.shape[0])
+    (lib or _get()).oracle_lse_f64(_p(a), _p(out), a.shape[0], a.shape[1])
+    return out
+
+
+def causal_mask(x, period: int, offset: int = 0, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """x with the entries c > (r mod period) + offset of row r set to -inf."""
+    a = _as_rows(x)
+    out = np.empty_like(a)
+    (lib or _get()).oracle_causal_mask_f64(_p(a), _p(out), a.shape[0], a.shape[1], int(period),
+                                           int(offset))
+    return out
+
+
+def softmax_causal(x, period: int, offset: int = 0, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """float64 softmax of each row of ``x`` under the causal mask above."""
+    return softmax(causal_mask(x, period, offset, lib=lib), lib=lib)

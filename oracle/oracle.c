@@ -89,6 +89,31 @@ void oracle_softmax_f64(const double *x, double *y, int64_t rows, int64_t cols) 
     }
 }
 
+/* Log-sum-exp of each row, ln sum_j e^(x_j) = m + ln d: the online
+ * normalizer's state (m, d) of "Online normalizer calculation for softmax"
+ * (notes), section 3, folded into one number ("6.2 FlashAttention V2" keeps it
+ * per row).  Rows that are all -inf give -inf. */
+void oracle_lse_f64(const double *x, double *lse, int64_t rows, int64_t cols) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double m, d;
+        row_stats(x + r * cols, cols, &m, &d);
+        lse[r] = m == -INFINITY ? -INFINITY : m + log(d);
+    }
+}
+
+/* Causal mask: row r keeps columns c <= (r mod period) + offset, the query
+ * position r mod period seeing keys up to its own position shifted by
+ * `offset` ("6.2 FlashAttention V2", causal masking); the other entries
+ * become -inf.  period >= 1. */
+void oracle_causal_mask_f64(const double *x, double *out, int64_t rows, int64_t cols,
+                            int64_t period, int64_t offset) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * cols + c] = c > (r % period) + offset ? -INFINITY : x[r * cols + c];
+}
+
 /* The online normalizer recurrence, one element at a time, from (-inf, 0). */
 void oracle_online_stats_f64(const double *x, int64_t n, double *m_out, double *d_out) {
     double m = -INFINITY, d = 0.0;

@@ -1,13 +1,15 @@
 """Python binding of libos_softmax.so (row-wise online softmax, fused softmax+TopK).
 
 The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
-``os_softmax_fwd``, ``os_softmax_topk``, ``os_topk``, ``os_softmax_fwd_path``,
+``os_softmax_fwd``, ``os_softmax_topk``, ``os_topk``, ``os_softmax_causal_fwd``,
+``os_softmax_stats``, ``os_softmax_fwd_path``,
 ``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_device_status``,
 ``os_set_wait_timeout_ns``, ``os_set_fault_injection``, ``os_status_string``.  They take raw
 device pointers (ints) and a raw stream handle, exactly like the C functions,
 and raise ``OsError`` on a non-OK status.
 
-``softmax``, ``softmax_topk`` and ``topk`` are the tensor-level conveniences: they take
+``softmax``, ``softmax_topk``, ``topk``, ``softmax_causal`` and ``softmax_stats`` are the
+tensor-level conveniences: they take
 torch CUDA tensors, allocate outputs with torch, pass the current torch
 stream, and call the same C entry points.  PyTorch only provides memory and
 streams; every step of the computation runs in the library's CUDA kernels.
@@ -62,6 +64,8 @@ def _load() -> ctypes.CDLL:
     lib.os_softmax_fwd_path.argtypes = [vp, vp, i64, i64, st, st, st, vp]
     lib.os_softmax_topk.argtypes = [vp, vp, vp, i64, i64, i32, vp]
     lib.os_topk.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+    lib.os_softmax_causal_fwd.argtypes = [vp, vp, i64, i64, i64, i64, st, st, vp]
+    lib.os_softmax_stats.argtypes = [vp, vp, vp, vp, i64, i64, st, vp]
     lib.os_softmax_plan.argtypes = [i64, i64, st, st, st, ctypes.POINTER(Plan)]
     lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
     lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
@@ -70,7 +74,8 @@ def _load() -> ctypes.CDLL:
     lib.os_set_fault_injection.argtypes = [i32]
     lib.os_status_string.argtypes = [st]
     lib.os_status_string.restype = ctypes.c_char_p
-    for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_topk", "os_softmax_plan",
+    for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_topk",
+                 "os_softmax_causal_fwd", "os_softmax_stats", "os_softmax_plan",
                  "os_topk_plan", "os_exp_f32", "os_device_status", "os_set_wait_timeout_ns",
                  "os_set_fault_injection"):
         getattr(lib, name).restype = st
@@ -109,6 +114,17 @@ def os_softmax_topk(x: int, vals: int, idx: int, rows: int, cols: int, K: int,
 def os_topk(x: int, vals: int, idx: int, rows: int, cols: int, K: int,
             stream: int | None) -> None:
     _check(_lib.os_topk(x, vals, idx, rows, cols, K, stream), "os_topk")
+
+
+def os_softmax_causal_fwd(x: int, y: int, rows: int, cols: int, period: int, offset: int,
+                          in_dtype: int, out_dtype: int, stream: int | None) -> None:
+    _check(_lib.os_softmax_causal_fwd(x, y, rows, cols, period, offset, in_dtype, out_dtype,
+                                      stream), "os_softmax_causal_fwd")
+
+
+def os_softmax_stats(x: int, m: int | None, d: int | None, lse: int | None, rows: int, cols: int,
+                     in_dtype: int, stream: int | None) -> None:
+    _check(_lib.os_softmax_stats(x, m, d, lse, rows, cols, in_dtype, stream), "os_softmax_stats")
 
 
 def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
@@ -224,6 +240,34 @@ def topk(x, K: int, vals=None, idx=None):
         os_topk(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, x.shape[1], K,
                 _stream_handle(x))
     return vals, idx
+
+
+def softmax_causal(x, period: int, offset: int = 0, out_dtype=None, out=None):
+    """softmax(x) with columns c > (r mod period) + offset of row r masked in the kernel."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D CUDA tensor")
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    with _OnDevice(x.device):
+        os_softmax_causal_fwd(x.data_ptr(), out.data_ptr(), x.shape[0], x.shape[1], int(period),
+                              int(offset), _dtype_code(x.dtype), _dtype_code(out.dtype),
+                              _stream_handle(x))
+    return out
+
+
+def softmax_stats(x):
+    """(m, d, lse) fp32 [rows] each: row maximum, sum of e^(x - m), and m + ln d."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D CUDA tensor")
+    rows = x.shape[0]
+    m, d, lse = (torch.empty(rows, dtype=torch.float32, device=x.device) for _ in range(3))
+    with _OnDevice(x.device):
+        os_softmax_stats(x.data_ptr(), m.data_ptr(), d.data_ptr(), lse.data_ptr(), rows,
+                         x.shape[1], _dtype_code(x.dtype), _stream_handle(x))
+    return m, d, lse
 
 
 def exp(z):

@@ -45,8 +45,8 @@ bool make_ctl(os::KernelCtl* ctl) {
 }
 
 using PlanFn = os_status (*)(int64_t, int64_t, os_path, bool, os_plan*);
-using LaunchFn = cudaError_t (*)(const os_plan&, const void*, void*, int64_t, int, bool,
-                                 const os::KernelCtl&, cudaStream_t);
+using LaunchFn = cudaError_t (*)(const os_plan&, const void*, void*, int64_t, int, bool, int64_t,
+                                 int64_t, const os::KernelCtl&, cudaStream_t);
 
 struct Pair {
     PlanFn plan;
@@ -89,6 +89,39 @@ os_status topk_checks(int64_t rows, int64_t cols, int32_t K) {
     return OS_OK;
 }
 
+// period > 0: causal mask; only the WARP and STREAM families take one, and AUTO
+// picks between those two.
+os_status softmax_entry(const void* x, void* y, int64_t rows, int64_t cols, os_dtype in,
+                        os_dtype out, os_path path, int64_t period, int64_t offset,
+                        os_stream_t stream) {
+    os_status st = softmax_checks(rows, cols, in, out, path);
+    if (st != OS_OK) return st;
+    if (rows == 0) return OS_OK;
+    if (!x || !y) return OS_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(x) % elem_bytes(in) ||
+        reinterpret_cast<uintptr_t>(y) % elem_bytes(out))
+        return OS_ERR_ALIGN;
+    if (overlaps(x, rows * cols * elem_bytes(in), y, rows * cols * elem_bytes(out)))
+        return OS_ERR_ALIAS;
+    if (period > 0) {
+        const int64_t nv = (cols + elems_per_vector(in) - 1) / elems_per_vector(in);
+        if (path == OS_PATH_AUTO) path = nv <= 256 ? OS_PATH_WARP : OS_PATH_STREAM;
+        if (path != OS_PATH_WARP && path != OS_PATH_STREAM) return OS_ERR_PATH;
+    }
+    const bool ptrs_aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                              reinterpret_cast<uintptr_t>(y) % 16 == 0;
+    os_plan plan;
+    st = kPairs[in][out].plan(rows, cols, path, ptrs_aligned, &plan);
+    if (st != OS_OK) return st;
+    os::KernelCtl ctl;
+    if (!make_ctl(&ctl)) return OS_ERR_CUDA;
+    const bool aligned = ptrs_aligned && cols % elems_per_vector(in) == 0;
+    const cudaError_t e = kPairs[in][out].launch(plan, x, y, rows, static_cast<int>(cols), aligned,
+                                                 period, offset, ctl,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -119,25 +152,37 @@ os_status os_softmax_plan(int64_t rows, int64_t cols, os_dtype in, os_dtype out,
 
 os_status os_softmax_fwd_path(const void* x, void* y, int64_t rows, int64_t cols, os_dtype in,
                               os_dtype out, os_path path, os_stream_t stream) {
-    os_status st = softmax_checks(rows, cols, in, out, path);
-    if (st != OS_OK) return st;
+    return softmax_entry(x, y, rows, cols, in, out, path, 0, 0, stream);
+}
+
+os_status os_softmax_causal_fwd(const void* x, void* y, int64_t rows, int64_t cols,
+                                int64_t period, int64_t offset, os_dtype in, os_dtype out,
+                                os_stream_t stream) {
+    if (period < 1 || offset < 0) return OS_ERR_SHAPE;
+    return softmax_entry(x, y, rows, cols, in, out, OS_PATH_AUTO, period, offset, stream);
+}
+
+os_status os_softmax_stats(const void* x, float* m, float* d, float* lse, int64_t rows,
+                           int64_t cols, os_dtype in, os_stream_t stream) {
+    if (!valid_dtype(in)) return OS_ERR_DTYPE;
+    if (!shape_ok(rows, cols)) return OS_ERR_SHAPE;
     if (rows == 0) return OS_OK;
-    if (!x || !y) return OS_ERR_NULL;
-    if (reinterpret_cast<uintptr_t>(x) % elem_bytes(in) ||
-        reinterpret_cast<uintptr_t>(y) % elem_bytes(out))
+    if (!x || (!m && !d && !lse)) return OS_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(x) % elem_bytes(in) || reinterpret_cast<uintptr_t>(m) % 4 ||
+        reinterpret_cast<uintptr_t>(d) % 4 || reinterpret_cast<uintptr_t>(lse) % 4)
         return OS_ERR_ALIGN;
-    if (overlaps(x, rows * cols * elem_bytes(in), y, rows * cols * elem_bytes(out)))
-        return OS_ERR_ALIAS;
-    const bool ptrs_aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
-                              reinterpret_cast<uintptr_t>(y) % 16 == 0;
-    os_plan plan;
-    st = kPairs[in][out].plan(rows, cols, path, ptrs_aligned, &plan);
-    if (st != OS_OK) return st;
-    os::KernelCtl ctl;
-    if (!make_ctl(&ctl)) return OS_ERR_CUDA;
-    const bool aligned = ptrs_aligned && cols % elems_per_vector(in) == 0;
-    const cudaError_t e = kPairs[in][out].launch(plan, x, y, rows, static_cast<int>(cols), aligned,
-                                                 ctl, reinterpret_cast<cudaStream_t>(stream));
+    const int64_t xb = rows * cols * elem_bytes(in), ob = rows * 4;
+    const float* outs[3] = {m, d, lse};
+    for (int i = 0; i < 3; ++i) {
+        if (!outs[i]) continue;
+        if (overlaps(x, xb, outs[i], ob)) return OS_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (outs[j] && overlaps(outs[i], ob, outs[j], ob)) return OS_ERR_ALIAS;
+    }
+    const bool aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0 && cols % elems_per_vector(in) == 0;
+    if (!os::device_info()) return OS_ERR_CUDA;
+    const cudaError_t e = os::launch_stats(x, in, m, d, lse, rows, static_cast<int>(cols), aligned,
+                                           reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
 }
 

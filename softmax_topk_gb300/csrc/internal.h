@@ -15,8 +15,8 @@ namespace os {
     os_status plan_softmax_##NAME(int64_t rows, int64_t cols, os_path path, bool aligned,      \
                                   os_plan* p);                                                 \
     cudaError_t launch_softmax_##NAME(const os_plan& p, const void* x, void* y, int64_t rows,  \
-                                      int cols, bool aligned, const KernelCtl& ctl,            \
-                                      cudaStream_t stream);
+                                      int cols, bool aligned, int64_t period, int64_t offset,  \
+                                      const KernelCtl& ctl, cudaStream_t stream);
 
 OS_DECLARE_SOFTMAX_PAIR(f32_f32)
 OS_DECLARE_SOFTMAX_PAIR(bf16_bf16)
@@ -30,5 +30,9 @@ cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* 
                         cudaStream_t stream);
 
 cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t stream);
+
+// (m, d, lse) of every row; any output may be NULL
+cudaError_t launch_stats(const void* x, os_dtype in, float* m, float* d, float* lse, int64_t rows,
+                         int cols, bool aligned, cudaStream_t stream);
 
 }  // namespace os

@@ -40,6 +40,14 @@ constexpr float kNegInf = -__builtin_huge_valf();
 
 // Load vector slot v of a row (elements v*EPV .. v*EPV+EPV-1) into out[];
 // elements at or beyond `cols` read as -inf.
+// Column limit of row `row` under a causal mask: columns c > (row mod period)
+// + offset are masked; period 0 means no mask (the whole row).
+__device__ __forceinline__ int causal_limit(int64_t row, int cols, int64_t period, int64_t offset) {
+    if (period <= 0) return cols;
+    const int64_t lim = row % period + offset + 1;
+    return int(lim < cols ? (lim > 0 ? lim : 0) : cols);
+}
+
 template <typename TI>
 __device__ __forceinline__ void load_slot(const TI* row, int64_t v, int cols, bool aligned,
                                           float* out) {
@@ -140,7 +148,7 @@ __device__ __forceinline__ void scale_all(float* e, float s) {
 template <typename TI, typename TO, int L, int VPT, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 warp_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
-                 int aligned) {
+                 int aligned, int64_t period, int64_t offset) {
     constexpr int EPV = VecTraits<TI>::EPV, EPT = VPT * EPV, RPW = 32 / L;
     const int lane_in_row = threadIdx.x % L;
     const int64_t warp = (int64_t(blockIdx.x) * THREADS + threadIdx.x) / 32;
@@ -152,13 +160,15 @@ warp_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
         const bool live = row < rows;
         const TI* xr = x + (live ? row : 0) * int64_t(cols);
         TO* yr = y + (live ? row : 0) * int64_t(cols);
+        // causal mask: columns at or past `lim` are -inf and never read
+        const int lim = live ? causal_limit(row, cols, period, offset) : 0;
 
         float e[EPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int64_t v = int64_t(k) * L + lane_in_row;
-            if (live && v < nv) {
-                load_slot(xr, v, cols, aligned, e + k * EPV);
+            if (v * EPV < lim) {
+                load_slot(xr, v, lim, aligned && (v + 1) * EPV <= lim, e + k * EPV);
             } else {
 #pragma unroll
                 for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
@@ -507,31 +517,41 @@ struct Chunk {
     }
 };
 
-// Vectors tid + k*THREADS (k < UNROLL) of chunk c of a range of `len`
-// vectors starting at vector `begin` of the row (xs points at that vector);
-// slots past the range (and, unaligned, columns past `cols`) read as -inf.
-template <typename TI, int THREADS, int UNROLL, bool ALIGNED>
-__device__ __forceinline__ void load_stream_chunk(const TI* xs, int c, int len, int begin, int cols,
-                                                  uint64_t policy, Chunk<TI, UNROLL>& ch) {
-    constexpr int EPV = VecTraits<TI>::EPV, STEP = THREADS * UNROLL;
-    const int v0 = c * STEP + int(threadIdx.x);
-    const bool full = c * STEP + STEP <= len;
+// Which vectors of a CTA's range [begin, begin + len) hold columns below a
+// limit `lim` (the row length, or its causal limit): [0, full) wholly,
+// [full, any) in part.
+struct VecLimits {
+    int full, any;
+};
+template <int EPV>
+__device__ __forceinline__ VecLimits vec_limits(int len, int begin, int lim) {
+    return {min(len, max(0, lim / EPV - begin)), min(len, max(0, (lim + EPV - 1) / EPV - begin))};
+}
+
+// Vectors t + k*GROUP (k < UNROLL) of chunk c of a CTA's range that starts
+// at vector `begin` of the row (xs points at that vector).  Columns at or
+// past `lim` read as -inf; vectors wholly past it are not loaded at all.
+template <typename TI, int GROUP, int UNROLL, bool ALIGNED>
+__device__ __forceinline__ void load_stream_chunk(const TI* xs, int c, VecLimits vl, int begin,
+                                                  int lim, uint64_t policy, Chunk<TI, UNROLL>& ch,
+                                                  int t) {
+    constexpr int EPV = VecTraits<TI>::EPV, STEP = GROUP * UNROLL;
+    const int v0 = c * STEP + t;
+    const bool full = c * STEP + STEP <= vl.full;
     const uint32_t neg_inf_word = sizeof(TI) == 2 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
-        const int v = v0 + k * THREADS;
-        if (full || v < len) {
-            if constexpr (ALIGNED) {
-                ch.raw[k] = ld_policy_v4(xs + v * EPV, policy);
-            } else {
-                TI tmp[EPV];
+        const int v = v0 + k * GROUP;
+        if (ALIGNED && (full || v < vl.full)) {
+            ch.raw[k] = ld_policy_v4(xs + v * EPV, policy);
+        } else if (full || v < vl.any) {
+            TI tmp[EPV];
 #pragma unroll
-                for (int q = 0; q < EPV; ++q) {
-                    const int j = (begin + v) * EPV + q;
-                    tmp[q] = j < cols ? xs[v * EPV + q] : from_f32<TI>(kNegInf);
-                }
-                ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
+            for (int q = 0; q < EPV; ++q) {
+                const int j = (begin + v) * EPV + q;
+                tmp[q] = j < lim ? xs[v * EPV + q] : from_f32<TI>(kNegInf);
             }
+            ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
         } else {
             ch.raw[k] = make_uint4(neg_inf_word, neg_inf_word, neg_inf_word, neg_inf_word);
         }
@@ -590,7 +610,8 @@ __device__ __forceinline__ float exp_sum_z(const float* z) {
 // lying wholly inside the CTA's range skip the per-vector range checks.
 template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER, bool ALIGNED>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
-stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols) {
+stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+                   int64_t period, int64_t offset) {
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV;
     constexpr bool FAST = fast_exp_for<TO>();
     constexpr int STEP = THREADS * UNROLL;  // vectors per chunk
@@ -607,19 +628,24 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
     const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     if (CLUSTER > 1) cluster_sync();
 
-    auto load_chunk = [&](const TI* xs, int c, uint64_t policy, Chunk<TI, UNROLL>& ch) {
-        load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, begin, cols, policy, ch);
-    };
-
     int parity = 0;
     for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
         const TI* xs = x + row * int64_t(cols) + int64_t(begin) * EPV;
         TO* ys = y + row * int64_t(cols) + int64_t(begin) * EPV;
+        // columns at or past `lim` are masked (-inf, never read): chunks from
+        // `live` on hold none of this CTA's unmasked columns
+        const int lim = causal_limit(row, cols, period, offset);
+        const VecLimits vl = vec_limits<EPV>(len, begin, lim);
+        const int live = (vl.any + STEP - 1) / STEP;
+        auto load_chunk = [&](int c, uint64_t policy, Chunk<TI, UNROLL>& ch) {
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, begin, lim, policy, ch,
+                                                            int(threadIdx.x));
+        };
         // pass 1: running (m, d), one rescale per chunk of UNROLL vectors
         float m = kNegInf, d = 0.f;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < live; ++c) {
             Chunk<TI, UNROLL> ch;
-            load_chunk(xs, c, keep, ch);
+            load_chunk(c, keep, ch);
             if (c < NS) {  // kept on chip for pass 2 (thread-private slots)
 #pragma unroll
                 for (int k = 0; k < UNROLL; ++k) kept[(c * UNROLL + k) * THREADS + threadIdx.x] = ch.raw[k];
@@ -636,11 +662,11 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
         // pass 2, last chunk first: y = e^(x - m) / d
         for (int c = nchunks - 1; c >= 0; --c) {
             Chunk<TI, UNROLL> ch;
-            if (c < NS) {
+            if (c < NS && c < live) {
 #pragma unroll
                 for (int k = 0; k < UNROLL; ++k) ch.raw[k] = kept[(c * UNROLL + k) * THREADS + threadIdx.x];
             } else {
-                load_chunk(xs, c, drop, ch);
+                load_chunk(c, drop, ch);  // masked chunks: -inf without a load, written as 0
             }
             float e[EPC];
             ch.shifted(md.x, e);
@@ -693,17 +719,20 @@ safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const TI* xs = x + row * int64_t(cols);
         TO* ys = y + row * int64_t(cols);
+        const VecLimits vl = vec_limits<EPV>(len, 0, cols);
         float m = kNegInf;
         for (int c = 0; c < nchunks; ++c) {  // pass 1: maximum
             Chunk<TI, UNROLL> ch;
-            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, 0, cols, normal, ch);
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, normal, ch,
+                                                            int(threadIdx.x));
             m = fmaxf(m, ch.max());
         }
         m = block_reduce(m, true);
         float d = 0.f;
         for (int c = 0; c < nchunks; ++c) {  // pass 2: normalizer
             Chunk<TI, UNROLL> ch;
-            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, 0, cols, normal, ch);
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, normal, ch,
+                                                            int(threadIdx.x));
             float z[EPC];
             ch.shifted(m, z);
             d += exp_sum_z<EPC, FAST>(z);
@@ -713,7 +742,8 @@ safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
         const float neg_log2_d = -__log2f(d);
         for (int c = 0; c < nchunks; ++c) {  // pass 3: outputs
             Chunk<TI, UNROLL> ch;
-            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, len, 0, cols, normal, ch);
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, normal, ch,
+                                                            int(threadIdx.x));
             float e[EPC];
             ch.shifted(m, e);
 #pragma unroll
@@ -724,6 +754,56 @@ safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
                 e[i + 1] = p.y;
             }
             store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, len, 0, cols, e);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// stats_rows: the online normalizer's state of each row, without the
+// normalisation ("Online normalizer calculation for softmax" (notes), section
+// 3): m = max_j x_j and d = sum_j e^(x_j - m) in one read of the row, one
+// rescale per chunk, then lse = m + ln d.  GROUP threads share a row: 32 (a
+// warp per row, for rows of up to 32 x UNROLL vectors) or THREADS (the CTA).
+// Outputs given as NULL are not written.
+template <typename TI, int THREADS, int GROUP, int UNROLL, bool ALIGNED>
+__global__ void __launch_bounds__(THREADS)
+stats_rows_kernel(const TI* __restrict__ x, float* __restrict__ m_out, float* __restrict__ d_out,
+                  float* __restrict__ lse_out, int64_t rows, int cols) {
+    static_assert(GROUP == 32 || GROUP == THREADS, "a warp or the whole CTA per row");
+    constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV, STEP = GROUP * UNROLL;
+    constexpr int GPC = THREADS / GROUP;  // rows in flight per CTA
+    __shared__ RowMergeSmem<THREADS, 1> sm;
+    const int t = int(threadIdx.x) % GROUP;
+    const int64_t g0 = int64_t(blockIdx.x) * GPC + threadIdx.x / GROUP;
+    const int64_t ng = int64_t(gridDim.x) * GPC;
+    const int len = (cols + EPV - 1) / EPV;
+    const int nchunks = (len + STEP - 1) / STEP;
+    const VecLimits vl = vec_limits<EPV>(len, 0, cols);
+    const uint64_t policy = l2_policy_evict_first();  // read once
+    int parity = 0;
+    for (int64_t row = g0; row < rows; row += ng, parity ^= 1) {  // uniform per group
+        const TI* xs = x + row * int64_t(cols);
+        float m = kNegInf, d = 0.f;
+        for (int c = 0; c < nchunks; ++c) {
+            Chunk<TI, UNROLL> ch;
+            load_stream_chunk<TI, GROUP, UNROLL, ALIGNED>(xs, c, vl, 0, cols, policy, ch, t);
+            const float m_new = fmaxf(m, ch.max());
+            float z[EPC];
+            ch.shifted(m_new, z);
+            d = d * rescale(m, m_new) + exp_sum_z<EPC, false>(z);
+            m = m_new;
+        }
+        float2 md;
+        if constexpr (GROUP == 32) {
+            group_merge<32>(m, d);
+            md = make_float2(m, d);
+        } else {
+            md = merge_row_state<THREADS, 1>(sm, m, d, parity, 0);
+        }
+        if (t == 0) {
+            if (m_out) m_out[row] = md.x;
+            if (d_out) d_out[row] = md.y;
+            if (lse_out) lse_out[row] = md.x + logf(md.y);  // all -inf: -inf + -inf
         }
     }
 }

@@ -49,6 +49,7 @@ template <typename TI> constexpr int tma_ept() { return sizeof(TI) == 4 ? 32 : 6
 template <typename TI, typename TO>
 struct SoftmaxFamily {
     using Kernel = void (*)(const TI*, TO*, int64_t, int, int);
+    using WarpKernel = void (*)(const TI*, TO*, int64_t, int, int, int64_t, int64_t);
     using TmaKernel = void (*)(const TI*, TO*, int64_t, int, KernelCtl);
     static constexpr int EPV = VecTraits<TI>::EPV;
     static constexpr int VPT = kOnchipElemsPerThread / EPV;
@@ -56,7 +57,7 @@ struct SoftmaxFamily {
     static constexpr int TMA_EPT = tma_ept<TI>();
     using Ring = TmaRing<TI, kTmaThreads, TMA_EPT, TMA_STAGES>;
 
-    static Kernel warp(int lanes, int vpt) {
+    static WarpKernel warp(int lanes, int vpt) {
         if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads>;
         switch (lanes) {
             case 1: return warp_rows_kernel<TI, TO, 1, 4, kWarpThreads>;
@@ -93,8 +94,9 @@ struct SoftmaxFamily {
         }
     }
     static constexpr int STREAM_UNROLL = stream_unroll<TI>();
-    using StreamKernel = void (*)(const TI*, TO*, int64_t, int);
-    static StreamKernel safe(bool aligned) {
+    using SafeKernel = void (*)(const TI*, TO*, int64_t, int);
+    using StreamKernel = void (*)(const TI*, TO*, int64_t, int, int64_t, int64_t);
+    static SafeKernel safe(bool aligned) {
         constexpr int T = kStreamThreads, U = STREAM_UNROLL;
         return aligned ? safe_rows_kernel<TI, TO, T, U, true> : safe_rows_kernel<TI, TO, T, U, false>;
     }
@@ -223,8 +225,11 @@ struct SoftmaxFamily {
         return OS_OK;
     }
 
+    // period > 0: causal mask (columns c > (row mod period) + offset masked);
+    // only the WARP and STREAM families take one.
     static cudaError_t launch(const os_plan& p, const void* x, void* y, int64_t rows, int cols,
-                              bool aligned, const KernelCtl& ctl, cudaStream_t stream) {
+                              bool aligned, int64_t period, int64_t offset, const KernelCtl& ctl,
+                              cudaStream_t stream) {
         const TI* xi = static_cast<const TI*>(x);
         TO* yo = static_cast<TO*>(y);
         if (p.path == OS_PATH_ONCHIP && p.stages > 0) {
@@ -234,7 +239,7 @@ struct SoftmaxFamily {
                                  rows, cols, ctl);
         }
         if (p.path == OS_PATH_SAFE) {
-            StreamKernel k = safe(aligned);
+            SafeKernel k = safe(aligned);
             if (!prepare_kernel(k, 1, 0)) return cudaErrorInvalidValue;
             return launch_kernel(k, p.grid, p.threads, 1, 0, stream, xi, yo, rows, cols);
         }
@@ -242,13 +247,16 @@ struct SoftmaxFamily {
             StreamKernel k = streaming(p.cluster, aligned);
             const int smem = stream_smem_bytes();
             if (!prepare_kernel(k, p.cluster, smem)) return cudaErrorInvalidValue;
-            return launch_kernel(k, p.grid, p.threads, p.cluster, smem, stream, xi, yo, rows, cols);
+            return launch_kernel(k, p.grid, p.threads, p.cluster, smem, stream, xi, yo, rows, cols,
+                                 period, offset);
         }
-        Kernel k = nullptr;
-        switch (p.path) {
-            case OS_PATH_WARP: k = warp(p.lanes_per_row, p.vectors_per_thread); break;
-            default: k = onchip(p.threads, p.cluster); break;
+        if (p.path == OS_PATH_WARP) {
+            WarpKernel k = warp(p.lanes_per_row, p.vectors_per_thread);
+            if (!prepare_kernel(k, 1, 0)) return cudaErrorInvalidValue;
+            return launch_kernel(k, p.grid, p.threads, 1, 0, stream, xi, yo, rows, cols,
+                                 aligned ? 1 : 0, period, offset);
         }
+        Kernel k = onchip(p.threads, p.cluster);
         if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
         return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, xi, yo, rows, cols,
                              aligned ? 1 : 0);
@@ -265,8 +273,9 @@ struct SoftmaxFamily {
         return SoftmaxFamily<TI, TO>::plan(rows, cols, path, aligned, p);                      \
     }                                                                                          \
     cudaError_t launch_softmax_##NAME(const os_plan& p, const void* x, void* y, int64_t rows,  \
-                                      int cols, bool aligned, const KernelCtl& ctl,            \
-                                      cudaStream_t stream) {                                   \
-        return SoftmaxFamily<TI, TO>::launch(p, x, y, rows, cols, aligned, ctl, stream);      \
+                                      int cols, bool aligned, int64_t period, int64_t offset,  \
+                                      const KernelCtl& ctl, cudaStream_t stream) {             \
+        return SoftmaxFamily<TI, TO>::launch(p, x, y, rows, cols, aligned, period, offset, ctl, \
+                                             stream);                                          \
     }                                                                                          \
     }

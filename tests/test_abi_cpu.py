@@ -108,6 +108,29 @@ def test_topk_argument_errors(lib, name):
     assert f(None, None, None, 0, 100, 8, None) == OK
 
 
+def test_stats_argument_errors(lib):
+    f = lib.os_softmax_stats
+    assert f(A, B, C, C + 4096, 4, 8, 2, None) == DTYPE
+    assert f(A, B, C, C + 4096, -1, 8, F32, None) == SHAPE
+    assert f(A, B, C, C + 4096, 4, 0, F32, None) == SHAPE
+    assert f(None, B, C, C + 4096, 4, 8, F32, None) == NULL
+    assert f(A, None, None, None, 4, 8, F32, None) == NULL
+    assert f(A + 2, B, C, C + 4096, 4, 8, F32, None) == ALIGN
+    assert f(A, A + 16, None, None, 4, 8, F32, None) == ALIAS        # m inside x
+    assert f(A, B, B + 8, None, 4, 8, F32, None) == ALIAS            # m and d overlap
+    assert f(None, None, None, None, 0, 8, F32, None) == OK
+
+
+def test_causal_argument_errors(lib):
+    f = lib.os_softmax_causal_fwd
+    assert f(A, B, 4, 8, 0, 0, F32, F32, None) == SHAPE
+    assert f(A, B, 4, 8, 4, -1, F32, F32, None) == SHAPE
+    assert f(A, B, 4, 8, 4, 0, 2, F32, None) == DTYPE
+    assert f(None, B, 4, 8, 4, 0, F32, F32, None) == NULL
+    assert f(A, A, 4, 8, 4, 0, F32, F32, None) == ALIAS
+    assert f(None, None, 0, 8, 4, 0, F32, F32, None) == OK
+
+
 def test_exp_argument_errors(lib):
     assert lib.os_exp_f32(A, B, -1, None) == SHAPE
     assert lib.os_exp_f32(None, B, 5, None) == NULL

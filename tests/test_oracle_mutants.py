@@ -32,6 +32,14 @@ MUTANTS = {
                               "vals[r * K + k] = exp(m - order[k].x) / d;"),
     "topk_ascending": ("if (a->x > b->x) return -1;\n    if (a->x < b->x) return 1;",
                        "if (a->x < b->x) return -1;\n    if (a->x > b->x) return 1;"),
+    "lse_drops_max": ("lse[r] = m == -INFINITY ? -INFINITY : m + log(d);",
+                      "lse[r] = m == -INFINITY ? -INFINITY : log(d);"),
+    "lse_log10": ("lse[r] = m == -INFINITY ? -INFINITY : m + log(d);",
+                  "lse[r] = m == -INFINITY ? -INFINITY : m + log10(d);"),
+    "causal_mask_off_by_one": ("c > (r % period) + offset ? -INFINITY",
+                               "c >= (r % period) + offset ? -INFINITY"),
+    "causal_mask_ignores_period": ("c > (r % period) + offset ? -INFINITY",
+                                   "c > r + offset ? -INFINITY"),
 }
 
 

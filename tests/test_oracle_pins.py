@@ -225,10 +225,52 @@ def pin_topk_ties_lower_index(lib):
     assert vals[0, 0] == vals[0, 3] and vals[0, 7] == 0.0 and vals[0, 8] == 0.0
 
 
+# ---------------------------------------------------------------- log-sum-exp
+def pin_lse_fsum_and_closed_forms(lib):
+    """lse = ln sum e^x: against an exactly rounded sum on small rows, the
+    constant-row closed form c + ln n, a dyadic shift, and m <= lse <= m + ln n."""
+    rng = np.random.default_rng(21)
+    for n in (1, 2, 3, 7, 40):
+        for _ in range(8):
+            x = rng.normal(size=n) * rng.choice([0.5, 4.0, 30.0])
+            got = oracle.lse(x, lib)[0]
+            ref = math.log(math.fsum(math.exp(v) for v in x))
+            assert abs(got - ref) <= 1e-13 * max(1.0, abs(ref)), (x, got, ref)
+            assert x.max() <= got <= x.max() + math.log(n) + 1e-14
+            assert abs(oracle.lse(x + 8.0, lib)[0] - (got + 8.0)) <= 1e-13 * max(1.0, abs(got))
+    for c, n in ((0.0, 1), (-3.25, 10), (100.0, 4096)):
+        assert abs(oracle.lse(np.full(n, c), lib)[0] - (c + math.log(n))) <= 1e-13 * max(1, abs(c))
+    x = np.array([[1.0, -np.inf, 2.0], [-np.inf, -np.inf, -np.inf]])
+    got = oracle.lse(x, lib)
+    assert abs(got[0] - math.log(math.e + math.e ** 2)) <= 1e-15 and got[1] == -np.inf
+
+
+# ---------------------------------------------------------------- causal mask
+def pin_causal_mask_rows(lib):
+    """Row r keeps columns c <= (r mod period) + offset: masked entries are
+    exactly 0, the kept prefix is the brute-force softmax of that prefix, and a
+    row that keeps only column 0 is [1, 0, ...]."""
+    rng = np.random.default_rng(22)
+    for period, offset, cols in ((4, 0, 4), (6, 2, 9), (3, 0, 8), (5, 10, 7)):
+        x = rng.normal(size=(2 * period + 1, cols)) * 3
+        masked = oracle.causal_mask(x, period, offset, lib)
+        y = oracle.softmax_causal(x, period, offset, lib)
+        for r in range(x.shape[0]):
+            lim = min(cols, r % period + offset + 1)
+            assert np.all(masked[r, lim:] == -np.inf) and np.array_equal(masked[r, :lim], x[r, :lim])
+            assert np.all(y[r, lim:] == 0.0)
+            for i in range(lim):
+                ref = 1.0 / math.fsum(math.exp(x[r, j] - x[r, i]) for j in range(lim))
+                assert abs(y[r, i] - ref) <= 1e-14 * ref
+            if lim == 1:
+                assert y[r, 0] == 1.0
+
+
 PINS = [pin_two_shard_example, pin_identity_element, pin_combine_associative_commutative,
         pin_online_recurrence_equals_definition, pin_normalizer_bound, pin_lesson7_numpy_check,
         pin_closed_forms, pin_shift_invariance, pin_brute_force_tiny_rows, pin_rows_sum_to_one,
-        pin_causal_and_spike_rows, pin_topk_exhaustive, pin_topk_ties_lower_index]
+        pin_causal_and_spike_rows, pin_topk_exhaustive, pin_topk_ties_lower_index,
+        pin_lse_fsum_and_closed_forms, pin_causal_mask_rows]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
