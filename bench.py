@@ -447,8 +447,12 @@ def run_baselines(st, dev, args):
             st.topk(y, K, vals=vals, idx=idx)
         t_online = _time_ms(lambda i: unfused(i, "auto"), dev, steps)
         t_safe = _time_ms(lambda i: unfused(i, "safe"), dev, steps)
+        u = torch.rand(w.rows, device=dev)
+        draws = torch.empty(w.rows, dtype=torch.int32, device=dev)
+        t_sample = _time_ms(lambda i: st.topk_sample(vals, idx, u, out=draws), dev, steps)
         out[f"{TOPK_NAME}_K{K}"] = {
-            "fused_ms": round(t_fused, 5), "online_softmax_then_topk_ms": round(t_online, 5),
+            "fused_ms": round(t_fused, 5), "sample_after_fused_ms": round(t_sample, 5),
+            "online_softmax_then_topk_ms": round(t_online, 5),
             "safe_softmax_then_topk_ms": round(t_safe, 5),
             "unfused_online_over_fused": round(t_online / t_fused, 3),
             "unfused_safe_over_fused": round(t_safe / t_fused, 3)}

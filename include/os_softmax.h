@@ -54,7 +54,7 @@ typedef enum {
     OS_ERR_NULL = 1,    /* a required pointer is NULL (with rows > 0) */
     OS_ERR_SHAPE = 2,   /* rows < 0, cols outside [1, 2^31 - 1] */
     OS_ERR_DTYPE = 3,   /* dtype value not in os_dtype */
-    OS_ERR_K = 4,       /* K outside [1, min(cols, 64)] */
+    OS_ERR_K = 4,       /* K outside [1, min(cols, 256)] */
     OS_ERR_ALIAS = 5,   /* an output overlaps an input or another output */
     OS_ERR_CUDA = 6,    /* the CUDA runtime reported an error (launch or device query) */
     OS_ERR_TIMEOUT = 7, /* a device-side bounded wait gave up (os_device_status) */
@@ -108,7 +108,7 @@ os_status os_softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols,
  *   vals  device pointer, rows*K fp32: vals[r*K + k] = e^(x[r,z] - m_r) / d_r
  *         of the k-th best column z.
  *   idx   device pointer, rows*K int32: the column indices z.
- *   K     1 <= K <= min(cols, 64).
+ *   K     1 <= K <= min(cols, 256).
  * Order: larger logit first; equal logits (ties) go to the LOWER column index.
  * Selection compares the input logits, so distinct logits whose probabilities
  * round to the same fp32 value keep their logit order.  vals and idx must not
@@ -158,6 +158,26 @@ os_status os_softmax_causal_fwd(const void *x, void *y, int64_t rows, int64_t co
  */
 os_status os_softmax_stats(const void *x, float *m, float *d, float *lse, int64_t rows,
                            int64_t cols, os_dtype in_dtype, os_stream_t stream);
+
+/*
+ * Top-K sampling after the fused pass ("Online normalizer calculation for
+ * softmax", section 4, names sampling from the top K as what the fused kernel
+ * feeds): for each row one column drawn from its K entries with probability
+ * proportional to their values, i.e. from the top-K distribution
+ * renormalised.
+ *   vals, idx  device pointers, rows*K: the outputs of os_softmax_topk (or
+ *              os_topk on probabilities), best first; values >= 0.
+ *   u          device pointer, rows fp32 uniform numbers in [0, 1), one per
+ *              row, supplied by the caller (the random source stays outside).
+ *   out        device pointer, rows int32, written: out[r] = idx[r*K + k] for
+ *              the smallest k with p_0 + ... + p_k > u[r] * (p_0 + ... +
+ *              p_{K-1}), every sum and the product rounded to fp32 in index
+ *              order (u >= 1 gives the last entry).  Must not overlap the
+ *              inputs (OS_ERR_ALIAS).
+ *   K          1 <= K <= 256 (OS_ERR_K).
+ */
+os_status os_topk_sample(const float *vals, const int32_t *idx, const float *u, int32_t *out,
+                         int64_t rows, int32_t K, os_stream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *os_status_string(os_status status);

@@ -13,8 +13,9 @@ Functions and the passages they follow are listed in ``oracle.c``'s header:
 ``softmax`` (three-pass safe softmax), ``row_stats`` ((m, d) by definition),
 ``online_stats`` (the single-pass recurrence), ``combine`` (the binary
 operator on (m, d) with identity (-inf, 0)), ``topk`` (full sort by
-logit descending, index ascending; v = e^(u - m)/d), ``lse`` (m + ln d) and
-``causal_mask`` / ``softmax_causal`` (the causal mask, then softmax).
+logit descending, index ascending; v = e^(u - m)/d), ``lse`` (m + ln d),
+``causal_mask`` / ``softmax_causal`` (the causal mask, then softmax) and
+``topk_sample`` (one draw per row from its top-K pairs).
 """
 from __future__ import annotations
 
@@ -69,6 +70,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.oracle_lse_f64.argtypes = [_dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64]
     lib.oracle_causal_mask_f64.argtypes = [_dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_int64, ctypes.c_int64]
+    lib.oracle_topk_sample_f64.argtypes = [_dbl_p, _i32_p, _dbl_p, _i32_p, ctypes.c_int64,
+                                           ctypes.c_int32]
     return lib
 
 
@@ -167,3 +170,17 @@ def causal_mask(x, period: int, offset: int = 0, lib: ctypes.CDLL | None = None)
 def softmax_causal(x, period: int, offset: int = 0, lib: ctypes.CDLL | None = None) -> np.ndarray:
     """float64 softmax of each row of ``x`` under the causal mask above."""
     return softmax(causal_mask(x, period, offset, lib=lib), lib=lib)
+
+
+def topk_sample(vals, idx, u, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """One column per row from its K (value, index) pairs: the smallest k whose
+    partial sum exceeds u times the total (sums in index order)."""
+    v = _as_rows(vals)
+    ix = np.ascontiguousarray(np.asarray(idx, dtype=np.int32).reshape(v.shape))
+    uu = np.ascontiguousarray(np.asarray(u, dtype=np.float64).ravel())
+    if uu.size != v.shape[0]:
+        raise ValueError("one u per row")
+    out = np.empty(v.shape[0], dtype=np.int32)
+    (lib or _get()).oracle_topk_sample_f64(_p(v), _p(ix, _i32_p), _p(uu), _p(out, _i32_p),
+                                           v.shape[0], v.shape[1])
+    return out

@@ -2,7 +2,7 @@
 
 The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
 ``os_softmax_fwd``, ``os_softmax_topk``, ``os_topk``, ``os_softmax_causal_fwd``,
-``os_softmax_stats``, ``os_softmax_fwd_path``,
+``os_softmax_stats``, ``os_topk_sample``, ``os_softmax_fwd_path``,
 ``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_device_status``,
 ``os_set_wait_timeout_ns``, ``os_set_fault_injection``, ``os_status_string``.  They take raw
 device pointers (ints) and a raw stream handle, exactly like the C functions,
@@ -30,7 +30,7 @@ PATHS = {"auto": OS_PATH_AUTO, "warp": OS_PATH_WARP, "onchip": OS_PATH_ONCHIP,
          "stream": OS_PATH_STREAM, "safe": OS_PATH_SAFE}
 STATUS = ["OS_OK", "OS_ERR_NULL", "OS_ERR_SHAPE", "OS_ERR_DTYPE", "OS_ERR_K", "OS_ERR_ALIAS",
           "OS_ERR_CUDA", "OS_ERR_TIMEOUT", "OS_ERR_PATH", "OS_ERR_ALIGN"]
-KMAX = 64
+KMAX = 256
 
 
 class OsError(RuntimeError):
@@ -66,6 +66,7 @@ def _load() -> ctypes.CDLL:
     lib.os_topk.argtypes = [vp, vp, vp, i64, i64, i32, vp]
     lib.os_softmax_causal_fwd.argtypes = [vp, vp, i64, i64, i64, i64, st, st, vp]
     lib.os_softmax_stats.argtypes = [vp, vp, vp, vp, i64, i64, st, vp]
+    lib.os_topk_sample.argtypes = [vp, vp, vp, vp, i64, i32, vp]
     lib.os_softmax_plan.argtypes = [i64, i64, st, st, st, ctypes.POINTER(Plan)]
     lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
     lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
@@ -75,7 +76,7 @@ def _load() -> ctypes.CDLL:
     lib.os_status_string.argtypes = [st]
     lib.os_status_string.restype = ctypes.c_char_p
     for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_topk",
-                 "os_softmax_causal_fwd", "os_softmax_stats", "os_softmax_plan",
+                 "os_softmax_causal_fwd", "os_softmax_stats", "os_topk_sample", "os_softmax_plan",
                  "os_topk_plan", "os_exp_f32", "os_device_status", "os_set_wait_timeout_ns",
                  "os_set_fault_injection"):
         getattr(lib, name).restype = st
@@ -125,6 +126,11 @@ def os_softmax_causal_fwd(x: int, y: int, rows: int, cols: int, period: int, off
 def os_softmax_stats(x: int, m: int | None, d: int | None, lse: int | None, rows: int, cols: int,
                      in_dtype: int, stream: int | None) -> None:
     _check(_lib.os_softmax_stats(x, m, d, lse, rows, cols, in_dtype, stream), "os_softmax_stats")
+
+
+def os_topk_sample(vals: int, idx: int, u: int, out: int, rows: int, K: int,
+                   stream: int | None) -> None:
+    _check(_lib.os_topk_sample(vals, idx, u, out, rows, K, stream), "os_topk_sample")
 
 
 def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
@@ -268,6 +274,24 @@ def softmax_stats(x):
         os_softmax_stats(x.data_ptr(), m.data_ptr(), d.data_ptr(), lse.data_ptr(), rows,
                          x.shape[1], _dtype_code(x.dtype), _stream_handle(x))
     return m, d, lse
+
+
+def topk_sample(vals, idx, u, out=None):
+    """One column per row drawn from its K (probability, column) pairs; u: fp32 [rows] in [0, 1)."""
+    import torch
+    rows, K = vals.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.int32, device=vals.device)
+    with _OnDevice(vals.device):
+        os_topk_sample(vals.data_ptr(), idx.data_ptr(), u.data_ptr(), out.data_ptr(), rows, K,
+                       _stream_handle(vals))
+    return out
+
+
+def softmax_topk_sample(x, K: int, u):
+    """Fused softmax + TopK, then one draw per row: (samples, vals, idx)."""
+    vals, idx = softmax_topk(x, K)
+    return topk_sample(vals, idx, u), vals, idx
 
 
 def exp(z):

@@ -85,7 +85,7 @@ os_status softmax_checks(int64_t rows, int64_t cols, os_dtype in, os_dtype out, 
 
 os_status topk_checks(int64_t rows, int64_t cols, int32_t K) {
     if (!shape_ok(rows, cols)) return OS_ERR_SHAPE;
-    if (K < 1 || K > 64 || int64_t(K) > cols) return OS_ERR_K;
+    if (K < 1 || K > 256 || int64_t(K) > cols) return OS_ERR_K;
     return OS_OK;
 }
 
@@ -132,7 +132,7 @@ const char* os_status_string(os_status s) {
         case OS_ERR_NULL: return "OS_ERR_NULL: a required pointer is NULL";
         case OS_ERR_SHAPE: return "OS_ERR_SHAPE: rows < 0 or cols outside [1, 2^31-1]";
         case OS_ERR_DTYPE: return "OS_ERR_DTYPE: unknown dtype";
-        case OS_ERR_K: return "OS_ERR_K: K outside [1, min(cols, 64)]";
+        case OS_ERR_K: return "OS_ERR_K: K outside [1, min(cols, 256)]";
         case OS_ERR_ALIAS: return "OS_ERR_ALIAS: an output overlaps an input or another output";
         case OS_ERR_CUDA: return "OS_ERR_CUDA: the CUDA runtime reported an error";
         case OS_ERR_TIMEOUT: return "OS_ERR_TIMEOUT: a device-side bounded wait gave up";
@@ -228,6 +228,24 @@ os_status os_softmax_topk(const float* x, float* vals, int32_t* idx, int64_t row
 os_status os_topk(const float* x, float* vals, int32_t* idx, int64_t rows, int64_t cols, int32_t K,
                   os_stream_t stream) {
     return topk_entry(x, vals, idx, rows, cols, K, true, stream);
+}
+
+os_status os_topk_sample(const float* vals, const int32_t* idx, const float* u, int32_t* out,
+                         int64_t rows, int32_t K, os_stream_t stream) {
+    if (rows < 0) return OS_ERR_SHAPE;
+    if (K < 1 || K > 256) return OS_ERR_K;
+    if (rows > INT64_MAX / 8 / K) return OS_ERR_SHAPE;
+    if (rows == 0) return OS_OK;
+    if (!vals || !idx || !u || !out) return OS_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(vals) % 4 || reinterpret_cast<uintptr_t>(idx) % 4 ||
+        reinterpret_cast<uintptr_t>(u) % 4 || reinterpret_cast<uintptr_t>(out) % 4)
+        return OS_ERR_ALIGN;
+    const int64_t kb = rows * int64_t(K) * 4, rb = rows * 4;
+    if (overlaps(out, rb, vals, kb) || overlaps(out, rb, idx, kb) || overlaps(out, rb, u, rb))
+        return OS_ERR_ALIAS;
+    const cudaError_t e = os::launch_topk_sample(vals, idx, u, out, rows, K,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
 }
 
 os_status os_exp_f32(const float* z, float* out, int64_t n, os_stream_t stream) {

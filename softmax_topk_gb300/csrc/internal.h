@@ -31,6 +31,10 @@ cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* 
 
 cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t stream);
 
+// one column per row drawn from its K (value, index) pairs, u[r] in [0, 1)
+cudaError_t launch_topk_sample(const float* vals, const int32_t* idx, const float* u, int32_t* out,
+                               int64_t rows, int K, cudaStream_t stream);
+
 // (m, d, lse) of every row; any output may be NULL
 cudaError_t launch_stats(const void* x, os_dtype in, float* m, float* d, float* lse, int64_t rows,
                          int cols, bool aligned, cudaStream_t stream);

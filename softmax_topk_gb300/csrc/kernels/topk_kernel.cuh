@@ -136,9 +136,7 @@ __device__ __forceinline__ int block_exclusive_scan(int c, int* scratch, int& to
     return before + incl - c;
 }
 
-constexpr int kTopkMaxCluster = 8;
-
-template <int THREADS, int KMAX, int CAP>
+template <int THREADS, int KMAX, int CAP, int MAXC>
 struct TopkSmem {
     uint64_t xbar[2];
     float warp_thr[THREADS / 32];
@@ -149,8 +147,8 @@ struct TopkSmem {
     int flag;
     Cand cand[CAP];
     Cand list[KMAX];
-    float2 xstate[2][kTopkMaxCluster];
-    Cand xlist[2][kTopkMaxCluster][KMAX];
+    float2 xstate[2][MAXC];
+    Cand xlist[2][MAXC][KMAX];
 };
 
 // Dynamic shared memory: per group of chunks and thread, the maximum of each
@@ -179,14 +177,15 @@ struct TopkSegment {
 
 // PLAIN: the K largest values themselves (TopK of x, no softmax): no (m, d)
 // is formed and vals are the selected x.
-template <int THREADS, int U, int KMAX, int CAP, int GROUPS, int FCAP, bool PLAIN>
+// KMAX: largest K; MAXC: largest cluster (CTAs per row) the launch may use.
+template <int THREADS, int U, int KMAX, int MAXC, int CAP, int GROUPS, int FCAP, bool PLAIN>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2)
 topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __restrict__ idx,
                  int64_t rows, int cols, int K, int S, KernelCtl ctl) {
     constexpr int NW = THREADS / 32;
     constexpr int CHUNK = THREADS * U;  // 16-byte blocks per chunk
     static_assert(CAP % 32 == 0 && CAP >= 128 && KMAX <= THREADS, "buffer sizes");
-    __shared__ __align__(16) TopkSmem<THREADS, KMAX, CAP> sm;
+    __shared__ __align__(16) TopkSmem<THREADS, KMAX, CAP, MAXC> sm;
     extern __shared__ __align__(16) unsigned char dyn_raw[];
     auto& dyn = *reinterpret_cast<TopkDynSmem<THREADS, U, GROUPS, FCAP>*>(dyn_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -452,7 +451,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
         // shared memory (its round trips are slow while the SM's other CTA
         // streams).
         {
-            constexpr int RC = 8;
+            constexpr int RC = KMAX > 64 ? 16 : 8;  // candidates cached per lane
             Cand reg[RC];
 #pragma unroll
             for (int j = 0; j < RC; ++j) reg[j] = lane + 32 * j < n ? sm.cand[lane + 32 * j] : pad;

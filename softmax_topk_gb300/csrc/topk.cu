@@ -2,8 +2,9 @@
 //
 // Persistent CTAs of 512 threads, two per SM, each taking whole rows in
 // chunks of 4 16-byte blocks per thread (8192 fp32); with fewer rows than
-// resident CTAs a row is split over a cluster of S CTAs (S <= 8, and no more
-// CTAs than the row has chunks) that merge through distributed shared memory.
+// resident CTAs a row is split over a cluster of S CTAs (S <= 8 for K <= 64,
+// S <= 2 for K up to 256, and no more CTAs than the row has chunks) that merge
+// through distributed shared memory.
 #include "host_common.h"
 #include "internal.h"
 #include "kernels/topk_kernel.cuh"
@@ -12,30 +13,36 @@ namespace os {
 
 constexpr int kTopkThreads = 512;
 constexpr int kTopkVpt = 4;      // 16-byte blocks per thread per chunk
-constexpr int kTopkKmax = 64;
 constexpr int kTopkCap = 2048;   // candidates
 constexpr int kTopkGroups = 4;   // block keys kept per thread slot (groups of chunks)
 constexpr int kTopkFcap = 2048;  // blocks read again in pass 2
 constexpr int kTopkDynBytes =
     int(sizeof(TopkDynSmem<kTopkThreads, kTopkVpt, kTopkGroups, kTopkFcap>));
+// Two builds: K <= 64 with clusters of up to 8 CTAs per row, and
+// 64 < K <= 256 with up to 2 (its exchange lists are 4x longer).
+constexpr int kTopkKmaxSmall = 64, kTopkClusterSmall = 8;
+constexpr int kTopkKmaxLarge = 256, kTopkClusterLarge = 2;
 
-template <bool PLAIN>
+template <int KMAX, int MAXC, bool PLAIN>
 static auto topk_kernel() {
-    return topk_rows_kernel<kTopkThreads, kTopkVpt, kTopkKmax, kTopkCap, kTopkGroups, kTopkFcap,
+    return topk_rows_kernel<kTopkThreads, kTopkVpt, KMAX, MAXC, kTopkCap, kTopkGroups, kTopkFcap,
                             PLAIN>;
 }
 
 os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
-    (void)K;
     const DeviceInfo* dev = device_info();
     if (!dev) return OS_ERR_CUDA;
-    const int per_sm = blocks_per_sm(topk_kernel<false>(), kTopkThreads, kTopkDynBytes);
+    const bool large = K > kTopkKmaxSmall;
+    const int per_sm = large
+        ? blocks_per_sm(topk_kernel<kTopkKmaxLarge, kTopkClusterLarge, false>(), kTopkThreads, kTopkDynBytes)
+        : blocks_per_sm(topk_kernel<kTopkKmaxSmall, kTopkClusterSmall, false>(), kTopkThreads, kTopkDynBytes);
     if (per_sm <= 0) return OS_ERR_CUDA;
     const int64_t resident = int64_t(dev->sms) * per_sm;
     const int64_t blocks = (cols + 3) / 4 + 1;  // upper bound over the 4 possible row offsets
     const int64_t chunks = ceil_div(blocks, int64_t(kTopkThreads) * kTopkVpt);
+    const int64_t max_cluster = large ? kTopkClusterLarge : kTopkClusterSmall;
     int64_t S = rows >= resident ? 1 : resident / rows;
-    if (S > kTopkMaxCluster) S = kTopkMaxCluster;
+    if (S > max_cluster) S = max_cluster;
     if (S > chunks) S = chunks;
     if (S < 1) S = 1;
     int64_t clusters = resident / S;
@@ -56,7 +63,11 @@ os_status plan_topk(int64_t rows, int64_t cols, int K, os_plan* p) {
 cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* idx,
                         int64_t rows, int cols, int K, bool plain, const KernelCtl& ctl,
                         cudaStream_t stream) {
-    auto k = plain ? topk_kernel<true>() : topk_kernel<false>();
+    const bool large = K > kTopkKmaxSmall;
+    auto k = large ? (plain ? topk_kernel<kTopkKmaxLarge, kTopkClusterLarge, true>()
+                            : topk_kernel<kTopkKmaxLarge, kTopkClusterLarge, false>())
+                   : (plain ? topk_kernel<kTopkKmaxSmall, kTopkClusterSmall, true>()
+                            : topk_kernel<kTopkKmaxSmall, kTopkClusterSmall, false>());
     if (!prepare_kernel(k, p.cluster, kTopkDynBytes)) return cudaErrorInvalidValue;
     return launch_kernel(k, p.grid, p.threads, p.cluster, kTopkDynBytes, stream, x, vals,
                          reinterpret_cast<int*>(idx), rows, cols, K, p.cluster, ctl);

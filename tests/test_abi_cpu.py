@@ -95,7 +95,7 @@ def test_softmax_without_device_fails_loudly(lib):
 def test_topk_argument_errors(lib, name):
     f = getattr(lib, name)
     assert f(A, B, C, 4, 100, 0, None) == KERR
-    assert f(A, B, C, 4, 100, 65, None) == KERR
+    assert f(A, B, C, 4, 1000, 257, None) == KERR
     assert f(A, B, C, 4, 5, 6, None) == KERR
     assert f(A, B, C, 4, 0, 1, None) == SHAPE
     assert f(A, B, C, -2, 100, 8, None) == SHAPE
@@ -129,6 +129,19 @@ def test_causal_argument_errors(lib):
     assert f(None, B, 4, 8, 4, 0, F32, F32, None) == NULL
     assert f(A, A, 4, 8, 4, 0, F32, F32, None) == ALIAS
     assert f(None, None, 0, 8, 4, 0, F32, F32, None) == OK
+
+
+def test_sample_argument_errors(lib):
+    f = lib.os_topk_sample
+    D = C + 65536
+    assert f(A, B, C, D, -1, 8, None) == SHAPE
+    assert f(A, B, C, D, 4, 0, None) == KERR
+    assert f(A, B, C, D, 4, 257, None) == KERR
+    assert f(None, B, C, D, 4, 8, None) == NULL
+    assert f(A, B, C, None, 4, 8, None) == NULL
+    assert f(A, B, C + 2, D, 4, 8, None) == ALIGN
+    assert f(A, B, C, A + 16, 4, 8, None) == ALIAS
+    assert f(None, None, None, None, 0, 8, None) == OK
 
 
 def test_exp_argument_errors(lib):

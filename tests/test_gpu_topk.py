@@ -40,7 +40,7 @@ COLS = [1, 2, 3, 5, 8, 63, 64, 65, 100, 1000, 4097, 8191, 8192, 8193, 16387, 327
 
 
 @pytest.mark.parametrize("cols", COLS)
-@pytest.mark.parametrize("K", [1, 2, 7, 8, 33, 64])
+@pytest.mark.parametrize("K", [1, 2, 7, 8, 33, 64, 65, 100, 256])
 def test_shapes(st, cols, K):
     if K > cols:
         pytest.skip("K > cols")
@@ -48,14 +48,14 @@ def test_shapes(st, cols, K):
     _run(st, _rand(rows, cols, seed=cols * 131 + K), K, f"cols={cols} K={K}")
 
 
-@pytest.mark.parametrize("K", [8, 64])
+@pytest.mark.parametrize("K", [8, 64, 256])
 def test_workload_full_size(st, K):
     w = workloads.WORKLOADS["topk_256x50257_f32"]
     x = workloads.make(w, device="cuda")
     _run(st, x, K, f"{w.name} K={K}")
 
 
-@pytest.mark.parametrize("K", [8, 64])
+@pytest.mark.parametrize("K", [8, 64, 200])
 def test_workload_with_planted_ties(st, K):
     w = workloads.WORKLOADS["topk_256x50257_f32"]
     x = workloads.plant_ties(workloads.make(w.scaled(rows=64), device="cuda"), per_row=K // 2 + 3)
@@ -67,7 +67,7 @@ def test_coarse_values_many_ties(st, cols):
     g = torch.Generator(device="cuda")
     g.manual_seed(cols)
     x = torch.randint(0, 4, (6, cols), generator=g, device="cuda").float()
-    for K in (1, 8, 64):
+    for K in (1, 8, 64, 256):
         if K <= cols:
             _run(st, x, K, f"values in 0..3, cols={cols} K={K}")
 
@@ -77,8 +77,9 @@ def test_constant_rows_overflow_path(st, cols):
     """Every entry ties: the threshold admits far more than the candidate
     buffer holds, so the kernel merges in several passes."""
     x = torch.full((3, cols), 2.5, device="cuda")
-    for K in (8, 64):
-        _run(st, x, K, f"constant cols={cols} K={K}")
+    for K in (8, 64, 256):
+        if K <= cols:
+            _run(st, x, K, f"constant cols={cols} K={K}")
 
 
 def test_fewer_finite_than_k(st):
@@ -88,12 +89,13 @@ def test_fewer_finite_than_k(st):
     x[2, 100:110] = torch.arange(10, dtype=torch.float32, device="cuda")
     x[3, 1] = 3.0
     _run(st, x, 64, "few finite entries")
+    _run(st, x, 256, "few finite entries, K = 256")
 
 
 def test_increasing_and_decreasing_rows(st):
     up = torch.arange(60000, dtype=torch.float32, device="cuda")[None, :] * 1e-3
     x = torch.cat([up, up.flip(1), -up]).contiguous()
-    for K in (8, 64):
+    for K in (8, 64, 256):
         _run(st, x, K, f"monotone K={K}")
 
 
@@ -128,7 +130,7 @@ def test_values_equal_softmax_output(st):
 def test_bad_k_raises(st):
     x = _rand(2, 100, seed=1)
     with pytest.raises(st.OsError) as e:
-        st.softmax_topk(x, 65)
+        st.softmax_topk(_rand(2, 1000, seed=1), 257)
     assert e.value.name == "OS_ERR_K"
     with pytest.raises(st.OsError):
         st.softmax_topk(_rand(2, 10, seed=1), 11)
@@ -148,7 +150,7 @@ def _run_plain(st, x, K, label):
 
 
 @pytest.mark.parametrize("cols", [1, 5, 64, 65, 1000, 8193, 50257, 300007])
-@pytest.mark.parametrize("K", [1, 8, 64])
+@pytest.mark.parametrize("K", [1, 8, 64, 256])
 def test_plain_topk_shapes(st, cols, K):
     if K > cols:
         pytest.skip("K > cols")
@@ -178,3 +180,35 @@ def test_unfused_pipeline_matches_fused(st, K):
     vals_f, _ = st.softmax_topk(x, K)
     rel = ((vals_u.double() - vals_f.double()).abs() / vals_f.double()).max()
     assert float(rel) <= 2e-5
+
+
+# ------------------------------------------------------------------ top-K sampling
+@pytest.mark.parametrize("K", [1, 8, 64, 256])
+def test_topk_sample_matches_oracle(st, K):
+    """Fused TopK, then one draw per row; the oracle draws from the same
+    (value, index) pairs and the same u, so the columns must agree exactly."""
+    w = workloads.WORKLOADS["topk_256x50257_f32"]
+    x = workloads.make(w, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(100 + K)
+    u = torch.rand(w.rows, generator=g, device="cuda")
+    samples, vals, idx = st.softmax_topk_sample(x, K, u)
+    torch.cuda.synchronize()
+    want = oracle.topk_sample(vals.double().cpu().numpy(), idx.cpu().numpy(),
+                              u.double().cpu().numpy())
+    assert np.array_equal(samples.cpu().numpy(), want)
+    assert np.all(np.any(idx.cpu().numpy() == samples.cpu().numpy()[:, None], axis=1))
+
+
+def test_topk_sample_frequencies(st):
+    rows, K = 4096, 4
+    vals = torch.tensor([[0.5, 0.25, 0.125, 0.125]], device="cuda").repeat(rows, 1)
+    idx = (torch.arange(K, dtype=torch.int32, device="cuda") + 3).repeat(rows, 1).contiguous()
+    u = ((torch.arange(rows, device="cuda", dtype=torch.float64) + 0.5) / rows).float()
+    out = st.topk_sample(vals, idx, u)
+    counts = torch.bincount(out.long() - 3, minlength=K)
+    assert counts.tolist() == [2048, 1024, 512, 512]
+    edge = st.topk_sample(torch.tensor([[0.0, 0.3, 0.7]] * 2, device="cuda"),
+                          torch.tensor([[5, 6, 7]] * 2, dtype=torch.int32, device="cuda"),
+                          torch.tensor([0.0, 1.0], device="cuda"))
+    assert edge.tolist() == [6, 7]

@@ -40,6 +40,10 @@ MUTANTS = {
                                "c >= (r % period) + offset ? -INFINITY"),
     "causal_mask_ignores_period": ("c > (r % period) + offset ? -INFINITY",
                                    "c > r + offset ? -INFINITY"),
+    "sample_ge_instead_of_gt": ("if (run > target) {", "if (run >= target) {"),
+    "sample_compares_single_value": ("run = run + (float)p[k];", "run = (float)p[k];"),
+    "sample_unnormalised_target": ("volatile float target = (float)u[r] * total;",
+                                   "volatile float target = (float)u[r];"),
 }
 
 

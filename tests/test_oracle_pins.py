@@ -266,11 +266,32 @@ def pin_causal_mask_rows(lib):
                 assert y[r, 0] == 1.0
 
 
+# ---------------------------------------------------------------- top-K sampling
+def pin_topk_sample_frequencies(lib):
+    """With u on a grid of N midpoints the draws split in proportion to the
+    values (dyadic values: exactly); zero-probability entries are never drawn,
+    also at u = 0; scaling all values changes nothing; u = 1 gives the last."""
+    N = 1024
+    u = (np.arange(N) + 0.5) / N
+    for p, want in (([0.5, 0.25, 0.125, 0.125], [512, 256, 128, 128]),
+                    ([1.0, 0.5, 0.25, 0.25], [512, 256, 128, 128]),
+                    ([0.5, 0.0, 0.5], [512, 0, 512]),
+                    ([0.75, 0.25], [768, 256])):
+        K = len(p)
+        vals = np.tile(np.array(p), (N, 1))
+        idx = np.tile(np.arange(K, dtype=np.int32) + 10, (N, 1))
+        got = oracle.topk_sample(vals, idx, u, lib)
+        assert list(np.bincount(got - 10, minlength=K)) == want, (p, np.bincount(got - 10))
+    vals = np.array([[0.0, 0.3, 0.7], [0.0, 0.3, 0.7], [0.2, 0.3, 0.5]])
+    idx = np.array([[5, 6, 7]] * 3, dtype=np.int32)
+    assert list(oracle.topk_sample(vals, idx, [0.0, 1.0, 0.2], lib)) == [6, 7, 6]
+
+
 PINS = [pin_two_shard_example, pin_identity_element, pin_combine_associative_commutative,
         pin_online_recurrence_equals_definition, pin_normalizer_bound, pin_lesson7_numpy_check,
         pin_closed_forms, pin_shift_invariance, pin_brute_force_tiny_rows, pin_rows_sum_to_one,
         pin_causal_and_spike_rows, pin_topk_exhaustive, pin_topk_ties_lower_index,
-        pin_lse_fsum_and_closed_forms, pin_causal_mask_rows]
+        pin_lse_fsum_and_closed_forms, pin_causal_mask_rows, pin_topk_sample_frequencies]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
