@@ -14,8 +14,9 @@ Functions and the passages they follow are listed in ``oracle.c``'s header:
 ``online_stats`` (the single-pass recurrence), ``combine`` (the binary
 operator on (m, d) with identity (-inf, 0)), ``topk`` (full sort by
 logit descending, index ascending; v = e^(u - m)/d), ``lse`` (m + ln d),
-``causal_mask`` / ``softmax_causal`` (the causal mask, then softmax) and
-``topk_sample`` (one draw per row from its top-K pairs).
+``causal_mask`` / ``softmax_causal`` (the causal mask, then softmax),
+``topk_sample`` (one draw per row from its top-K pairs) and ``attention``
+(softmax(scale Q K^T) V and the logsumexp of each query row).
 """
 from __future__ import annotations
 
@@ -72,6 +73,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                            ctypes.c_int64, ctypes.c_int64]
     lib.oracle_topk_sample_f64.argtypes = [_dbl_p, _i32_p, _dbl_p, _i32_p, ctypes.c_int64,
                                            ctypes.c_int32]
+    lib.oracle_attention_f64.argtypes = [_dbl_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_double,
+                                                                              ctypes.c_int]
     return lib
 
 
@@ -184,3 +187,32 @@ def topk_sample(vals, idx, u, lib: ctypes.CDLL | None = None) -> np.ndarray:
     (lib or _get()).oracle_topk_sample_f64(_p(v), _p(ix, _i32_p), _p(uu), _p(out, _i32_p),
                                            v.shape[0], v.shape[1])
     return out
+
+
+def _as_heads(x) -> np.ndarray:
+    """Widen a [bh, n, dh] array (or tensor) to C-contiguous float64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    if a.ndim == 2:
+        a = a[None]
+    if a.ndim != 3:
+        raise ValueError("attention inputs are [bh, n, dh] (or [n, dh])")
+    return a
+
+
+def attention(q, k, v, scale: float | None = None, causal: bool = False,
+              lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """float64 softmax(scale Q K^T) V per (batch, head) slice and the logsumexp
+    L = m + ln d of each query row; with ``causal`` query i sees keys j <= i.
+    ``scale`` defaults to 1/sqrt(dh).  Returns (O [bh, n, dh], L [bh, n])."""
+    a, b, c = _as_heads(q), _as_heads(k), _as_heads(v)
+    if a.shape != b.shape or a.shape != c.shape:
+        raise ValueError("q, k and v must have one shape [bh, n, dh]")
+    bh, n, dh = a.shape
+    s = 1.0 / np.sqrt(dh) if scale is None else float(scale)
+    o = np.empty_like(a)
+    lse_out = np.empty((bh, n))
+    (lib or _get()).oracle_attention_f64(_p(a), _p(b), _p(c), _p(o), _p(lse_out), bh, n, dh, s,
+                                         int(bool(causal)))
+    return o, lse_out

@@ -32,6 +32,8 @@
  *              then v = e^(u - m_V) / d_V).  Selection is a full sort of the
  *              row by (x descending, index ascending); the pages leave ties
  *              open and this build breaks them toward the lower index.
+ *   attention: softmax(scale Q K^T) V and L = m + ln d per query row, with
+ *              an optional causal mask (see oracle_attention_f64).
  *
  * Conventions: exp(-inf) = 0 from libm, so a -inf entry contributes nothing to
  * d and gets probability +0.  A row whose entries are all -inf has m = -inf and
@@ -208,4 +210,49 @@ int oracle_topk_f64(const double *x, double *vals, int32_t *idx,
         free(order);
     }
     return failed ? -1 : 0;
+}
+
+/* Attention forward by its definition, one query row at a time:
+ *   s_j = scale * (q_i . k_j)          for the keys j the query sees,
+ *   m   = max_j s_j,  d = sum_j e^(s_j - m),
+ *   o_i = sum_j (e^(s_j - m) / d) v_j,  L_i = m + ln d.
+ * Without the mask a query sees every key; with it, query i sees keys j <= i
+ * (equal query and key lengths).  This is softmax(scale Q K^T) V of the
+ * "Online normalizer calculation for softmax" notes, FlashAttention section
+ * (the attention definition and the (m, d, o) recurrence that reaches it),
+ * and the output O and logsumexp L of the "6.2 FlashAttention V2" forward
+ * algorithm (section 6.1), whose tiled recurrence telescopes to the same
+ * values in exact arithmetic; the definition is therefore the oracle.
+ * Layout: q, k, v, o are [bh][n][dh] row-major, lse is [bh][n]. */
+void oracle_attention_f64(const double *q, const double *k, const double *v, double *o,
+                          double *lse, int64_t bh, int64_t n, int64_t dh, double scale,
+                          int causal) {
+    #pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+        #pragma omp for schedule(static)
+        for (int64_t r = 0; r < bh * n; ++r) {
+            const int64_t b = r / n, i = r % n;
+            const double *qi = q + r * dh;
+            const double *kb = k + b * n * dh, *vb = v + b * n * dh;
+            const int64_t seen = causal ? i + 1 : n;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < seen; ++j) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < dh; ++c) acc += qi[c] * kb[j * dh + c];
+                s[j] = scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double d = 0.0;
+            for (int64_t j = 0; j < seen; ++j) d += exp(s[j] - m);
+            double *oi = o + r * dh;
+            for (int64_t c = 0; c < dh; ++c) oi[c] = 0.0;
+            for (int64_t j = 0; j < seen; ++j) {
+                const double p = exp(s[j] - m) / d;
+                for (int64_t c = 0; c < dh; ++c) oi[c] += p * vb[j * dh + c];
+            }
+            lse[r] = m + log(d);
+        }
+        free(s);
+    }
 }

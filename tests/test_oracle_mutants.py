@@ -44,6 +44,18 @@ MUTANTS = {
     "sample_compares_single_value": ("run = run + (float)p[k];", "run = (float)p[k];"),
     "sample_unnormalised_target": ("volatile float target = (float)u[r] * total;",
                                    "volatile float target = (float)u[r];"),
+    "attention_drops_scale": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "attention_mask_excludes_diagonal": ("const int64_t seen = causal ? i + 1 : n;",
+                                         "const int64_t seen = causal ? i : n;"),
+    "attention_mask_from_the_end": ("const int64_t seen = causal ? i + 1 : n;",
+                                    "const int64_t seen = causal ? n - i : n;"),
+    "attention_value_row_of_query": ("oi[c] += p * vb[j * dh + c];", "oi[c] += p * vb[i * dh + c];"),
+    "attention_key_row_of_query": ("acc += qi[c] * kb[j * dh + c];", "acc += qi[c] * kb[i * dh + c];"),
+    "attention_unnormalised": ("const double p = exp(s[j] - m) / d;",
+                               "const double p = exp(s[j] - m);"),
+    "attention_lse_drops_max": ("lse[r] = m + log(d);", "lse[r] = log(d);"),
+    "attention_max_not_subtracted_in_weights": ("d += exp(s[j] - m);\n            double *oi",
+                                                "d += exp(s[j]);\n            double *oi"),
 }
 
 

@@ -17,6 +17,9 @@ Sources of the facts (pages named by title and section):
     invariant under adding a constant to every entry.
   * Closed forms: one entry -> 1; constant row -> 1/n; two entries -> the
     logistic function of their difference; y_i = 1 / sum_j e^(x_j - x_i).
+  * "6.2 FlashAttention V2", section 6.1: the tiled forward loop (running max,
+    running sum, rescaled output, final division, L = m + ln l) reaches the
+    attention oracle's O and L; attention closed forms and invariants.
 """
 import itertools
 import math
@@ -287,11 +290,134 @@ def pin_topk_sample_frequencies(lib):
     assert list(oracle.topk_sample(vals, idx, [0.0, 1.0, 0.2], lib)) == [6, 7, 6]
 
 
+# ---------------------------------------------------------------- attention
+def _tiled_attention(q, k, v, scale, causal, Br, Bc):
+    """The forward loop of "6.2 FlashAttention V2" (section 6.1) in plain
+    Python: query tiles of Br rows, key/value tiles of Bc rows, running row
+    maximum m, running sum l and unnormalised output, the masked key range
+    ending at the query tile's end, and O = O~ / l, L = m + ln l at the end."""
+    n, dh = len(q), len(q[0])
+    O = [[0.0] * dh for _ in range(n)]
+    L = [0.0] * n
+    for i0 in range(0, n, Br):
+        rows = range(i0, min(n, i0 + Br))
+        m = {r: -math.inf for r in rows}
+        l = {r: 0.0 for r in rows}
+        acc = {r: [0.0] * dh for r in rows}
+        kv_end = min(n, i0 + Br) if causal else n
+        for j0 in range(0, kv_end, Bc):
+            cols = range(j0, min(kv_end, j0 + Bc))
+            for r in rows:
+                s = [scale * sum(q[r][c] * k[j][c] for c in range(dh)) for j in cols]
+                s = [-math.inf if causal and j > r else sj for sj, j in zip(s, cols)]
+                m_new = max([m[r]] + s)
+                p = [math.exp(sj - m_new) for sj in s]
+                corr = math.exp(m[r] - m_new)
+                l[r] = corr * l[r] + sum(p)
+                acc[r] = [corr * a + sum(pj * v[j][c] for pj, j in zip(p, cols))
+                          for c, a in enumerate(acc[r])]
+                m[r] = m_new
+        for r in rows:
+            O[r] = [a / l[r] for a in acc[r]]
+            L[r] = m[r] + math.log(l[r])
+    return O, L
+
+
+def pin_attention_tiled_recurrence(lib):
+    """The oracle's attention equals the FlashAttention-2 tiled forward loop,
+    run in plain Python on tiny heads with ragged tiles, with and without the
+    causal mask, for the default 1/sqrt(dh) scale and another one."""
+    rng = np.random.default_rng(31)
+    for n, dh, Br, Bc in ((7, 3, 3, 2), (5, 4, 2, 3), (1, 2, 1, 1), (9, 2, 4, 4)):
+        q, k, v = (rng.normal(size=(2, n, dh)) * 2 for _ in range(3))
+        for causal in (False, True):
+            for scale in (None, 0.7):
+                o, L = oracle.attention(q, k, v, scale, causal, lib=lib)
+                sc = 1.0 / math.sqrt(dh) if scale is None else scale
+                for b in range(2):
+                    O_ref, L_ref = _tiled_attention(q[b].tolist(), k[b].tolist(), v[b].tolist(),
+                                                    sc, causal, Br, Bc)
+                    assert np.allclose(o[b], O_ref, rtol=1e-12, atol=1e-12), (n, dh, causal)
+                    assert np.allclose(L[b], L_ref, rtol=1e-12, atol=1e-12), (n, dh, causal)
+
+
+def pin_attention_closed_forms(lib):
+    """One key: O = v_0 and L = scale q.k_0.  Equal keys: uniform weights over
+    the keys a query sees, so O_i is the mean of those v_j (all of them, or
+    j <= i under the mask) and L_i = s + ln(count).  A key that scores 200
+    above the rest: O equals its value row to rounding."""
+    rng = np.random.default_rng(32)
+    q, k, v = (rng.normal(size=(3, 1, 5)) for _ in range(3))
+    o, L = oracle.attention(q, k, v, 0.5, lib=lib)
+    assert np.allclose(o, v, rtol=0, atol=1e-15)
+    assert np.allclose(L[:, 0], 0.5 * np.einsum("bd,bd->b", q[:, 0], k[:, 0]), rtol=1e-14)
+    n, dh = 6, 4
+    q = rng.normal(size=(1, n, dh))
+    k = np.tile(rng.normal(size=(1, 1, dh)), (1, n, 1))
+    v = rng.normal(size=(1, n, dh))
+    for causal in (False, True):
+        o, L = oracle.attention(q, k, v, 1.5, causal, lib=lib)
+        for i in range(n):
+            cnt = i + 1 if causal else n
+            s = 1.5 * float(q[0, i] @ k[0, 0])
+            assert np.allclose(o[0, i], v[0, :cnt].mean(0), rtol=1e-13, atol=1e-14), (causal, i)
+            assert abs(L[0, i] - (s + math.log(cnt))) <= 1e-13 * max(1.0, abs(s)), (causal, i)
+    q = np.zeros((1, 4, 2))
+    q[0, :, 0] = 1.0
+    k = np.zeros((1, 4, 2))
+    k[0, 2, 0] = 200.0  # scores 0, 0, 200, 0 for every query
+    v = rng.normal(size=(1, 4, 2))
+    o, _ = oracle.attention(q, k, v, 1.0, lib=lib)
+    assert np.allclose(o[0], np.tile(v[0, 2], (4, 1)), rtol=0, atol=1e-15)
+
+
+def pin_attention_softmax_times_v(lib):
+    """O = softmax(scale Q K^T) V with the oracle's own pinned softmax applied
+    to scores from a numpy matmul, and the mask applied by the pinned causal
+    mask (period n); L from the pinned log-sum-exp."""
+    rng = np.random.default_rng(33)
+    for bh, n, dh in ((3, 17, 8), (1, 40, 16)):
+        q, k, v = (rng.normal(size=(bh, n, dh)) for _ in range(3))
+        for causal in (False, True):
+            o, L = oracle.attention(q, k, v, None, causal, lib=lib)
+            for b in range(bh):
+                s = (q[b] @ k[b].T) / math.sqrt(dh)
+                if causal:
+                    s = oracle.causal_mask(s, n, 0, lib)
+                p = oracle.softmax(s, lib)
+                assert np.allclose(o[b], p @ v[b], rtol=1e-12, atol=1e-13), (b, causal)
+                assert np.allclose(L[b], oracle.lse(s, lib), rtol=1e-13, atol=1e-13), (b, causal)
+
+
+def pin_attention_invariants(lib):
+    """Weights sum to 1, so adding c to every value row adds c to O; without the
+    mask, permuting keys and values together leaves O and L alone; scaling
+    values scales O; and under the mask row i depends only on keys j <= i."""
+    rng = np.random.default_rng(34)
+    bh, n, dh = 2, 11, 6
+    q, k, v = (rng.normal(size=(bh, n, dh)) * 1.5 for _ in range(3))
+    o, L = oracle.attention(q, k, v, lib=lib)
+    c = rng.normal(size=dh)
+    assert np.allclose(oracle.attention(q, k, v + c, lib=lib)[0], o + c, rtol=1e-12, atol=1e-12)
+    assert np.allclose(oracle.attention(q, k, 3 * v, lib=lib)[0], 3 * o, rtol=1e-12, atol=1e-12)
+    perm = rng.permutation(n)
+    o2, L2 = oracle.attention(q, k[:, perm], v[:, perm], lib=lib)
+    assert np.allclose(o2, o, rtol=1e-12, atol=1e-12) and np.allclose(L2, L, rtol=1e-13)
+    oc, Lc = oracle.attention(q, k, v, causal=True, lib=lib)
+    for i in (0, 4, n - 1):
+        oi, Li = oracle.attention(q[:, : i + 1], k[:, : i + 1], v[:, : i + 1], lib=lib)
+        assert np.allclose(oc[:, i], oi[:, i], rtol=1e-12, atol=1e-12), i
+        assert np.allclose(Lc[:, i], Li[:, i], rtol=1e-13, atol=1e-13), i
+    assert np.allclose(oc[:, n - 1], o[:, n - 1], rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_two_shard_example, pin_identity_element, pin_combine_associative_commutative,
         pin_online_recurrence_equals_definition, pin_normalizer_bound, pin_lesson7_numpy_check,
         pin_closed_forms, pin_shift_invariance, pin_brute_force_tiny_rows, pin_rows_sum_to_one,
         pin_causal_and_spike_rows, pin_topk_exhaustive, pin_topk_ties_lower_index,
-        pin_lse_fsum_and_closed_forms, pin_causal_mask_rows, pin_topk_sample_frequencies]
+        pin_lse_fsum_and_closed_forms, pin_causal_mask_rows, pin_topk_sample_frequencies,
+        pin_attention_tiled_recurrence, pin_attention_closed_forms, pin_attention_softmax_times_v,
+        pin_attention_invariants]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

@@ -16,6 +16,12 @@ Workloads (rows x cols, dtype, distribution, seed):
   increasing_65536x4096_f32   65536 x 4096 fp32, each row sorted N(0, 1)
                               draws made strictly increasing,                seed 1006
 
+Attention (batch x heads x seq_len x head_dim, Q, K, V bf16, all N(0, 1)):
+
+  attention_4x16x4096x128_bf16  64 (batch, head) slices of 4096 x 128,       seed 1007
+                                with and without the causal mask
+  attention_1x2x300x64_bf16     small case for the oracle (ragged tile),     seed 1008
+
 Readings of the workload text (each is listed with its reason in the design doc):
   * "N(0, s)": s is the standard deviation, x = s * randn.
   * "4 spikes at +40 at random positions": row r gets one spike in each quarter
@@ -138,3 +144,39 @@ def plant_ties(x: torch.Tensor, g_seed: int = 7, per_row: int = 6) -> torch.Tens
     top = x.max(dim=1, keepdim=True).values.expand(rows, per_row)
     x.scatter_(1, pos, top.contiguous())
     return x
+
+
+@dataclass(frozen=True)
+class AttentionWorkload:
+    name: str
+    batch: int
+    heads: int
+    seq_len: int
+    head_dim: int
+    seed: int = 0
+
+    @property
+    def bh(self) -> int:
+        return self.batch * self.heads
+
+    def scaled(self, batch: int | None = None, heads: int | None = None,
+               seq_len: int | None = None) -> "AttentionWorkload":
+        return replace(self, batch=batch or self.batch, heads=heads or self.heads,
+                       seq_len=seq_len or self.seq_len)
+
+
+ATTENTION_WORKLOADS = {
+    w.name: w for w in [
+        AttentionWorkload("attention_4x16x4096x128_bf16", 4, 16, 4096, 128, 1007),
+        AttentionWorkload("attention_1x2x300x64_bf16", 1, 2, 300, 64, 1008),
+    ]
+}
+
+
+def make_attention(w: AttentionWorkload, device="cpu", seed: int | None = None):
+    """Draw (Q, K, V), each [batch * heads, seq_len, head_dim] bf16 N(0, 1)."""
+    device = torch.device(device)
+    g = _generator(device, w.seed if seed is None else seed)
+    shape = (w.bh, w.seq_len, w.head_dim)
+    return tuple(torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+                 for _ in range(3))
