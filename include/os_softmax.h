@@ -59,7 +59,8 @@ typedef enum {
     OS_ERR_CUDA = 6,    /* the CUDA runtime reported an error (launch or device query) */
     OS_ERR_TIMEOUT = 7, /* a device-side bounded wait gave up (os_device_status) */
     OS_ERR_PATH = 8,    /* the requested kernel family cannot run this shape */
-    OS_ERR_ALIGN = 9    /* a pointer is not aligned to its element size */
+    OS_ERR_ALIGN = 9,   /* a pointer is not aligned to its element size */
+    OS_ERR_VALUE = 10   /* a scalar argument outside its range (attention scale, causal flag) */
 } os_status;
 
 /* Kernel families (see os_softmax_fwd_path). */
@@ -180,6 +181,31 @@ os_status os_topk_sample(const float *vals, const int32_t *idx, const float *u, 
                          int64_t rows, int32_t K, os_stream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
+/* Attention forward on the tensor cores ("6.2 FlashAttention V2", section 6.1,
+ * forward algorithm; the (m, d, o) recurrence of the "Online normalizer
+ * calculation for softmax" notes, FlashAttention section):
+ *   O[s, i, :] = sum_j softmax_j(scale * q_i . k_j) v_j,
+ *   L[s, i]    = ln sum_j e^(scale * q_i . k_j)  (the logsumexp kept for a backward pass),
+ * over the keys j that query i sees: all n of them, or j <= i when `causal`
+ * is 1.  s runs over the bh (batch x head) slices.
+ *   q, k, v    [bh][n][head_dim] bf16, row-major, 16-byte aligned (OS_ERR_ALIGN).
+ *   o          [bh][n][head_dim] bf16 output, 16-byte aligned; must not overlap
+ *              q, k or v (OS_ERR_ALIAS).
+ *   lse        [bh][n] fp32 output, 4-byte aligned, or NULL (not written); must
+ *              not overlap any other argument (OS_ERR_ALIAS).
+ *   bh >= 0 and n >= 0 (either 0: no-op); n <= 2^31 - 1 and bh * ceil(n/128)
+ *   <= 2^31 - 1; head_dim 64 or 128 (OS_ERR_SHAPE otherwise).
+ *   scale      finite and > 0, usually 1/sqrt(head_dim) (OS_ERR_VALUE).
+ *   causal     0 or 1 (OS_ERR_VALUE).
+ * Arithmetic: scores Q K^T in fp32 on the tensor cores from bf16 operands;
+ * probabilities e^(scale s - m) in fp32, summed into l in fp32 and rounded to
+ * bf16 for the P V product (fp32 accumulation); O = (P V) / l rounded to bf16;
+ * L = m + ln l in fp32.  The buffers are the caller's; the
+ * library allocates nothing. */
+os_status os_attention_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t bh, int64_t n, int32_t head_dim, float scale, int32_t causal,
+                           os_stream_t stream);
+
 const char *os_status_string(os_status status);
 
 /*

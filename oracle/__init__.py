@@ -36,6 +36,7 @@ _lib = None
 
 _dbl_p = ctypes.POINTER(ctypes.c_double)
 _i32_p = ctypes.POINTER(ctypes.c_int32)
+_i64_p = ctypes.POINTER(ctypes.c_int64)
 
 
 def compile_oracle(src: str = _SRC, out: str = _LIB_PATH, defines: tuple = ()) -> str:
@@ -75,6 +76,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                            ctypes.c_int32]
     lib.oracle_attention_f64.argtypes = [_dbl_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_double,
                                                                               ctypes.c_int]
+    lib.oracle_attention_rows_f64.argtypes = [_dbl_p] * 3 + [_i64_p, _i64_p] + \
+        [ctypes.c_int64] * 3 + [ctypes.c_double, ctypes.c_int, _dbl_p, _dbl_p]
     return lib
 
 
@@ -215,4 +218,29 @@ def attention(q, k, v, scale: float | None = None, causal: bool = False,
     lse_out = np.empty((bh, n))
     (lib or _get()).oracle_attention_f64(_p(a), _p(b), _p(c), _p(o), _p(lse_out), bh, n, dh, s,
                                          int(bool(causal)))
+    return o, lse_out
+
+
+def attention_rows(q_rows, k, v, slices, rows, scale: float | None = None, causal: bool = False,
+                   lib: ctypes.CDLL | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """The attention oracle for selected query rows only: ``q_rows`` [p, dh] holds
+    query ``rows[p]`` of slice ``slices[p]``; k, v are the full [bh, n, dh].
+    Returns (O [p, dh], L [p])."""
+    b, c = _as_heads(k), _as_heads(v)
+    if b.shape != c.shape:
+        raise ValueError("k and v must have one shape [bh, n, dh]")
+    bh, n, dh = b.shape
+    a = _as_heads(q_rows).reshape(-1, dh)
+    sl = np.ascontiguousarray(np.asarray(slices, dtype=np.int64).ravel())
+    rw = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).ravel())
+    if not (len(sl) == len(rw) == a.shape[0]):
+        raise ValueError("one (slice, row) pair per query row")
+    if len(sl) and (sl.min() < 0 or sl.max() >= bh or rw.min() < 0 or rw.max() >= n):
+        raise ValueError("(slice, row) pair out of range")
+    s = 1.0 / np.sqrt(dh) if scale is None else float(scale)
+    o = np.empty((len(sl), dh))
+    lse_out = np.empty(len(sl))
+    (lib or _get()).oracle_attention_rows_f64(_p(a), _p(b), _p(c), _p(sl, _i64_p), _p(rw, _i64_p),
+                                              len(sl), n, dh, s, int(bool(causal)), _p(o),
+                                              _p(lse_out))
     return o, lse_out

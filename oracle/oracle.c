@@ -224,6 +224,27 @@ int oracle_topk_f64(const double *x, double *vals, int32_t *idx,
  * algorithm (section 6.1), whose tiled recurrence telescopes to the same
  * values in exact arithmetic; the definition is therefore the oracle.
  * Layout: q, k, v, o are [bh][n][dh] row-major, lse is [bh][n]. */
+static void attend_row(const double *qi, const double *kb, const double *vb, int64_t i, int64_t n,
+                       int64_t dh, double scale, int causal, double *s, double *oi,
+                       double *lse_out) {
+    const int64_t seen = causal ? i + 1 : n;
+    double m = -INFINITY;  /* the maximum of the scores seen */
+    for (int64_t j = 0; j < seen; ++j) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < dh; ++c) acc += qi[c] * kb[j * dh + c];
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double d = 0.0;
+    for (int64_t j = 0; j < seen; ++j) d += exp(s[j] - m);
+    for (int64_t c = 0; c < dh; ++c) oi[c] = 0.0;
+    for (int64_t j = 0; j < seen; ++j) {
+        const double p = exp(s[j] - m) / d;
+        for (int64_t c = 0; c < dh; ++c) oi[c] += p * vb[j * dh + c];
+    }
+    *lse_out = m + log(d);
+}
+
 void oracle_attention_f64(const double *q, const double *k, const double *v, double *o,
                           double *lse, int64_t bh, int64_t n, int64_t dh, double scale,
                           int causal) {
@@ -233,26 +254,27 @@ void oracle_attention_f64(const double *q, const double *k, const double *v, dou
         #pragma omp for schedule(static)
         for (int64_t r = 0; r < bh * n; ++r) {
             const int64_t b = r / n, i = r % n;
-            const double *qi = q + r * dh;
-            const double *kb = k + b * n * dh, *vb = v + b * n * dh;
-            const int64_t seen = causal ? i + 1 : n;
-            double m = -INFINITY;
-            for (int64_t j = 0; j < seen; ++j) {
-                double acc = 0.0;
-                for (int64_t c = 0; c < dh; ++c) acc += qi[c] * kb[j * dh + c];
-                s[j] = scale * acc;
-                if (s[j] > m) m = s[j];
-            }
-            double d = 0.0;
-            for (int64_t j = 0; j < seen; ++j) d += exp(s[j] - m);
-            double *oi = o + r * dh;
-            for (int64_t c = 0; c < dh; ++c) oi[c] = 0.0;
-            for (int64_t j = 0; j < seen; ++j) {
-                const double p = exp(s[j] - m) / d;
-                for (int64_t c = 0; c < dh; ++c) oi[c] += p * vb[j * dh + c];
-            }
-            lse[r] = m + log(d);
+            attend_row(q + r * dh, k + b * n * dh, v + b * n * dh, i, n, dh, scale, causal, s,
+                       o + r * dh, lse + r);
         }
+        free(s);
+    }
+}
+
+/* The same rows for a list of (slice, query) pairs only: row p of the output
+ * is query row[p] of slice slice[p]; q holds just those query rows
+ * ([npairs][dh]), k and v the full [bh][n][dh] tensors. */
+void oracle_attention_rows_f64(const double *q, const double *k, const double *v,
+                               const int64_t *slice, const int64_t *row, int64_t npairs,
+                               int64_t n, int64_t dh, double scale, int causal, double *o,
+                               double *lse) {
+    #pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+        #pragma omp for schedule(dynamic)
+        for (int64_t p = 0; p < npairs; ++p)
+            attend_row(q + p * dh, k + slice[p] * n * dh, v + slice[p] * n * dh, row[p], n, dh,
+                       scale, causal, s, o + p * dh, lse + p);
         free(s);
     }
 }

@@ -2,13 +2,14 @@
 
 The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
 ``os_softmax_fwd``, ``os_softmax_topk``, ``os_topk``, ``os_softmax_causal_fwd``,
-``os_softmax_stats``, ``os_topk_sample``, ``os_softmax_fwd_path``,
+``os_softmax_stats``, ``os_topk_sample``, ``os_attention_fwd``, ``os_softmax_fwd_path``,
 ``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_device_status``,
 ``os_set_wait_timeout_ns``, ``os_set_fault_injection``, ``os_status_string``.  They take raw
 device pointers (ints) and a raw stream handle, exactly like the C functions,
 and raise ``OsError`` on a non-OK status.
 
-``softmax``, ``softmax_topk``, ``topk``, ``softmax_causal`` and ``softmax_stats`` are the
+``softmax``, ``softmax_topk``, ``topk``, ``softmax_causal``, ``softmax_stats`` and
+``attention`` are the
 tensor-level conveniences: they take
 torch CUDA tensors, allocate outputs with torch, pass the current torch
 stream, and call the same C entry points.  PyTorch only provides memory and
@@ -29,7 +30,7 @@ OS_PATH_AUTO, OS_PATH_WARP, OS_PATH_ONCHIP, OS_PATH_STREAM, OS_PATH_SAFE = 0, 1,
 PATHS = {"auto": OS_PATH_AUTO, "warp": OS_PATH_WARP, "onchip": OS_PATH_ONCHIP,
          "stream": OS_PATH_STREAM, "safe": OS_PATH_SAFE}
 STATUS = ["OS_OK", "OS_ERR_NULL", "OS_ERR_SHAPE", "OS_ERR_DTYPE", "OS_ERR_K", "OS_ERR_ALIAS",
-          "OS_ERR_CUDA", "OS_ERR_TIMEOUT", "OS_ERR_PATH", "OS_ERR_ALIGN"]
+          "OS_ERR_CUDA", "OS_ERR_TIMEOUT", "OS_ERR_PATH", "OS_ERR_ALIGN", "OS_ERR_VALUE"]
 KMAX = 256
 
 
@@ -67,6 +68,7 @@ def _load() -> ctypes.CDLL:
     lib.os_softmax_causal_fwd.argtypes = [vp, vp, i64, i64, i64, i64, st, st, vp]
     lib.os_softmax_stats.argtypes = [vp, vp, vp, vp, i64, i64, st, vp]
     lib.os_topk_sample.argtypes = [vp, vp, vp, vp, i64, i32, vp]
+    lib.os_attention_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, ctypes.c_float, i32, vp]
     lib.os_softmax_plan.argtypes = [i64, i64, st, st, st, ctypes.POINTER(Plan)]
     lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
     lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
@@ -76,7 +78,8 @@ def _load() -> ctypes.CDLL:
     lib.os_status_string.argtypes = [st]
     lib.os_status_string.restype = ctypes.c_char_p
     for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_topk",
-                 "os_softmax_causal_fwd", "os_softmax_stats", "os_topk_sample", "os_softmax_plan",
+                 "os_softmax_causal_fwd", "os_softmax_stats", "os_topk_sample", "os_attention_fwd",
+                 "os_softmax_plan",
                  "os_topk_plan", "os_exp_f32", "os_device_status", "os_set_wait_timeout_ns",
                  "os_set_fault_injection"):
         getattr(lib, name).restype = st
@@ -131,6 +134,12 @@ def os_softmax_stats(x: int, m: int | None, d: int | None, lse: int | None, rows
 def os_topk_sample(vals: int, idx: int, u: int, out: int, rows: int, K: int,
                    stream: int | None) -> None:
     _check(_lib.os_topk_sample(vals, idx, u, out, rows, K, stream), "os_topk_sample")
+
+
+def os_attention_fwd(q: int, k: int, v: int, o: int, lse: int | None, bh: int, n: int,
+                     head_dim: int, scale: float, causal: int, stream: int | None) -> None:
+    _check(_lib.os_attention_fwd(q, k, v, o, lse, bh, n, head_dim, scale, causal, stream),
+           "os_attention_fwd")
 
 
 def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
@@ -292,6 +301,32 @@ def softmax_topk_sample(x, K: int, u):
     """Fused softmax + TopK, then one draw per row: (samples, vals, idx)."""
     vals, idx = softmax_topk(x, K)
     return topk_sample(vals, idx, u), vals, idx
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+              want_lse: bool = True):
+    """Attention forward on the tensor cores: (O, L) for bf16 CUDA tensors q, k, v
+    of one shape [..., n, head_dim] (leading dims are the batch x head slices),
+    head_dim 64 or 128.  O has q's shape (bf16); L is fp32 [..., n], or None
+    when ``want_lse`` is false.  ``scale`` defaults to 1/sqrt(head_dim)."""
+    import torch
+    for t_ in (q, k, v):
+        if not t_.is_cuda or t_.dtype != torch.bfloat16 or not t_.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() < 2:
+        raise ValueError("q, k, v must share one shape [..., n, head_dim]")
+    n, hd = q.shape[-2], q.shape[-1]
+    bh = q.numel() // max(n * hd, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    s = (1.0 / hd ** 0.5) if scale is None else float(scale)
+    with _OnDevice(q.device):
+        os_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, bh, n, hd, s, int(causal),
+                         _stream_handle(q))
+    return out, lse
 
 
 def exp(z):

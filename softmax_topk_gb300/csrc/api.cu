@@ -130,7 +130,7 @@ const char* os_status_string(os_status s) {
     switch (s) {
         case OS_OK: return "OS_OK";
         case OS_ERR_NULL: return "OS_ERR_NULL: a required pointer is NULL";
-        case OS_ERR_SHAPE: return "OS_ERR_SHAPE: rows < 0 or cols outside [1, 2^31-1]";
+        case OS_ERR_SHAPE: return "OS_ERR_SHAPE: a size or head dimension outside its range";
         case OS_ERR_DTYPE: return "OS_ERR_DTYPE: unknown dtype";
         case OS_ERR_K: return "OS_ERR_K: K outside [1, min(cols, 256)]";
         case OS_ERR_ALIAS: return "OS_ERR_ALIAS: an output overlaps an input or another output";
@@ -138,6 +138,7 @@ const char* os_status_string(os_status s) {
         case OS_ERR_TIMEOUT: return "OS_ERR_TIMEOUT: a device-side bounded wait gave up";
         case OS_ERR_PATH: return "OS_ERR_PATH: the kernel family cannot run this shape";
         case OS_ERR_ALIGN: return "OS_ERR_ALIGN: pointer not aligned to its element size";
+        case OS_ERR_VALUE: return "OS_ERR_VALUE: a scalar argument outside its range";
     }
     return "unknown os_status";
 }
@@ -245,6 +246,34 @@ os_status os_topk_sample(const float* vals, const int32_t* idx, const float* u, 
         return OS_ERR_ALIAS;
     const cudaError_t e = os::launch_topk_sample(vals, idx, u, out, rows, K,
                                                  reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
+}
+
+os_status os_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t bh, int64_t n, int32_t head_dim, float scale, int32_t causal,
+                           os_stream_t stream) {
+    if (bh < 0 || n < 0 || n > INT32_MAX || (head_dim != 64 && head_dim != 128))
+        return OS_ERR_SHAPE;
+    if (!(scale > 0.f) || !(scale < INFINITY) || (causal != 0 && causal != 1)) return OS_ERR_VALUE;
+    if (bh == 0 || n == 0) return OS_OK;
+    const int64_t nq = (n + 127) / 128;
+    if (bh > INT32_MAX / nq || bh > INT64_MAX / 2 / head_dim / n) return OS_ERR_SHAPE;
+    if (!q || !k || !v || !o) return OS_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(k) % 16 ||
+        reinterpret_cast<uintptr_t>(v) % 16 || reinterpret_cast<uintptr_t>(o) % 16 ||
+        reinterpret_cast<uintptr_t>(lse) % 4)
+        return OS_ERR_ALIGN;
+    const int64_t tb = bh * n * head_dim * 2, lb = bh * n * 4;
+    if (overlaps(o, tb, q, tb) || overlaps(o, tb, k, tb) || overlaps(o, tb, v, tb))
+        return OS_ERR_ALIAS;
+    if (lse && (overlaps(lse, lb, q, tb) || overlaps(lse, lb, k, tb) || overlaps(lse, lb, v, tb) ||
+                overlaps(lse, lb, o, tb)))
+        return OS_ERR_ALIAS;
+    os::KernelCtl ctl;
+    if (!make_ctl(&ctl)) return OS_ERR_CUDA;
+    const cudaError_t e = os::launch_attention(q, k, v, o, lse, bh, static_cast<int>(n), head_dim,
+                                               scale, causal != 0, ctl,
+                                               reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
 }
 

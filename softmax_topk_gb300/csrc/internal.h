@@ -35,6 +35,12 @@ cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t strea
 cudaError_t launch_topk_sample(const float* vals, const int32_t* idx, const float* u, int32_t* out,
                                int64_t rows, int K, cudaStream_t stream);
 
+// attention forward over bh slices of [n][d] bf16 (d = 64 or 128): o bf16,
+// lse fp32 (may be NULL); scale > 0
+cudaError_t launch_attention(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int64_t bh, int n, int d, float scale, bool causal,
+                             const KernelCtl& ctl, cudaStream_t stream);
+
 // (m, d, lse) of every row; any output may be NULL
 cudaError_t launch_stats(const void* x, os_dtype in, float* m, float* d, float* lse, int64_t rows,
                          int cols, bool aligned, cudaStream_t stream);

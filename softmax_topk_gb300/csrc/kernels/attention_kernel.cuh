@@ -1,0 +1,326 @@
+// attention_kernel.cuh -- attention forward, O = softmax(scale Q K^T) V with the
+// per-row logsumexp, on the fifth-generation tensor cores.
+//
+// What it computes follows "6.2 FlashAttention V2" (section 6.1, forward
+// algorithm): a CTA owns one tile of 128 query rows of one (batch, head) and
+// walks the key/value tiles of 128 rows, keeping per query row the running
+// maximum m, the running sum l and the unnormalised output; at the end it
+// writes O = O~ / l and L = m + ln l.  The recurrence is the (m, d, o) one of
+// the "Online normalizer calculation for softmax" notes (FlashAttention
+// section): o is rescaled by e^(m_old - m_new) whenever the maximum moves.
+// With the causal mask, query i sees keys j <= i and the key walk stops at the
+// diagonal tile (section 5 of the same page).
+//
+// GB300 mapping (one CTA per query tile, 192 threads, warp-specialised):
+//   * warp 4 (one lane) streams the Q tile once and the K/V tiles through a
+//     two-stage ring with TMA tiled loads (128-byte swizzle, rows past the
+//     sequence end zero-filled by the copy engine);
+//   * warp 5 (one lane) issues tcgen05.mma: S_j = Q K_j^T into one of two
+//     128-column fp32 accumulators in tensor memory, then O += P_j V_j into a
+//     D-column accumulator that stays in tensor memory for the whole walk;
+//   * warps 0-3 (the softmax warps) own one query row per thread, which is one
+//     tensor-memory lane: they read S_j with tcgen05.ld, mask, update (m, l),
+//     write P_j = 2^(S_j scale log2e - m) as bf16 into shared memory in the
+//     layout the next MMA reads, and at the end normalise O.
+// S_{j+1} is computed while the softmax warps work on S_j, and P_j V_j runs
+// while they work on S_{j+1}.
+//
+// Rescaling differs from the pages' every-tile form: the exponent base m is
+// only moved when a tile's maximum exceeds it by more than 2^8 (in the base-2
+// exponent), so P stays <= 256 and the tensor-memory O is read and rewritten
+// only on those (rare) tiles.  l and O always share one base, so O / l is the
+// same quotient in exact arithmetic.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "../ctl.h"
+#include "ops.cuh"
+#include "umma.cuh"
+
+namespace os {
+namespace attn {
+
+constexpr int kBM = 128;  // query rows per CTA (one per tensor-memory lane)
+constexpr int kBN = 128;  // keys per tile
+constexpr int kSoftmaxWarps = 4;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS1 = 128;         // S accumulators at columns 0 and 128
+constexpr uint32_t kTmemO = 256;          // O accumulator, D columns
+constexpr float kRescaleLog2 = 8.0f;      // move the base when the max grows by more than 2^8
+constexpr float kLn2 = 0.693147182f;
+
+// Dynamic shared memory, 1024-byte aligned regions (the 128-byte swizzle
+// repeats every 1024 bytes).  A Q/K/V tile is D/64 blocks of [128 rows][64
+// bf16]; P is 2 blocks of [128 query rows][64 keys].
+template <int D>
+struct Layout {
+    static constexpr int kBlock = kBM * 64 * 2;  // 16 KB
+    static constexpr int kTile = kBM * D * 2;
+    static constexpr int kPTile = kBM * kBN * 2;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTile;       // 2 stages
+    static constexpr int kV = kK + 2 * kTile;   // 2 stages
+    static constexpr int kP = kV + 2 * kTile;   // 2 buffers
+    static constexpr int kBytes = kP + 2 * kPTile;
+    static constexpr int kDynBytes = kBytes + 1024;
+};
+
+struct Barriers {
+    uint64_t q_full;
+    uint64_t k_full[2], v_full[2];    // TMA landed (transaction bytes)
+    uint64_t k_empty[2], v_empty[2];  // the MMAs reading the stage completed
+    uint64_t s_full[2];               // S_j in tensor memory
+    uint64_t p_full[2];               // P_j in shared memory (128 arrivals)
+    uint64_t pv_done[2];              // P_j V_j accumulated into O
+    uint32_t tmem;
+};
+
+// The query tile and (batch, head) slice of CTA `b`: slices in order, so CTAs
+// that run together share their K/V tiles in L2; with the mask the longest
+// tiles of a slice come first.
+__device__ __forceinline__ void work_item(int64_t b, int nq, bool causal, int& bh, int& qi) {
+    bh = int(b / nq);
+    const int r = int(b % nq);
+    qi = causal ? nq - 1 - r : r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
+                     const __grid_constant__ CUtensorMap map_k,
+                     const __grid_constant__ CUtensorMap map_v, __nv_bfloat16* __restrict__ o,
+                     float* __restrict__ lse, int n, int nq, float scale_log2, int causal,
+                     KernelCtl ctl) {
+    static_assert(D == 64 || D == 128, "head dimension");
+    using L = Layout<D>;
+    extern __shared__ unsigned char dyn_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ Barriers bars;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    int bh, qi;
+    work_item(blockIdx.x, nq, causal != 0, bh, qi);
+    const int q0 = qi * kBM;
+    const int ntiles = causal ? qi + 1 : nq;  // kBM == kBN: the diagonal tile is tile qi
+
+    if (tid == 0) {
+        mbar_init(&bars.q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
+            mbar_init(&bars.s_full[s], 1);
+            mbar_init(&bars.p_full[s], kSoftmaxWarps * 32);
+            mbar_init(&bars.pv_done[s], 1);
+        }
+        mbar_init_fence();
+    }
+    if (warp == 0) umma::tmem_alloc(&bars.tmem, kTmemCols);
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = bars.tmem;
+
+    if (warp == kLoadWarp) {
+        // ---------------------------------------------------------------- loads
+        if (lane == 0) {
+            umma::prefetch_tensormap(&map_q);
+            umma::prefetch_tensormap(&map_k);
+            umma::prefetch_tensormap(&map_v);
+            mbar_arrive_expect_tx(&bars.q_full, L::kTile);
+#pragma unroll
+            for (int blk = 0; blk < D / 64; ++blk)
+                umma::tma_load_3d(smem + L::kQ + blk * L::kBlock, &map_q, 64 * blk, q0, bh,
+                                  &bars.q_full);
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j & 1;
+                const uint32_t reuse_parity = ((j >> 1) - 1) & 1;
+                if (j >= 2) mbar_wait_bounded(&bars.k_empty[st], reuse_parity, ctl);
+                mbar_arrive_expect_tx(&bars.k_full[st], L::kTile);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    umma::tma_load_3d(smem + L::kK + st * L::kTile + blk * L::kBlock, &map_k,
+                                      64 * blk, j * kBN, bh, &bars.k_full[st]);
+                if (j >= 2) mbar_wait_bounded(&bars.v_empty[st], reuse_parity, ctl);
+                mbar_arrive_expect_tx(&bars.v_full[st], L::kTile);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    umma::tma_load_3d(smem + L::kV + st * L::kTile + blk * L::kBlock, &map_v,
+                                      64 * blk, j * kBN, bh, &bars.v_full[st]);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMAs
+        if (lane == 0) {
+            constexpr uint32_t id_s = umma::idesc_bf16(kBM, kBN, false);
+            constexpr uint32_t id_o = umma::idesc_bf16(kBM, D, true);
+            const uint32_t q_addr = smem_addr(smem + L::kQ);
+            // O += P_i V_i: P K-major (rows = queries), V MN-major (rows = keys)
+            auto issue_pv = [&](int i) {
+                const int b = i & 1;
+                mbar_wait_bounded(&bars.p_full[b], (i >> 1) & 1, ctl);
+                mbar_wait_bounded(&bars.v_full[b], (i >> 1) & 1, ctl);
+                umma::fence_after_sync();
+                const uint32_t p_addr = smem_addr(smem + L::kP + b * L::kPTile);
+                const uint32_t v_addr = smem_addr(smem + L::kV + b * L::kTile);
+#pragma unroll
+                for (int s = 0; s < kBN / 16; ++s) {
+                    const uint64_t a =
+                        umma::desc_sw128(p_addr + (s >> 2) * L::kBlock + (s & 3) * 32, 16, 1024);
+                    const uint64_t bd = umma::desc_sw128(v_addr + s * 2048, L::kBlock, 1024);
+                    umma::mma_bf16(tmem + kTmemO, a, bd, id_o, i > 0 || s > 0);
+                }
+                umma::commit(&bars.pv_done[b]);
+                umma::commit(&bars.v_empty[b]);
+            };
+            mbar_wait_bounded(&bars.q_full, 0, ctl);
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j & 1;
+                // S buffer st was last read for tile j-2, whose P the previous
+                // issue_pv(j-2) already waited for
+                mbar_wait_bounded(&bars.k_full[st], (j >> 1) & 1, ctl);
+                umma::fence_after_sync();
+                const uint32_t k_addr = smem_addr(smem + L::kK + st * L::kTile);
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * L::kBlock + (s & 3) * 32;
+                    umma::mma_bf16(tmem + st * kTmemS1, umma::desc_sw128(q_addr + koff, 16, 1024),
+                                   umma::desc_sw128(k_addr + koff, 16, 1024), id_s, s > 0);
+                }
+                umma::commit(&bars.s_full[st]);
+                umma::commit(&bars.k_empty[st]);
+                if (j >= 1) issue_pv(j - 1);
+            }
+            issue_pv(ntiles - 1);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax
+        const int r = tid;  // row of the tile == tensor-memory lane
+        const int row_q = q0 + r;
+        const uint32_t lane_addr = tmem + (uint32_t(warp * 32) << 16);
+        float m = -INFINITY;  // exponent base, base-2 units of the scaled scores
+        float l = 0.f;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            mbar_wait_bounded(&bars.s_full[st], (j >> 1) & 1, ctl);
+            umma::fence_after_sync();
+            float s[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) umma::tmem_ld32(lane_addr + st * kTmemS1 + 32 * c, s + 32 * c);
+            umma::tmem_wait_ld();
+
+            // keys past the sequence end, and under the mask keys after the query
+            int lim = min(kBN, n - j * kBN);
+            if (causal) lim = min(lim, row_q - j * kBN + 1);
+            float mt = -INFINITY;
+            if (lim >= kBN) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, s[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    if (c >= lim) s[c] = -INFINITY;
+                    mt = fmaxf(mt, s[c]);
+                }
+            }
+            const float mt2 = mt * scale_log2;  // scale > 0: the maximum of the scaled scores
+            const bool grow = mt2 > m + kRescaleLog2;
+            float alpha = 1.f;
+            if (grow) {
+                alpha = ex2_sfu(m - mt2);  // +0 when m = -inf
+                l *= alpha;
+                m = mt2;
+            }
+            // tcgen05.ld/st are warp-collective: a warp rescales its O rows when
+            // any of its rows moved its base (the others multiply by 1)
+            if (j > 0 && __any_sync(kFullMask, grow)) {
+                mbar_wait_bounded(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl);
+                umma::fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float t[32];
+                    umma::tmem_ld32(lane_addr + kTmemO + 32 * c, t);
+                    umma::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) t[e] *= alpha;
+                    umma::tmem_st32(lane_addr + kTmemO + 32 * c, t);
+                }
+                umma::tmem_wait_st();
+            }
+            // P buffer st was read by P_{j-2} V_{j-2}
+            if (j >= 2) mbar_wait_bounded(&bars.pv_done[st], ((j - 2) >> 1) & 1, ctl);
+
+            // P = 2^(s scale log2e - m) in bf16, written in the 128-byte-swizzled
+            // K-major layout (16-byte chunk c of row r at chunk c ^ (r mod 8));
+            // l sums the fp32 values before rounding
+            const float base = m == -INFINITY ? 0.f : m;
+            unsigned char* prow = smem + L::kP + st * L::kPTile + r * 128;
+            float2 lsum = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int blk = 0; blk < kBN / 64; ++blk) {
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = blk * 64 + ch * 8 + 2 * e;
+                        const float p0 = ex2_sfu(fmaf(s[k], scale_log2, -base));
+                        const float p1 = ex2_sfu(fmaf(s[k + 1], scale_log2, -base));
+                        w[e] = pack_bf16x2(p0, p1);
+                        lsum = add2(lsum, make_float2(p0, p1));
+                    }
+                    const int pos = blk * L::kBlock + ((ch ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(prow + pos) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            l += lsum.x + lsum.y;
+            umma::fence_proxy_async_smem();
+            umma::fence_before_sync();
+            umma::mbar_arrive(&bars.p_full[st]);
+        }
+
+        // ---------------------------------------------------------------- epilogue
+        const int last = ntiles - 1;
+        mbar_wait_bounded(&bars.pv_done[last & 1], (last >> 1) & 1, ctl);
+        umma::fence_after_sync();
+        const float inv_l = 1.f / l;
+        __nv_bfloat16* orow = o + (int64_t(bh) * n + row_q) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float t[32];
+            umma::tmem_ld32(lane_addr + kTmemO + 32 * c, t);
+            umma::tmem_wait_ld();
+            if (row_q < n) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16x2(t[8 * v + 0] * inv_l, t[8 * v + 1] * inv_l);
+                    w.y = pack_bf16x2(t[8 * v + 2] * inv_l, t[8 * v + 3] * inv_l);
+                    w.z = pack_bf16x2(t[8 * v + 4] * inv_l, t[8 * v + 5] * inv_l);
+                    w.w = pack_bf16x2(t[8 * v + 6] * inv_l, t[8 * v + 7] * inv_l);
+                    *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = w;
+                }
+            }
+        }
+        if (lse && row_q < n) lse[int64_t(bh) * n + row_q] = (m + __log2f(l)) * kLn2;
+    }
+
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        umma::fence_after_sync();
+        umma::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace attn
+}  // namespace os

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 LIB = os.path.join(ROOT, "softmax_topk_gb300", "lib", "libos_softmax.so")
 
 F32, BF16 = 0, 1
-OK, NULL, SHAPE, DTYPE, KERR, ALIAS, CUDA, TIMEOUT, PATH, ALIGN = range(10)
+OK, NULL, SHAPE, DTYPE, KERR, ALIAS, CUDA, TIMEOUT, PATH, ALIGN, VALUE = range(11)
 
 
 def _ensure_built():
@@ -38,7 +38,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ("os_softmax_fwd", "os_softmax_topk", "os_status_string"):
+    for required in ("os_softmax_fwd", "os_softmax_topk", "os_attention_fwd", "os_status_string"):
         assert required in names, names
 
 
@@ -142,6 +142,33 @@ def test_sample_argument_errors(lib):
     assert f(A, B, C + 2, D, 4, 8, None) == ALIGN
     assert f(A, B, C, A + 16, 4, 8, None) == ALIAS
     assert f(None, None, None, None, 0, 8, None) == OK
+
+
+def test_attention_argument_errors(lib):
+    f = lib.os_attention_fwd
+    D = 0xC000000  # o; 16-byte aligned, clear of A, B, C for these sizes
+    E = 0xE000000  # lse
+    s = 0.125
+    assert f(A, B, C, D, E, -1, 128, 64, s, 0, None) == SHAPE
+    assert f(A, B, C, D, E, 2, -1, 64, s, 0, None) == SHAPE
+    assert f(A, B, C, D, E, 2, 128, 96, s, 0, None) == SHAPE
+    assert f(A, B, C, D, E, 2, 2 ** 31, 64, s, 0, None) == SHAPE
+    assert f(A, B, C, D, E, 2 ** 31, 4096, 64, s, 0, None) == SHAPE
+    assert f(A, B, C, D, E, 2, 128, 64, 0.0, 0, None) == VALUE
+    assert f(A, B, C, D, E, 2, 128, 64, -s, 0, None) == VALUE
+    assert f(A, B, C, D, E, 2, 128, 64, float("inf"), 0, None) == VALUE
+    assert f(A, B, C, D, E, 2, 128, 64, float("nan"), 0, None) == VALUE
+    assert f(A, B, C, D, E, 2, 128, 64, s, 2, None) == VALUE
+    assert f(None, B, C, D, E, 2, 128, 64, s, 0, None) == NULL
+    assert f(A, B, C, None, E, 2, 128, 64, s, 0, None) == NULL
+    assert f(A + 8, B, C, D, E, 2, 128, 64, s, 0, None) == ALIGN
+    assert f(A, B, C, D + 8, E, 2, 128, 64, s, 0, None) == ALIGN
+    assert f(A, B, C, D, E + 2, 2, 128, 64, s, 0, None) == ALIGN
+    assert f(A, B, C, A + 16, E, 2, 128, 64, s, 0, None) == ALIAS
+    assert f(A, B, C, D, D + 64, 2, 128, 64, s, 0, None) == ALIAS
+    assert f(A, B, C, D, C, 2, 128, 64, s, 0, None) == ALIAS
+    assert f(None, None, None, None, None, 0, 128, 64, s, 0, None) == OK
+    assert f(None, None, None, None, None, 4, 0, 128, s, 1, None) == OK
 
 
 def test_exp_argument_errors(lib):

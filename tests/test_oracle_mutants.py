@@ -53,9 +53,9 @@ MUTANTS = {
     "attention_key_row_of_query": ("acc += qi[c] * kb[j * dh + c];", "acc += qi[c] * kb[i * dh + c];"),
     "attention_unnormalised": ("const double p = exp(s[j] - m) / d;",
                                "const double p = exp(s[j] - m);"),
-    "attention_lse_drops_max": ("lse[r] = m + log(d);", "lse[r] = log(d);"),
-    "attention_max_not_subtracted_in_weights": ("d += exp(s[j] - m);\n            double *oi",
-                                                "d += exp(s[j]);\n            double *oi"),
+    "attention_lse_drops_max": ("*lse_out = m + log(d);", "*lse_out = log(d);"),
+    "attention_max_not_subtracted_in_weights": ("d += exp(s[j] - m);\n    for (int64_t c",
+                                                "d += exp(s[j]);\n    for (int64_t c"),
 }
 
 

@@ -334,11 +334,20 @@ def pin_attention_tiled_recurrence(lib):
             for scale in (None, 0.7):
                 o, L = oracle.attention(q, k, v, scale, causal, lib=lib)
                 sc = 1.0 / math.sqrt(dh) if scale is None else scale
+                refs = []
                 for b in range(2):
                     O_ref, L_ref = _tiled_attention(q[b].tolist(), k[b].tolist(), v[b].tolist(),
                                                     sc, causal, Br, Bc)
+                    refs.append((np.array(O_ref), np.array(L_ref)))
                     assert np.allclose(o[b], O_ref, rtol=1e-12, atol=1e-12), (n, dh, causal)
                     assert np.allclose(L[b], L_ref, rtol=1e-12, atol=1e-12), (n, dh, causal)
+                # the selected-rows entry: pairs in scrambled order
+                sl = np.array([1, 0, 1, 0])
+                rw = np.array([n - 1, 0, n // 2, n - 1])
+                o2, L2 = oracle.attention_rows(q[sl, rw], k, v, sl, rw, scale, causal, lib=lib)
+                for p, (b, i) in enumerate(zip(sl, rw)):
+                    assert np.allclose(o2[p], refs[b][0][i], rtol=1e-12, atol=1e-12), (b, i)
+                    assert np.allclose(L2[p], refs[b][1][i], rtol=1e-12, atol=1e-12), (b, i)
 
 
 def pin_attention_closed_forms(lib):
