@@ -56,7 +56,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
                      float* lse, int64_t bh, int n, float scale_log2, bool causal,
                      const KernelCtl& ctl, cudaStream_t stream) {
     auto k = attn::attention_fwd_kernel<D>;
-    constexpr int smem = attn::Layout<D>::kDynBytes;
+    constexpr int smem = attn::Layout<D, attn::Stages<D>::value>::kDynBytes;
     if (!prepare_kernel(k, 1, smem)) return cudaErrorInvalidConfiguration;
     const int nq = (n + attn::kBM - 1) / attn::kBM;
     return launch_kernel(k, bh * nq, attn::kThreads, 1, smem, stream, mq, mk, mv,

@@ -11,17 +11,22 @@
 // With the causal mask, query i sees keys j <= i and the key walk stops at the
 // diagonal tile (section 5 of the same page).
 //
-// GB300 mapping (one CTA per query tile, 192 threads, warp-specialised):
+// GB300 mapping (one CTA per query tile, 224 threads, warp-specialised):
 //   * warp 4 (one lane) streams the Q tile once and the K/V tiles through a
-//     two-stage ring with TMA tiled loads (128-byte swizzle, rows past the
-//     sequence end zero-filled by the copy engine);
-//   * warp 5 (one lane) issues tcgen05.mma: S_j = Q K_j^T into one of two
-//     128-column fp32 accumulators in tensor memory, then O += P_j V_j into a
-//     D-column accumulator that stays in tensor memory for the whole walk;
+//     ring of STAGES buffers with TMA tiled loads (128-byte swizzle, rows past
+//     the sequence end zero-filled by the copy engine);
+//   * warp 5 (one lane) issues S_j = Q K_j^T (tcgen05.mma) into one of two
+//     128-column fp32 accumulators in tensor memory;
+//   * warp 6 (one lane) issues O += P_j V_j into a D-column accumulator that
+//     stays in tensor memory for the whole walk.  The two products touch
+//     disjoint tensor-memory columns, and with two issuers one keeps the
+//     tensor pipe fed while the other waits on a barrier (the pipe queues
+//     only about one instruction ahead of its issuer);
 //   * warps 0-3 (the softmax warps) own one query row per thread, which is one
 //     tensor-memory lane: they read S_j with tcgen05.ld, mask, update (m, l),
-//     write P_j = 2^(S_j scale log2e - m) as bf16 into shared memory in the
-//     layout the next MMA reads, and at the end normalise O.
+//     write P_j = 2^(S_j scale log2e - m) as packed bf16 pairs into tensor
+//     memory with tcgen05.st (the A operand of the P V product is read from
+//     there, so P never touches shared memory), and at the end normalise O.
 // S_{j+1} is computed while the softmax warps work on S_j, and P_j V_j runs
 // while they work on S_{j+1}.
 //
@@ -48,36 +53,42 @@ constexpr int kBM = 128;  // query rows per CTA (one per tensor-memory lane)
 constexpr int kBN = 128;  // keys per tile
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kMmaSWarp = 5;
+constexpr int kMmaPVWarp = 6;
+constexpr int kThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS1 = 128;         // S accumulators at columns 0 and 128
 constexpr uint32_t kTmemO = 256;          // O accumulator, D columns
+constexpr uint32_t kTmemP = 384;          // P buffers at columns 384 and 448 (bf16 pairs)
 constexpr float kRescaleLog2 = 8.0f;      // move the base when the max grows by more than 2^8
 constexpr float kLn2 = 0.693147182f;
 
 // Dynamic shared memory, 1024-byte aligned regions (the 128-byte swizzle
 // repeats every 1024 bytes).  A Q/K/V tile is D/64 blocks of [128 rows][64
-// bf16]; P is 2 blocks of [128 query rows][64 keys].
-template <int D>
+// bf16].
+template <int D, int STAGES>
 struct Layout {
     static constexpr int kBlock = kBM * 64 * 2;  // 16 KB
     static constexpr int kTile = kBM * D * 2;
-    static constexpr int kPTile = kBM * kBN * 2;
     static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTile;       // 2 stages
-    static constexpr int kV = kK + 2 * kTile;   // 2 stages
-    static constexpr int kP = kV + 2 * kTile;   // 2 buffers
-    static constexpr int kBytes = kP + 2 * kPTile;
+    static constexpr int kK = kQ + kTile;            // STAGES buffers
+    static constexpr int kV = kK + STAGES * kTile;   // STAGES buffers
+    static constexpr int kBytes = kV + STAGES * kTile;
     static constexpr int kDynBytes = kBytes + 1024;
 };
 
+// Ring depth per head dimension: as deep as shared memory allows.
+template <int D> struct Stages;
+template <> struct Stages<128> { static constexpr int value = 3; };
+template <> struct Stages<64> { static constexpr int value = 5; };
+
+template <int STAGES>
 struct Barriers {
     uint64_t q_full;
-    uint64_t k_full[2], v_full[2];    // TMA landed (transaction bytes)
-    uint64_t k_empty[2], v_empty[2];  // the MMAs reading the stage completed
+    uint64_t k_full[STAGES], v_full[STAGES];    // TMA landed (transaction bytes)
+    uint64_t k_empty[STAGES], v_empty[STAGES];  // the MMAs reading the stage completed
     uint64_t s_full[2];               // S_j in tensor memory
-    uint64_t p_full[2];               // P_j in shared memory (128 arrivals)
+    uint64_t p_full[2];               // P_j in tensor memory (128 arrivals)
     uint64_t pv_done[2];              // P_j V_j accumulated into O
     uint32_t tmem;
 };
@@ -99,11 +110,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                      float* __restrict__ lse, int n, int nq, float scale_log2, int causal,
                      KernelCtl ctl) {
     static_assert(D == 64 || D == 128, "head dimension");
-    using L = Layout<D>;
+    constexpr int STAGES = Stages<D>::value;
+    using L = Layout<D, STAGES>;
     extern __shared__ unsigned char dyn_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ Barriers bars;
+    __shared__ Barriers<STAGES> bars;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     int bh, qi;
@@ -113,11 +125,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
 
     if (tid == 0) {
         mbar_init(&bars.q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
             mbar_init(&bars.v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.s_full[s], 1);
             mbar_init(&bars.p_full[s], kSoftmaxWarps * 32);
             mbar_init(&bars.pv_done[s], 1);
@@ -142,15 +156,15 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                 umma::tma_load_3d(smem + L::kQ + blk * L::kBlock, &map_q, 64 * blk, q0, bh,
                                   &bars.q_full);
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j & 1;
-                const uint32_t reuse_parity = ((j >> 1) - 1) & 1;
-                if (j >= 2) mbar_wait_bounded(&bars.k_empty[st], reuse_parity, ctl);
+                const int st = j % STAGES;
+                const uint32_t reuse_parity = (j / STAGES - 1) & 1;
+                if (j >= STAGES) mbar_wait_bounded(&bars.k_empty[st], reuse_parity, ctl);
                 mbar_arrive_expect_tx(&bars.k_full[st], L::kTile);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
                     umma::tma_load_3d(smem + L::kK + st * L::kTile + blk * L::kBlock, &map_k,
                                       64 * blk, j * kBN, bh, &bars.k_full[st]);
-                if (j >= 2) mbar_wait_bounded(&bars.v_empty[st], reuse_parity, ctl);
+                if (j >= STAGES) mbar_wait_bounded(&bars.v_empty[st], reuse_parity, ctl);
                 mbar_arrive_expect_tx(&bars.v_full[st], L::kTile);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
@@ -158,38 +172,20 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                                       64 * blk, j * kBN, bh, &bars.v_full[st]);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- MMAs
+    } else if (warp == kMmaSWarp) {
+        // ---------------------------------------------------------------- S = Q K^T
         if (lane == 0) {
             constexpr uint32_t id_s = umma::idesc_bf16(kBM, kBN, false);
-            constexpr uint32_t id_o = umma::idesc_bf16(kBM, D, true);
             const uint32_t q_addr = smem_addr(smem + L::kQ);
-            // O += P_i V_i: P K-major (rows = queries), V MN-major (rows = keys)
-            auto issue_pv = [&](int i) {
-                const int b = i & 1;
-                mbar_wait_bounded(&bars.p_full[b], (i >> 1) & 1, ctl);
-                mbar_wait_bounded(&bars.v_full[b], (i >> 1) & 1, ctl);
-                umma::fence_after_sync();
-                const uint32_t p_addr = smem_addr(smem + L::kP + b * L::kPTile);
-                const uint32_t v_addr = smem_addr(smem + L::kV + b * L::kTile);
-#pragma unroll
-                for (int s = 0; s < kBN / 16; ++s) {
-                    const uint64_t a =
-                        umma::desc_sw128(p_addr + (s >> 2) * L::kBlock + (s & 3) * 32, 16, 1024);
-                    const uint64_t bd = umma::desc_sw128(v_addr + s * 2048, L::kBlock, 1024);
-                    umma::mma_bf16(tmem + kTmemO, a, bd, id_o, i > 0 || s > 0);
-                }
-                umma::commit(&bars.pv_done[b]);
-                umma::commit(&bars.v_empty[b]);
-            };
             mbar_wait_bounded(&bars.q_full, 0, ctl);
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j & 1;
-                // S buffer st was last read for tile j-2, whose P the previous
-                // issue_pv(j-2) already waited for
-                mbar_wait_bounded(&bars.k_full[st], (j >> 1) & 1, ctl);
+                const int st = j & 1, ks = j % STAGES;
+                // S buffer st is free once the softmax warps have turned S_{j-2}
+                // into P_{j-2}
+                if (j >= 2) mbar_wait_bounded(&bars.p_full[st], ((j - 2) >> 1) & 1, ctl);
+                mbar_wait_bounded(&bars.k_full[ks], (j / STAGES) & 1, ctl);
                 umma::fence_after_sync();
-                const uint32_t k_addr = smem_addr(smem + L::kK + st * L::kTile);
+                const uint32_t k_addr = smem_addr(smem + L::kK + ks * L::kTile);
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t koff = (s >> 2) * L::kBlock + (s & 3) * 32;
@@ -197,10 +193,30 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                                    umma::desc_sw128(k_addr + koff, 16, 1024), id_s, s > 0);
                 }
                 umma::commit(&bars.s_full[st]);
-                umma::commit(&bars.k_empty[st]);
-                if (j >= 1) issue_pv(j - 1);
+                umma::commit(&bars.k_empty[ks]);
             }
-            issue_pv(ntiles - 1);
+        }
+    } else if (warp == kMmaPVWarp) {
+        // ---------------------------------------------------------------- O += P V
+        // P from tensor memory (lane = query row, 16 keys per 8 columns), V
+        // MN-major in shared memory (rows = keys)
+        if (lane == 0) {
+            constexpr uint32_t id_o = umma::idesc_bf16(kBM, D, true);
+            for (int i = 0; i < ntiles; ++i) {
+                const int b = i & 1, vs = i % STAGES;
+                mbar_wait_bounded(&bars.p_full[b], (i >> 1) & 1, ctl);
+                mbar_wait_bounded(&bars.v_full[vs], (i / STAGES) & 1, ctl);
+                umma::fence_after_sync();
+                const uint32_t v_addr = smem_addr(smem + L::kV + vs * L::kTile);
+#pragma unroll
+                for (int s = 0; s < kBN / 16; ++s) {
+                    const uint64_t bd = umma::desc_sw128(v_addr + s * 2048, L::kBlock, 1024);
+                    umma::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + 64 * b + 8 * s, bd, id_o,
+                                          i > 0 || s > 0);
+                }
+                umma::commit(&bars.pv_done[b]);
+                umma::commit(&bars.v_empty[vs]);
+            }
         }
     } else {
         // ---------------------------------------------------------------- softmax
@@ -221,17 +237,21 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
             // keys past the sequence end, and under the mask keys after the query
             int lim = min(kBN, n - j * kBN);
             if (causal) lim = min(lim, row_q - j * kBN + 1);
-            float mt = -INFINITY;
-            if (lim >= kBN) {
+            if (lim < kBN) {
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, s[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
+                for (int c = 0; c < kBN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
-                    mt = fmaxf(mt, s[c]);
-                }
             }
+            // tile maximum: eight independent chains of three-input maxima
+            float mx[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = s[a];
+#pragma unroll
+            for (int c = 8; c < kBN; c += 16) {
+#pragma unroll
+                for (int a = 0; a < 8; ++a) mx[a] = max3(mx[a], s[c + a], s[c + 8 + a < kBN ? c + 8 + a : c + a]);
+            }
+            const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), fmaxf(max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float mt2 = mt * scale_log2;  // scale > 0: the maximum of the scaled scores
             const bool grow = mt2 > m + kRescaleLog2;
             float alpha = 1.f;
@@ -254,36 +274,29 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                     for (int e = 0; e < 32; ++e) t[e] *= alpha;
                     umma::tmem_st32(lane_addr + kTmemO + 32 * c, t);
                 }
-                umma::tmem_wait_st();
             }
-            // P buffer st was read by P_{j-2} V_{j-2}
-            if (j >= 2) mbar_wait_bounded(&bars.pv_done[st], ((j - 2) >> 1) & 1, ctl);
 
-            // P = 2^(s scale log2e - m) in bf16, written in the 128-byte-swizzled
-            // K-major layout (16-byte chunk c of row r at chunk c ^ (r mod 8));
-            // l sums the fp32 values before rounding
+            // P = 2^(s scale log2e - m): fp32 values summed into l, bf16 pairs
+            // (even key in the low half) into tensor memory; the P buffer was
+            // last read by P_{j-2} V_{j-2}
             const float base = m == -INFINITY ? 0.f : m;
-            unsigned char* prow = smem + L::kP + st * L::kPTile + r * 128;
-            float2 lsum = make_float2(0.f, 0.f);
+            const float2 sl2 = splat2(scale_log2), nb2 = splat2(-base);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            uint32_t pk[kBN / 2];
 #pragma unroll
-            for (int blk = 0; blk < kBN / 64; ++blk) {
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = blk * 64 + ch * 8 + 2 * e;
-                        const float p0 = ex2_sfu(fmaf(s[k], scale_log2, -base));
-                        const float p1 = ex2_sfu(fmaf(s[k + 1], scale_log2, -base));
-                        w[e] = pack_bf16x2(p0, p1);
-                        lsum = add2(lsum, make_float2(p0, p1));
-                    }
-                    const int pos = blk * L::kBlock + ((ch ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(prow + pos) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
+            for (int c = 0; c < kBN / 2; ++c) {
+                const float2 z = fma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nb2);
+                const float2 p = make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
+                acc[c & 3] = add2(acc[c & 3], p);
+                pk[c] = pack_bf16x2(p.x, p.y);
             }
-            l += lsum.x + lsum.y;
-            umma::fence_proxy_async_smem();
+            l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) +
+                 (acc[3].x + acc[3].y);
+            if (j >= 2) mbar_wait_bounded(&bars.pv_done[st], ((j - 2) >> 1) & 1, ctl);
+            umma::tmem_st32(lane_addr + kTmemP + 64 * st, reinterpret_cast<const float*>(pk));
+            umma::tmem_st32(lane_addr + kTmemP + 64 * st + 32, reinterpret_cast<const float*>(pk + 32));
+            umma::tmem_wait_st();
             umma::fence_before_sync();
             umma::mbar_arrive(&bars.p_full[st]);
         }

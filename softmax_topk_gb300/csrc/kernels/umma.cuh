@@ -49,6 +49,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
                  : "memory");
 }
 
+// The same with A read from tensor memory at `tmem_a` (lane = row of A, each
+// 32-bit column two consecutive K elements, the lower one in the low half).
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b,
+                                                uint32_t idesc, bool accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(tmem_d), "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
+                 : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
