@@ -158,13 +158,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % STAGES;
                 const uint32_t reuse_parity = (j / STAGES - 1) & 1;
-                if (j >= STAGES) mbar_wait_bounded(&bars.k_empty[st], reuse_parity, ctl);
+                if (j >= STAGES) umma::mbar_wait(&bars.k_empty[st], reuse_parity, ctl);
                 mbar_arrive_expect_tx(&bars.k_full[st], L::kTile);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
                     umma::tma_load_3d(smem + L::kK + st * L::kTile + blk * L::kBlock, &map_k,
                                       64 * blk, j * kBN, bh, &bars.k_full[st]);
-                if (j >= STAGES) mbar_wait_bounded(&bars.v_empty[st], reuse_parity, ctl);
+                if (j >= STAGES) umma::mbar_wait(&bars.v_empty[st], reuse_parity, ctl);
                 mbar_arrive_expect_tx(&bars.v_full[st], L::kTile);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
@@ -177,13 +177,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
         if (lane == 0) {
             constexpr uint32_t id_s = umma::idesc_bf16(kBM, kBN, false);
             const uint32_t q_addr = smem_addr(smem + L::kQ);
-            mbar_wait_bounded(&bars.q_full, 0, ctl);
+            umma::mbar_wait(&bars.q_full, 0, ctl);
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j & 1, ks = j % STAGES;
                 // S buffer st is free once the softmax warps have turned S_{j-2}
                 // into P_{j-2}
-                if (j >= 2) mbar_wait_bounded(&bars.p_full[st], ((j - 2) >> 1) & 1, ctl);
-                mbar_wait_bounded(&bars.k_full[ks], (j / STAGES) & 1, ctl);
+                if (j >= 2) umma::mbar_wait(&bars.p_full[st], ((j - 2) >> 1) & 1, ctl);
+                umma::mbar_wait(&bars.k_full[ks], (j / STAGES) & 1, ctl);
                 umma::fence_after_sync();
                 const uint32_t k_addr = smem_addr(smem + L::kK + ks * L::kTile);
 #pragma unroll
@@ -204,8 +204,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
             constexpr uint32_t id_o = umma::idesc_bf16(kBM, D, true);
             for (int i = 0; i < ntiles; ++i) {
                 const int b = i & 1, vs = i % STAGES;
-                mbar_wait_bounded(&bars.p_full[b], (i >> 1) & 1, ctl);
-                mbar_wait_bounded(&bars.v_full[vs], (i / STAGES) & 1, ctl);
+                umma::mbar_wait(&bars.p_full[b], (i >> 1) & 1, ctl);
+                umma::mbar_wait(&bars.v_full[vs], (i / STAGES) & 1, ctl);
                 umma::fence_after_sync();
                 const uint32_t v_addr = smem_addr(smem + L::kV + vs * L::kTile);
 #pragma unroll
@@ -227,7 +227,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
         float l = 0.f;
         for (int j = 0; j < ntiles; ++j) {
             const int st = j & 1;
-            mbar_wait_bounded(&bars.s_full[st], (j >> 1) & 1, ctl);
+            umma::mbar_wait(&bars.s_full[st], (j >> 1) & 1, ctl);
             umma::fence_after_sync();
             float s[kBN];
 #pragma unroll
@@ -242,58 +242,83 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                 for (int c = 0; c < kBN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            // tile maximum: eight independent chains of three-input maxima
-            float mx[8];
+            // P = 2^(s scale log2e - m): fp32 values summed into l, bf16 pairs
+            // (even key in the low half) for tensor memory.  Once a base m
+            // exists the exponentials are taken against it speculatively,
+            // with the tile maximum folded into the same pass (eight chains of
+            // three-input maxima hidden under the SFU work); only a warp in
+            // which some row's maximum outgrew its base by more than 2^8 does
+            // the pass again with the new bases.
+            uint32_t pk[kBN / 2];
+            auto exp_pass = [&](float base, bool want_max, float& mt) {
+                const float2 sl2 = splat2(scale_log2), nb2 = splat2(-base);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float mx[8];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) mx[a] = s[a];
+                for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
 #pragma unroll
-            for (int c = 8; c < kBN; c += 16) {
+                for (int c = 0; c < kBN / 2; ++c) {
+                    if (want_max) mx[c & 7] = max3(mx[c & 7], s[2 * c], s[2 * c + 1]);
+                    const float2 z = fma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nb2);
+                    const float2 p = make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
+                    acc[c & 3] = add2(acc[c & 3], p);
+                    pk[c] = pack_bf16x2(p.x, p.y);
+                }
+                if (want_max)
+                    mt = fmaxf(max3(mx[0], mx[1], mx[2]),
+                               fmaxf(max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) +
+                       (acc[3].x + acc[3].y);
+            };
+            float mt = -INFINITY, lsum = 0.f;
+            bool grow;
+            if (__all_sync(kFullMask, m != -INFINITY)) {
+                lsum = exp_pass(m, true, mt);
+                grow = mt * scale_log2 > m + kRescaleLog2;  // scale > 0
+            } else {
+                float mx[8];
 #pragma unroll
-                for (int a = 0; a < 8; ++a) mx[a] = max3(mx[a], s[c + a], s[c + 8 + a < kBN ? c + 8 + a : c + a]);
+                for (int a = 0; a < 8; ++a) mx[a] = s[a];
+#pragma unroll
+                for (int c = 8; c < kBN; c += 16) {
+#pragma unroll
+                    for (int a = 0; a < 8; ++a)
+                        mx[a] = max3(mx[a], s[c + a], s[c + 8 + a < kBN ? c + 8 + a : c + a]);
+                }
+                mt = fmaxf(max3(mx[0], mx[1], mx[2]),
+                           fmaxf(max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                grow = true;  // every row takes a new base (a row still at -inf keeps it)
             }
-            const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), fmaxf(max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float mt2 = mt * scale_log2;  // scale > 0: the maximum of the scaled scores
-            const bool grow = mt2 > m + kRescaleLog2;
+            const float mt2 = mt * scale_log2;
+            grow = grow && mt2 > m;
             float alpha = 1.f;
             if (grow) {
                 alpha = ex2_sfu(m - mt2);  // +0 when m = -inf
                 l *= alpha;
                 m = mt2;
             }
-            // tcgen05.ld/st are warp-collective: a warp rescales its O rows when
-            // any of its rows moved its base (the others multiply by 1)
-            if (j > 0 && __any_sync(kFullMask, grow)) {
-                mbar_wait_bounded(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl);
-                umma::fence_after_sync();
+            if (__any_sync(kFullMask, grow)) {
+                float unused;
+                lsum = exp_pass(m == -INFINITY ? 0.f : m, false, unused);
+                // tcgen05.ld/st are warp-collective: the warp rescales its O
+                // rows (rows that kept their base multiply by 1)
+                if (j > 0) {
+                    umma::mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl);
+                    umma::fence_after_sync();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float t[32];
-                    umma::tmem_ld32(lane_addr + kTmemO + 32 * c, t);
-                    umma::tmem_wait_ld();
+                    for (int c = 0; c < D / 32; ++c) {
+                        float t[32];
+                        umma::tmem_ld32(lane_addr + kTmemO + 32 * c, t);
+                        umma::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) t[e] *= alpha;
-                    umma::tmem_st32(lane_addr + kTmemO + 32 * c, t);
+                        for (int e = 0; e < 32; ++e) t[e] *= alpha;
+                        umma::tmem_st32(lane_addr + kTmemO + 32 * c, t);
+                    }
                 }
             }
-
-            // P = 2^(s scale log2e - m): fp32 values summed into l, bf16 pairs
-            // (even key in the low half) into tensor memory; the P buffer was
-            // last read by P_{j-2} V_{j-2}
-            const float base = m == -INFINITY ? 0.f : m;
-            const float2 sl2 = splat2(scale_log2), nb2 = splat2(-base);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
-            uint32_t pk[kBN / 2];
-#pragma unroll
-            for (int c = 0; c < kBN / 2; ++c) {
-                const float2 z = fma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nb2);
-                const float2 p = make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
-                acc[c & 3] = add2(acc[c & 3], p);
-                pk[c] = pack_bf16x2(p.x, p.y);
-            }
-            l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) +
-                 (acc[3].x + acc[3].y);
-            if (j >= 2) mbar_wait_bounded(&bars.pv_done[st], ((j - 2) >> 1) & 1, ctl);
+            l += lsum;
+            if (j >= 2) umma::mbar_wait(&bars.pv_done[st], ((j - 2) >> 1) & 1, ctl);
             umma::tmem_st32(lane_addr + kTmemP + 64 * st, reinterpret_cast<const float*>(pk));
             umma::tmem_st32(lane_addr + kTmemP + 64 * st + 32, reinterpret_cast<const float*>(pk + 32));
             umma::tmem_wait_st();
@@ -303,7 +328,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
 
         // ---------------------------------------------------------------- epilogue
         const int last = ntiles - 1;
-        mbar_wait_bounded(&bars.pv_done[last & 1], (last >> 1) & 1, ctl);
+        umma::mbar_wait(&bars.pv_done[last & 1], (last >> 1) & 1, ctl);
         umma::fence_after_sync();
         const float inv_l = 1.f / l;
         __nv_bfloat16* orow = o + (int64_t(bh) * n + row_q) * D;
