@@ -289,6 +289,8 @@ def run_ours(args):
         line["extra_workloads"] = run_extra(st, dev, args)
         line["unfused_baselines"] = run_baselines(st, dev, args)
         line["stats_and_causal"] = run_stats_and_causal(st, dev, args)
+        line["attention"] = run_attention(st, dev, args, rank == 0 and world == 1 and
+                                          not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -515,6 +517,73 @@ def run_stats_and_causal(st, dev, args):
     return out
 
 
+def attention_flops(w, causal: bool, head_dim: int | None = None) -> int:
+    """Algorithmic FLOPs of one attention forward: 2 for each multiply-add of
+    Q K^T and of P V over the (query, key) pairs the mask keeps."""
+    d = head_dim or w.head_dim
+    pairs = w.seq_len * (w.seq_len + 1) // 2 if causal else w.seq_len ** 2
+    return 4 * w.bh * pairs * d
+
+
+def attention_oracle_rate(w, causal: bool, target_seconds: float) -> dict:
+    """The float64 oracle on a bounded sample of query rows of the attention
+    workload: FLOP/s over the same algorithmic count per row."""
+    import oracle
+    q, k, v = workloads.make_attention(w, device="cpu")
+    k64, v64 = k.double().numpy(), v.double().numpy()
+    qf = q.double().numpy()
+    rng = np.random.default_rng(7)
+    n_rows, done_rows, flops, t_total = 16, 0, 0, 0.0
+    while t_total < target_seconds and done_rows < 65536:
+        sl = rng.integers(0, w.bh, n_rows)
+        rw = rng.integers(0, w.seq_len, n_rows)
+        t0 = time.perf_counter()
+        oracle.attention_rows(qf[sl, rw], k64, v64, sl, rw, None, causal)
+        t_total += time.perf_counter() - t0
+        done_rows += n_rows
+        flops += int(sum(4 * w.head_dim * ((r + 1) if causal else w.seq_len) for r in rw))
+        n_rows = min(n_rows * 2, 512)
+    return {"value": round(flops / t_total / 1e9, 3), "unit": "GFLOP/s", "kind": "oracle",
+            "cores": oracle.num_threads(),
+            "sample": f"{done_rows} random query rows of {w.name}, causal={causal}"}
+
+
+def run_attention(st, dev, args, with_cpu: bool) -> dict:
+    """Attention forward on the tensor cores: the 4 x 16 x 4096 x 128 workload
+    (and its first 64 head dimensions) with and without the causal mask; FLOP/s
+    against the measured dense bf16 peak (burst, and sustained for context)."""
+    w = workloads.ATTENTION_WORKLOADS["attention_4x16x4096x128_bf16"]
+    q, k, v = workloads.make_attention(w, device=dev)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pj = json.load(f)
+        peaks = {"burst": pj.get("bf16_tflops"), "sustained": pj.get("bf16_tflops_sustained")}
+    except (OSError, ValueError):
+        peaks = {"burst": 1900.0, "sustained": 1700.0, "source": "fallback"}
+    steps = max(20, min(args.steps, 200))
+    out = {"workload": w.name, "layout": "[batch*heads][seq][head_dim] bf16, O bf16, L fp32",
+           "inputs": "Q, K, V = 192 MiB, larger than L2", "peaks_tflops": peaks, "cases": {}}
+    for d in (128, 64):
+        qd, kd, vd = (t if d == 128 else t[..., :64].contiguous() for t in (q, k, v))
+        o = torch.empty_like(qd)
+        lse = torch.empty(qd.shape[:-1], dtype=torch.float32, device=dev)
+        for causal in (False, True):
+            ms = _time_ms(lambda i: st.attention(qd, kd, vd, causal=causal, out=o, lse=lse), dev,
+                          steps)
+            fl = attention_flops(w, causal, d)
+            tf = fl / ms / 1e9
+            case = {"ms": round(ms, 5), "tflops": round(tf, 1),
+                    "frac_of_measured_bf16_burst": round(tf / peaks["burst"], 4),
+                    "frac_of_measured_bf16_sustained": round(tf / peaks["sustained"], 4),
+                    "algorithmic_flops": fl}
+            out["cases"][f"d{d}_{'causal' if causal else 'full'}"] = case
+        del qd, kd, vd, o, lse
+    if with_cpu:
+        out["cpu_baseline"] = attention_oracle_rate(w, False, args.cpu_seconds / 3)
+    return out
+
+
 # ------------------------------------------------------------------ oracle (CPU) legs
 def oracle_sample_run(rows_fraction: float, seed_offset: int = 0):
     """Run the float64 oracle on the first rows of every step workload.
@@ -588,6 +657,8 @@ def run_only(args):
     import softmax_topk_gb300 as st
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.only in workloads.ATTENTION_WORKLOADS:
+        return run_only_attention(st, dev, args)
     w = workloads.WORKLOADS[args.only]
     if args.rows:
         w = w.scaled(rows=args.rows)
@@ -638,6 +709,24 @@ def run_only(args):
     print(json.dumps(out), flush=True)
 
 
+def run_only_attention(st, dev, args):
+    """One attention case for profilers: --only <attention workload>
+    [--batch-heads B] [--causal]; prints a short JSON line."""
+    w = workloads.ATTENTION_WORKLOADS[args.only]
+    if args.rows:  # batch x heads slices
+        w = w.scaled(batch=1, heads=args.rows)
+    q, k, v = workloads.make_attention(w, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    fn = lambda i: st.attention(q, k, v, causal=args.causal, out=o, lse=lse)  # noqa: E731
+    for i in range(args.warmup):
+        fn(i)
+    ms = _time_ms(fn, dev, args.steps)
+    fl = attention_flops(w, args.causal)
+    print(json.dumps({"only": w.name, "bh": w.bh, "causal": args.causal, "ms": round(ms, 5),
+                      "tflops": round(fl / ms / 1e9, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -652,11 +741,20 @@ def main():
     ap.add_argument("--K", type=int, default=64, help="with --only on the TopK workload")
     ap.add_argument("--path", default="auto", help="with --only: softmax kernel family")
     ap.add_argument("--graph", action="store_true", help="with --only: also time a CUDA graph replay")
+    ap.add_argument("--causal", action="store_true", help="with --only on an attention workload")
+    ap.add_argument("--attention", action="store_true",
+                    help="time only the attention forward leg (one JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.only:
         run_only(args)
+    elif args.attention:
+        import softmax_topk_gb300 as st
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"attention": run_attention(st, dev, args, not args.no_cpu_baseline)}),
+              flush=True)
     elif args.impl == "reference":
         run_reference(args)
     else:
