@@ -91,12 +91,21 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources the softmax kernels are compiled from (their translation units
+# and every header they include); a recorded DRAM traffic figure stands only
+# while these are unchanged.
+SOFTMAX_KERNEL_SOURCES = ("softmax_*.cu", "softmax_dispatch.cuh", "host_common.h", "internal.h",
+                          "../../include/os_softmax.h",
+                          "ctl.h", "kernels/softmax_kernels.cuh", "kernels/ops.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "softmax_topk_gb300", "csrc", "**", "*.cu*"),
-                              recursive=True)):
+    csrc = os.path.join(ROOT, "softmax_topk_gb300", "csrc")
+    files = sorted({f for pat in SOFTMAX_KERNEL_SOURCES for f in glob.glob(os.path.join(csrc, pat))})
+    for f in files:
         with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+            h.update(os.path.relpath(f, csrc).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
