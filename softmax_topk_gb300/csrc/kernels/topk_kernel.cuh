@@ -56,12 +56,17 @@ namespace os {
 
 constexpr float kLn2f = 0.693147182f;  // fp32(ln 2)
 
-struct Cand {
+// 8-byte aligned: candidates move as one 64-bit word (cluster exchange) and
+// the selection sort reuses the candidate buffer for 64-bit keys.
+struct __align__(8) Cand {
     float v;
     int j;
 };
 
 constexpr int kNoIndex = INT_MAX;
+// Candidate counts up to this are ranked by counting (n^2 / 32 comparisons
+// per warp); more are sorted (bitonic, log^2 n stages).
+constexpr int kRankMax = 256;
 
 __device__ __forceinline__ bool beats(float v1, int j1, float v2, int j2) {
     return v1 > v2 || (v1 == v2 && j1 < j2);
@@ -97,6 +102,93 @@ __device__ __forceinline__ int count_beating(const Cand* L, int K, const Cand& c
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t b = __float_as_uint(v);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_key_inverse(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Sort key of a candidate: ascending key = "beats" order (larger logit first,
+// then lower column).  -0 is keyed as +0, as the comparison treats them equal.
+__device__ __forceinline__ uint64_t cand_key(const Cand& c) {
+    return (uint64_t(~order_key(c.v + 0.0f)) << 32) | uint32_t(c.j);
+}
+
+// The best min(K, n) of the n candidates cand[0..n) into list[0..), best
+// first, by a bitonic sort of their keys over the CTA: partners within a warp
+// exchange by shuffles, across warps through shared memory (cand[] is reused
+// for the keys), and across a thread's own elements (element e * THREADS +
+// tid) in registers.  n <= THREADS * EMAX.  Entries past n stay as they were.
+// Zero values come back as +0 (the caller restores the sign from the row).
+// Every thread of the CTA must call it.
+template <int THREADS, int EMAX>
+__device__ __forceinline__ void bitonic_select(Cand* cand, int n, Cand* list, int K) {
+    static_assert(EMAX == 1 || EMAX == 2 || EMAX == 4, "elements per thread");
+    const int tid = threadIdx.x;
+    int P = 32;
+    while (P < n) P <<= 1;
+    const int E = P > THREADS ? P / THREADS : 1;  // elements per thread
+    const bool active = tid < P;                  // whole warps (P is a multiple of 32)
+    uint64_t key[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int i = e * THREADS + tid;
+        key[e] = (active && e < E && i < n) ? cand_key(cand[i]) : ~0ull;
+    }
+    uint64_t* ks = reinterpret_cast<uint64_t*>(cand);
+    __syncthreads();  // every candidate read before cand[] holds keys
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {  // uniform over the CTA
+            if (j >= THREADS) {  // j / THREADS is 1 or 2: element pairs (0,1),(2,3) or (0,2),(1,3)
+                auto cas = [&](uint64_t& a, uint64_t& b, int i) {
+                    const uint64_t lo = min(a, b), hi = max(a, b);
+                    const bool up = (i & k) == 0;
+                    a = up ? lo : hi;
+                    b = up ? hi : lo;
+                };
+                if constexpr (EMAX >= 2) {
+                    if (j == THREADS) {
+                        cas(key[0], key[1], tid);
+                        if constexpr (EMAX >= 4) cas(key[2], key[3], 2 * THREADS + tid);
+                    } else if constexpr (EMAX >= 4) {
+                        cas(key[0], key[2], tid);
+                        cas(key[1], key[3], THREADS + tid);
+                    }
+                }
+            } else if (j >= 32) {
+#pragma unroll
+                for (int e = 0; e < EMAX; ++e)
+                    if (active && e < E) ks[e * THREADS + tid] = key[e];
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < EMAX; ++e) {
+                    if (active && e < E) {
+                        const int i = e * THREADS + tid;
+                        const uint64_t o = ks[i ^ j];
+                        const bool keep_min = ((i & k) == 0) == ((i & j) == 0);
+                        key[e] = keep_min ? min(key[e], o) : max(key[e], o);
+                    }
+                }
+                __syncthreads();
+            } else if (active) {
+#pragma unroll
+                for (int e = 0; e < EMAX; ++e) {
+                    if (e < E) {
+                        const int i = e * THREADS + tid;
+                        const uint64_t o = __shfl_xor_sync(kFullMask, key[e], j);
+                        const bool keep_min = ((i & k) == 0) == ((i & j) == 0);
+                        key[e] = keep_min ? min(key[e], o) : max(key[e], o);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int i = e * THREADS + tid;
+        if (active && e < E && i < K && i < n)
+            list[i] = Cand{order_key_inverse(~uint32_t(key[e] >> 32)), int(uint32_t(key[e]))};
+    }
 }
 
 template <int THREADS>
@@ -184,7 +276,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                  int64_t rows, int cols, int K, int S, KernelCtl ctl) {
     constexpr int NW = THREADS / 32;
     constexpr int CHUNK = THREADS * U;  // 16-byte blocks per chunk
-    static_assert(CAP % 32 == 0 && CAP >= 128 && KMAX <= THREADS, "buffer sizes");
+    static_assert(CAP % THREADS == 0 && CAP >= 128 && KMAX <= THREADS, "buffer sizes");
     __shared__ __align__(16) TopkSmem<THREADS, KMAX, CAP, MAXC> sm;
     extern __shared__ __align__(16) unsigned char dyn_raw[];
     auto& dyn = *reinterpret_cast<TopkDynSmem<THREADS, U, GROUPS, FCAP>*>(dyn_raw);
@@ -444,13 +536,14 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             __syncthreads();
         }
 
-        // ---- selection: list[r] = the candidate that r candidates beat (r < K).
+        // ---- selection.  Up to kRankMax candidates: list[r] = the candidate
+        // that r candidates beat (r < K).
         // One warp per candidate, the lanes splitting the count.  The first
         // 32 * RC candidates are loaded into registers once (lane l holds l,
         // l + 32, ...) and items are passed around by shuffles, not reread from
         // shared memory (its round trips are slow while the SM's other CTA
         // streams).
-        {
+        if (n <= kRankMax) {
             constexpr int RC = KMAX > 64 ? 16 : 8;  // candidates cached per lane
             Cand reg[RC];
 #pragma unroll
@@ -475,6 +568,12 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 r = __reduce_add_sync(kFullMask, r);
                 if (lane == 0 && r < K) sm.list[r] = c;
             }
+        } else {
+            // more candidates (large K): the K best, best first, by a bitonic
+            // sort; zeros come back as +0 and take their sign from the row
+            bitonic_select<THREADS, CAP / THREADS>(sm.cand, n, sm.list, K);
+            __syncthreads();
+            if (tid < K && tid < n && sm.list[tid].v == 0.f) sm.list[tid].v = g.xr[sm.list[tid].j];
         }
 
         __syncthreads();  // the list is complete

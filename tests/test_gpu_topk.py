@@ -168,6 +168,29 @@ def test_plain_topk_ties_and_inf(st):
         _run_plain(st, x, K, f"plain ties K={K}")
 
 
+@pytest.mark.parametrize("K", [200, 256])
+def test_sorted_selection_zero_ties(st, K):
+    """More candidates than the counting rank takes (the sort path): rows of
+    -|x| with 600 zeros, half of them -0.0, so the K best are all zeros, tied,
+    and must come in column order with their own sign bits."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(17)
+    rows, cols = 4, 20000
+    x = -torch.randn(rows, cols, generator=g, device="cuda").abs() - 1e-3
+    for r in range(rows):
+        pos = torch.randperm(cols, generator=g, device="cuda")[:600]
+        x[r, pos[:300]] = 0.0
+        x[r, pos[300:]] = -0.0
+    _run_plain(st, x, K, f"zero ties K={K}")
+    vals, idx = st.topk(x, K)
+    want = torch.gather(x, 1, idx.long())
+    assert torch.equal(vals.view(torch.int32), want.view(torch.int32)), "sign of zero lost"
+    fv, fi = st.softmax_topk(x, K)
+    torch.cuda.synchronize()
+    rv, ri = oracle.topk(x.double().cpu().numpy(), K)
+    assert_topk_equal(fv.cpu().numpy(), fi.cpu().numpy(), rv, ri, f"fused zero ties K={K}")
+
+
 @pytest.mark.parametrize("K", [8, 64])
 def test_unfused_pipeline_matches_fused(st, K):
     """softmax then TopK of the probabilities (the unfused pipeline) against the
