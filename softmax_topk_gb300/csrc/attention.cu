@@ -1,6 +1,7 @@
 // Attention forward: tensor maps for Q, K, V and the launch.
 //
-// One CTA per 128-row query tile of each (batch, head) slice.  Q, K and V are
+// Persistent CTAs, one per SM, walk the 128-row query tiles of every (batch,
+// head) slice.  Q, K and V are
 // [bh][n][D] bf16, read through 3-D tensor maps (D, n, bh) with 128-byte
 // swizzle and boxes of 64 x 128 x 1, so rows past n inside a slice are
 // zero-filled by the copy engine and never read from the next slice.
@@ -58,10 +59,16 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     auto k = attn::attention_fwd_kernel<D>;
     constexpr int smem = attn::Layout<D, attn::Stages<D>::value>::kDynBytes;
     if (!prepare_kernel(k, 1, smem)) return cudaErrorInvalidConfiguration;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return cudaErrorInvalidDevice;
     const int nq = (n + attn::kBM - 1) / attn::kBM;
-    return launch_kernel(k, bh * nq, attn::kThreads, 1, smem, stream, mq, mk, mv,
-                         static_cast<__nv_bfloat16*>(o), lse, n, nq, scale_log2, causal ? 1 : 0,
-                         ctl);
+    // work units: query tiles, or with the mask pairs of them (see work_unit);
+    // one persistent CTA per SM (shared memory admits one) walks them
+    const int64_t units = causal ? bh * ((nq + 1) / 2) : bh * nq;
+    const int64_t grid = units < dev->sms ? units : dev->sms;
+    return launch_kernel(k, grid, attn::kThreads, 1, smem, stream, mq, mk, mv,
+                         static_cast<__nv_bfloat16*>(o), lse, n, nq, static_cast<int>(units),
+                         scale_log2, causal ? 1 : 0, ctl);
 }
 
 }  // namespace

@@ -90,16 +90,29 @@ struct Barriers {
     uint64_t s_full[2];               // S_j in tensor memory
     uint64_t p_full[2];               // P_j in tensor memory (128 arrivals)
     uint64_t pv_done[2];              // P_j V_j accumulated into O
+    uint64_t q_empty;                 // the S products of an item have read its Q tile
+    uint64_t o_empty;                 // the softmax warps have read an item's O (128 arrivals)
     uint32_t tmem;
 };
 
-// The query tile and (batch, head) slice of CTA `b`: slices in order, so CTAs
-// that run together share their K/V tiles in L2; with the mask the longest
-// tiles of a slice come first.
-__device__ __forceinline__ void work_item(int64_t b, int nq, bool causal, int& bh, int& qi) {
-    bh = int(b / nq);
-    const int r = int(b % nq);
-    qi = causal ? nq - 1 - r : r;
+// Work unit u of the persistent walk: one query tile (bh, qa) without the
+// mask; with it the pair of query tiles qa = nq - 1 - p and qb = p of a slice
+// (one tile when they coincide), so every unit walks nq + 1 key tiles and a
+// static round-robin over units stays balanced.  Units go slice by slice, so
+// the CTAs running together share their K/V tiles in L2.  Returns the number
+// of query tiles in the unit.
+__device__ __forceinline__ int work_unit(int u, int nq, bool causal, int& bh, int& qa, int& qb) {
+    if (!causal) {
+        bh = u / nq;
+        qa = qb = u % nq;
+        return 1;
+    }
+    const int pairs = (nq + 1) / 2;
+    bh = u / pairs;
+    const int p = u % pairs;
+    qa = nq - 1 - p;
+    qb = p;
+    return qa == qb ? 1 : 2;
 }
 
 template <int D>
@@ -107,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                      const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, __nv_bfloat16* __restrict__ o,
-                     float* __restrict__ lse, int n, int nq, float scale_log2, int causal,
-                     KernelCtl ctl) {
+                     float* __restrict__ lse, int n, int nq, int units, float scale_log2,
+                     int causal, KernelCtl ctl) {
     static_assert(D == 64 || D == 128, "head dimension");
     constexpr int STAGES = Stages<D>::value;
     using L = Layout<D, STAGES>;
@@ -117,14 +130,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
         (reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Barriers<STAGES> bars;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    int bh, qi;
-    work_item(blockIdx.x, nq, causal != 0, bh, qi);
-    const int q0 = qi * kBM;
-    const int ntiles = causal ? qi + 1 : nq;  // kBM == kBN: the diagonal tile is tile qi
+    const bool masked = causal != 0;
 
     if (tid == 0) {
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
+        mbar_init(&bars.o_empty, kSoftmaxWarps * 32);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
@@ -144,32 +155,47 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
     umma::fence_after_sync();
     const uint32_t tmem = bars.tmem;
 
+    // Every role walks the same items in the same order: units blockIdx.x,
+    // blockIdx.x + gridDim.x, ...; within a unit its query tiles.  Barrier
+    // phases follow item and key-tile counters that run across items, so the
+    // next item's loads and S products start while this one finishes.
     if (warp == kLoadWarp) {
         // ---------------------------------------------------------------- loads
         if (lane == 0) {
             umma::prefetch_tensormap(&map_q);
             umma::prefetch_tensormap(&map_k);
             umma::prefetch_tensormap(&map_v);
-            mbar_arrive_expect_tx(&bars.q_full, L::kTile);
+            int g = 0, it = 0;  // key tiles and items so far
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                int bh, qa, qb;
+                const int cnt = work_unit(u, nq, masked, bh, qa, qb);
+                for (int e = 0; e < cnt; ++e, ++it) {
+                    const int qi = e == 0 ? qa : qb;
+                    const int ntiles = masked ? qi + 1 : nq;
+                    // the Q buffer is free once the previous item's S products completed
+                    if (it > 0) umma::mbar_wait(&bars.q_empty, (it - 1) & 1, ctl);
+                    mbar_arrive_expect_tx(&bars.q_full, L::kTile);
 #pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk)
-                umma::tma_load_3d(smem + L::kQ + blk * L::kBlock, &map_q, 64 * blk, q0, bh,
-                                  &bars.q_full);
-            for (int j = 0; j < ntiles; ++j) {
-                const int st = j % STAGES;
-                const uint32_t reuse_parity = (j / STAGES - 1) & 1;
-                if (j >= STAGES) umma::mbar_wait(&bars.k_empty[st], reuse_parity, ctl);
-                mbar_arrive_expect_tx(&bars.k_full[st], L::kTile);
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        umma::tma_load_3d(smem + L::kQ + blk * L::kBlock, &map_q, 64 * blk,
+                                          qi * kBM, bh, &bars.q_full);
+                    for (int j = 0; j < ntiles; ++j, ++g) {
+                        const int st = g % STAGES;
+                        const uint32_t reuse_parity = (g / STAGES - 1) & 1;
+                        if (g >= STAGES) umma::mbar_wait(&bars.k_empty[st], reuse_parity, ctl);
+                        mbar_arrive_expect_tx(&bars.k_full[st], L::kTile);
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    umma::tma_load_3d(smem + L::kK + st * L::kTile + blk * L::kBlock, &map_k,
-                                      64 * blk, j * kBN, bh, &bars.k_full[st]);
-                if (j >= STAGES) umma::mbar_wait(&bars.v_empty[st], reuse_parity, ctl);
-                mbar_arrive_expect_tx(&bars.v_full[st], L::kTile);
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            umma::tma_load_3d(smem + L::kK + st * L::kTile + blk * L::kBlock, &map_k,
+                                              64 * blk, j * kBN, bh, &bars.k_full[st]);
+                        if (g >= STAGES) umma::mbar_wait(&bars.v_empty[st], reuse_parity, ctl);
+                        mbar_arrive_expect_tx(&bars.v_full[st], L::kTile);
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    umma::tma_load_3d(smem + L::kV + st * L::kTile + blk * L::kBlock, &map_v,
-                                      64 * blk, j * kBN, bh, &bars.v_full[st]);
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            umma::tma_load_3d(smem + L::kV + st * L::kTile + blk * L::kBlock, &map_v,
+                                              64 * blk, j * kBN, bh, &bars.v_full[st]);
+                    }
+                }
             }
         }
     } else if (warp == kMmaSWarp) {
@@ -177,23 +203,34 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
         if (lane == 0) {
             constexpr uint32_t id_s = umma::idesc_bf16(kBM, kBN, false);
             const uint32_t q_addr = smem_addr(smem + L::kQ);
-            umma::mbar_wait(&bars.q_full, 0, ctl);
-            for (int j = 0; j < ntiles; ++j) {
-                const int st = j & 1, ks = j % STAGES;
-                // S buffer st is free once the softmax warps have turned S_{j-2}
-                // into P_{j-2}
-                if (j >= 2) umma::mbar_wait(&bars.p_full[st], ((j - 2) >> 1) & 1, ctl);
-                umma::mbar_wait(&bars.k_full[ks], (j / STAGES) & 1, ctl);
-                umma::fence_after_sync();
-                const uint32_t k_addr = smem_addr(smem + L::kK + ks * L::kTile);
+            int g = 0, it = 0;
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                int bh, qa, qb;
+                const int cnt = work_unit(u, nq, masked, bh, qa, qb);
+                for (int e = 0; e < cnt; ++e, ++it) {
+                    const int qi = e == 0 ? qa : qb;
+                    const int ntiles = masked ? qi + 1 : nq;
+                    umma::mbar_wait(&bars.q_full, it & 1, ctl);
+                    for (int j = 0; j < ntiles; ++j, ++g) {
+                        const int st = g & 1, ks = g % STAGES;
+                        // S buffer st is free once the softmax warps have turned
+                        // S of key tile g - 2 into P
+                        if (g >= 2) umma::mbar_wait(&bars.p_full[st], ((g - 2) >> 1) & 1, ctl);
+                        umma::mbar_wait(&bars.k_full[ks], (g / STAGES) & 1, ctl);
+                        umma::fence_after_sync();
+                        const uint32_t k_addr = smem_addr(smem + L::kK + ks * L::kTile);
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t koff = (s >> 2) * L::kBlock + (s & 3) * 32;
-                    umma::mma_bf16(tmem + st * kTmemS1, umma::desc_sw128(q_addr + koff, 16, 1024),
-                                   umma::desc_sw128(k_addr + koff, 16, 1024), id_s, s > 0);
+                        for (int s = 0; s < D / 16; ++s) {
+                            const uint32_t koff = (s >> 2) * L::kBlock + (s & 3) * 32;
+                            umma::mma_bf16(tmem + st * kTmemS1,
+                                           umma::desc_sw128(q_addr + koff, 16, 1024),
+                                           umma::desc_sw128(k_addr + koff, 16, 1024), id_s, s > 0);
+                        }
+                        umma::commit(&bars.s_full[st]);
+                        umma::commit(&bars.k_empty[ks]);
+                    }
+                    umma::commit(&bars.q_empty);
                 }
-                umma::commit(&bars.s_full[st]);
-                umma::commit(&bars.k_empty[ks]);
             }
         }
     } else if (warp == kMmaPVWarp) {
@@ -202,32 +239,51 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
         // MN-major in shared memory (rows = keys)
         if (lane == 0) {
             constexpr uint32_t id_o = umma::idesc_bf16(kBM, D, true);
-            for (int i = 0; i < ntiles; ++i) {
-                const int b = i & 1, vs = i % STAGES;
-                umma::mbar_wait(&bars.p_full[b], (i >> 1) & 1, ctl);
-                umma::mbar_wait(&bars.v_full[vs], (i / STAGES) & 1, ctl);
-                umma::fence_after_sync();
-                const uint32_t v_addr = smem_addr(smem + L::kV + vs * L::kTile);
+            int g = 0, it = 0;
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                int bh, qa, qb;
+                const int cnt = work_unit(u, nq, masked, bh, qa, qb);
+                for (int e = 0; e < cnt; ++e, ++it) {
+                    const int qi = e == 0 ? qa : qb;
+                    const int ntiles = masked ? qi + 1 : nq;
+                    // O is overwritten by the item's first product: the softmax
+                    // warps must have read the previous item's O
+                    if (it > 0) umma::mbar_wait(&bars.o_empty, (it - 1) & 1, ctl);
+                    for (int j = 0; j < ntiles; ++j, ++g) {
+                        const int b = g & 1, vs = g % STAGES;
+                        umma::mbar_wait(&bars.p_full[b], (g >> 1) & 1, ctl);
+                        umma::mbar_wait(&bars.v_full[vs], (g / STAGES) & 1, ctl);
+                        umma::fence_after_sync();
+                        const uint32_t v_addr = smem_addr(smem + L::kV + vs * L::kTile);
 #pragma unroll
-                for (int s = 0; s < kBN / 16; ++s) {
-                    const uint64_t bd = umma::desc_sw128(v_addr + s * 2048, L::kBlock, 1024);
-                    umma::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + 64 * b + 8 * s, bd, id_o,
-                                          i > 0 || s > 0);
+                        for (int s = 0; s < kBN / 16; ++s) {
+                            const uint64_t bd = umma::desc_sw128(v_addr + s * 2048, L::kBlock, 1024);
+                            umma::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + 64 * b + 8 * s, bd,
+                                                  id_o, j > 0 || s > 0);
+                        }
+                        umma::commit(&bars.pv_done[b]);
+                        umma::commit(&bars.v_empty[vs]);
+                    }
                 }
-                umma::commit(&bars.pv_done[b]);
-                umma::commit(&bars.v_empty[vs]);
             }
         }
     } else {
         // ---------------------------------------------------------------- softmax
         const int r = tid;  // row of the tile == tensor-memory lane
-        const int row_q = q0 + r;
         const uint32_t lane_addr = tmem + (uint32_t(warp * 32) << 16);
+        int g = 0, it = 0;  // key tiles and items so far
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        int bh, qa, qb;
+        const int cnt = work_unit(u, nq, masked, bh, qa, qb);
+        for (int e = 0; e < cnt; ++e, ++it) {
+        const int qi = e == 0 ? qa : qb;
+        const int ntiles = masked ? qi + 1 : nq;
+        const int row_q = qi * kBM + r;
         float m = -INFINITY;  // exponent base, base-2 units of the scaled scores
         float l = 0.f;
-        for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            umma::mbar_wait(&bars.s_full[st], (j >> 1) & 1, ctl);
+        for (int j = 0; j < ntiles; ++j, ++g) {
+            const int st = g & 1;
+            umma::mbar_wait(&bars.s_full[st], (g >> 1) & 1, ctl);
             umma::fence_after_sync();
             float s[kBN];
 #pragma unroll
@@ -304,7 +360,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                 // tcgen05.ld/st are warp-collective: the warp rescales its O
                 // rows (rows that kept their base multiply by 1)
                 if (j > 0) {
-                    umma::mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl);
+                    umma::mbar_wait(&bars.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ctl);
                     umma::fence_after_sync();
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -318,7 +374,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                 }
             }
             l += lsum;
-            if (j >= 2) umma::mbar_wait(&bars.pv_done[st], ((j - 2) >> 1) & 1, ctl);
+            // the P buffer was last read by the P V product of key tile g - 2
+            // (possibly of the previous item)
+            if (g >= 2) umma::mbar_wait(&bars.pv_done[st], ((g - 2) >> 1) & 1, ctl);
             umma::tmem_st32(lane_addr + kTmemP + 64 * st, reinterpret_cast<const float*>(pk));
             umma::tmem_st32(lane_addr + kTmemP + 64 * st + 32, reinterpret_cast<const float*>(pk + 32));
             umma::tmem_wait_st();
@@ -327,29 +385,33 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
         }
 
         // ---------------------------------------------------------------- epilogue
-        const int last = ntiles - 1;
+        // O read into registers, then released to the next item's first P V
+        // product before it is normalised and stored
+        const int last = g - 1;
         umma::mbar_wait(&bars.pv_done[last & 1], (last >> 1) & 1, ctl);
         umma::fence_after_sync();
+        float ov[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) umma::tmem_ld32(lane_addr + kTmemO + 32 * c, ov + 32 * c);
+        umma::tmem_wait_ld();
+        umma::fence_before_sync();
+        umma::mbar_arrive(&bars.o_empty);
         const float inv_l = 1.f / l;
-        __nv_bfloat16* orow = o + (int64_t(bh) * n + row_q) * D;
+        if (row_q < n) {
+            __nv_bfloat16* orow = o + (int64_t(bh) * n + row_q) * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float t[32];
-            umma::tmem_ld32(lane_addr + kTmemO + 32 * c, t);
-            umma::tmem_wait_ld();
-            if (row_q < n) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 w;
-                    w.x = pack_bf16x2(t[8 * v + 0] * inv_l, t[8 * v + 1] * inv_l);
-                    w.y = pack_bf16x2(t[8 * v + 2] * inv_l, t[8 * v + 3] * inv_l);
-                    w.z = pack_bf16x2(t[8 * v + 4] * inv_l, t[8 * v + 5] * inv_l);
-                    w.w = pack_bf16x2(t[8 * v + 6] * inv_l, t[8 * v + 7] * inv_l);
-                    *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = w;
-                }
+            for (int v = 0; v < D / 8; ++v) {
+                uint4 w;
+                w.x = pack_bf16x2(ov[8 * v + 0] * inv_l, ov[8 * v + 1] * inv_l);
+                w.y = pack_bf16x2(ov[8 * v + 2] * inv_l, ov[8 * v + 3] * inv_l);
+                w.z = pack_bf16x2(ov[8 * v + 4] * inv_l, ov[8 * v + 5] * inv_l);
+                w.w = pack_bf16x2(ov[8 * v + 6] * inv_l, ov[8 * v + 7] * inv_l);
+                *reinterpret_cast<uint4*>(orow + 8 * v) = w;
             }
+            if (lse) lse[int64_t(bh) * n + row_q] = (m + __log2f(l)) * kLn2;
         }
-        if (lse && row_q < n) lse[int64_t(bh) * n + row_q] = (m + __log2f(l)) * kLn2;
+        }  // query tiles of the unit
+        }  // units
     }
 
     umma::fence_before_sync();
