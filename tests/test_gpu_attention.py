@@ -134,6 +134,16 @@ def test_rescale_every_tile_increasing_scores(st, causal):
     _full_check(st, q, k, v, causal, label=f"increasing causal={causal}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_items_per_cta(st, d, causal):
+    """More work units than SMs (200 slices of 3 query tiles, the last ragged):
+    every persistent CTA walks several items, so barrier phases and buffers
+    carry over from one item to the next; every row against the oracle."""
+    q, k, v = _rand(200, 259, d, seed=400 + d + int(causal))
+    _full_check(st, q, k, v, causal, label=f"many items d={d} causal={causal}")
+
+
 def test_explicit_scale_and_equal_keys(st):
     """Equal keys: uniform weights, O = mean of the visible values; another
     scale value goes through unchanged."""
