@@ -225,6 +225,30 @@ def test_full_size_workload_sampled_rows(st, causal):
     _check(o_sel, l_sel, ro, rl, aw, sb, seen, f"{w.name} causal={causal}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_ragged_sequence_sampled_rows(st, causal):
+    """A long ragged sequence (n = 16389, 129 query tiles, the last holding 5
+    rows): 64 sampled rows, including both ends and tile edges, against the
+    oracle row by row."""
+    bh, n, d = 2, 16389, 128
+    q, k, v = _rand(bh, n, d, seed=900 + int(causal))
+    o, lse = st.attention(q, k, v, causal=causal)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(31 + int(causal))
+    rows = [0, 127, 128, 8191, 16383, 16384, n - 1]
+    pairs = [(r % bh, r) for r in rows] + [(int(rng.integers(bh)), int(rng.integers(n)))
+                                           for _ in range(64 - len(rows))]
+    sl = np.array([p[0] for p in pairs])
+    rw = np.array([p[1] for p in pairs])
+    k64, v64 = _np(k), _np(v)
+    qsel = _np(q)[sl, rw]
+    ro, rl = oracle.attention_rows(qsel, k64, v64, sl, rw, None, causal)
+    aw, _ = oracle.attention_rows(qsel, k64, np.abs(v64), sl, rw, None, causal)
+    sb, seen = _score_bound(qsel, k64, sl, rw, None, causal)
+    idx = (torch.as_tensor(sl, device="cuda"), torch.as_tensor(rw, device="cuda"))
+    _check(o[idx], lse[idx], ro, rl, aw, sb, seen, f"long n={n} causal={causal}")
+
+
 def test_lse_matches_stats_kernel_on_scores(st):
     """L of a short sequence equals the row log-sum-exp of the scaled score
     matrix computed by the library's own statistics kernel from the same
