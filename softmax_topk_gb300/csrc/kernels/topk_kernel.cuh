@@ -26,9 +26,11 @@
 //     again (about one in a hundred for random data), and their elements at
 //     or above it become the candidates, a warp reserving its slots in the
 //     shared-memory buffer with one atomic;
-//   selection: each candidate's rank is the number of candidates that beat it
-//     (one warp per candidate, the lanes splitting the count); rank r < K puts
-//     it in slot r of the list.  If the candidates overflow the buffer (heavy
+//   selection: up to 256 candidates, each one's rank is the number of
+//     candidates that beat it (one warp per candidate, the lanes splitting the
+//     count) and rank r < K puts it in slot r of the list; more candidates
+//     (large K) are sorted by a CTA-wide bitonic sort of 64-bit keys (logit
+//     order key, then column).  If the candidates overflow the buffer (heavy
 //     ties at the threshold), an exact path finds the K-th largest key of the
 //     segment by bisection and admits the ties at it in column order;
 //   output: the CTA's (m, d) is the (+)-fold of its threads' states.  With
