@@ -1,6 +1,8 @@
 /*
  * os_softmax.h -- C ABI of libos_softmax.so: row-wise online-normalizer
- * softmax and fused softmax+TopK on one NVIDIA GB300 GPU (sm_103a).
+ * softmax and fused softmax+TopK on one NVIDIA GB300 GPU (sm_103a), with the
+ * attention forward that the same (m, d) recurrence carries onto the tensor
+ * cores (os_attention_fwd).
  *
  * Operations (statement of the problem):
  *   softmax : for each row r of x[rows, cols], y[r, i] = e^(x[r,i] - m_r) / d_r
@@ -13,6 +15,8 @@
  *             section 4, "Softmax and top-k fusion": select the K largest
  *             logits u in the normalizer's single pass, then
  *             v_i = e^(u_i - m_r) / d_r).
+ *   attention : softmax(scale Q K^T) V per (batch, head) slice and its
+ *             logsumexp (see os_attention_fwd).
  *
  * Conventions shared by every entry point:
  *   - Pointers are DEVICE pointers into dense row-major buffers (row stride =
