@@ -2,7 +2,7 @@
 // per-row logsumexp, on the fifth-generation tensor cores.
 //
 // What it computes follows "6.2 FlashAttention V2" (section 6.1, forward
-// algorithm): a CTA owns one tile of 128 query rows of one (batch, head) and
+// algorithm): for one tile of 128 query rows of one (batch, head) the kernel
 // walks the key/value tiles of 128 rows, keeping per query row the running
 // maximum m, the running sum l and the unnormalised output; at the end it
 // writes O = O~ / l and L = m + ln l.  The recurrence is the (m, d, o) one of
@@ -11,7 +11,8 @@
 // With the causal mask, query i sees keys j <= i and the key walk stops at the
 // diagonal tile (section 5 of the same page).
 //
-// GB300 mapping (one CTA per query tile, 224 threads, warp-specialised):
+// GB300 mapping (persistent CTAs, one per SM, 224 threads, warp-specialised;
+// each CTA walks work units round-robin, see work_unit):
 //   * warp 4 (one lane) streams the Q tile once and the K/V tiles through a
 //     ring of STAGES buffers with TMA tiled loads (128-byte swizzle, rows past
 //     the sequence end zero-filled by the copy engine);
@@ -28,7 +29,8 @@
 //     memory with tcgen05.st (the A operand of the P V product is read from
 //     there, so P never touches shared memory), and at the end normalise O.
 // S_{j+1} is computed while the softmax warps work on S_j, and P_j V_j runs
-// while they work on S_{j+1}.
+// while they work on S_{j+1}; the next query tile's loads and first S
+// products overlap the end of the current one.
 //
 // Rescaling differs from the pages' every-tile form: the exponent base m is
 // only moved when a tile's maximum exceeds it by more than 2^8 (in the base-2
