@@ -420,13 +420,32 @@ def pin_attention_invariants(lib):
     assert np.allclose(oc[:, n - 1], o[:, n - 1], rtol=1e-12, atol=1e-12)
 
 
+def pin_attention_hard_limit(lib):
+    """With a huge scale the weights become one-hot on each query's best key
+    (distinct scores): O is that key's value row and L the scaled best score,
+    with the mask limiting the keys each query sees."""
+    rng = np.random.default_rng(35)
+    bh, n, dh = 2, 9, 4
+    q, k, v = (rng.normal(size=(bh, n, dh)) for _ in range(3))
+    scale = 1e6
+    for causal in (False, True):
+        o, L = oracle.attention(q, k, v, scale, causal, lib=lib)
+        for b in range(bh):
+            for i in range(n):
+                cnt = i + 1 if causal else n
+                s = k[b, :cnt] @ q[b, i]
+                j = int(np.argmax(s))
+                assert np.allclose(o[b, i], v[b, j], rtol=0, atol=1e-12), (b, i, causal)
+                assert abs(L[b, i] - scale * s[j]) <= 1e-9 * abs(scale * s[j]) + 1e-9
+
+
 PINS = [pin_two_shard_example, pin_identity_element, pin_combine_associative_commutative,
         pin_online_recurrence_equals_definition, pin_normalizer_bound, pin_lesson7_numpy_check,
         pin_closed_forms, pin_shift_invariance, pin_brute_force_tiny_rows, pin_rows_sum_to_one,
         pin_causal_and_spike_rows, pin_topk_exhaustive, pin_topk_ties_lower_index,
         pin_lse_fsum_and_closed_forms, pin_causal_mask_rows, pin_topk_sample_frequencies,
         pin_attention_tiled_recurrence, pin_attention_closed_forms, pin_attention_softmax_times_v,
-        pin_attention_invariants]
+        pin_attention_invariants, pin_attention_hard_limit]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
