@@ -331,7 +331,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
             };
             float mt = -INFINITY, lsum = 0.f;
             bool grow;
-            if (__all_sync(kFullMask, m != -INFINITY)) {
+            const bool speculate = __all_sync(kFullMask, m != -INFINITY);
+            if (speculate) {
                 lsum = exp_pass(m, true, mt);
                 grow = mt * scale_log2 > m + kRescaleLog2;  // scale > 0
             } else {
@@ -356,7 +357,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                 l *= alpha;
                 m = mt2;
             }
-            if (__any_sync(kFullMask, grow)) {
+            if (__any_sync(kFullMask, grow) || !speculate) {  // without a base: the pass runs once
                 float unused;
                 lsum = exp_pass(m == -INFINITY ? 0.f : m, false, unused);
                 // tcgen05.ld/st are warp-collective: the warp rescales its O
