@@ -27,8 +27,9 @@
 //     or above it become the candidates, a warp reserving its slots in the
 //     shared-memory buffer with one atomic;
 //   selection: up to 256 candidates, each one's rank is the number of
-//     candidates that beat it (one warp per candidate, the lanes splitting the
-//     count) and rank r < K puts it in slot r of the list; more candidates
+//     candidates that beat it (one thread per candidate, comparing against
+//     register-held slabs of all candidates by broadcast shuffles) and rank
+//     r < K puts it in slot r of the list; more candidates
 //     (large K) are sorted by a CTA-wide bitonic sort of 64-bit keys (logit
 //     order key, then column).  If the candidates overflow the buffer (heavy
 //     ties at the threshold), an exact path finds the K-th largest key of the
@@ -538,37 +539,32 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             __syncthreads();
         }
 
-        // ---- selection.  Up to kRankMax candidates: list[r] = the candidate
-        // that r candidates beat (r < K).
-        // One warp per candidate, the lanes splitting the count.  The first
-        // 32 * RC candidates are loaded into registers once (lane l holds l,
-        // l + 32, ...) and items are passed around by shuffles, not reread from
-        // shared memory (its round trips are slow while the SM's other CTA
-        // streams).
+        // ---- selection.  Up to kRankMax candidates: thread t ranks candidate
+        // t by counting the candidates that beat it; rank r < K puts it in slot
+        // r of the list.  Each warp holding candidates loads all of them into
+        // registers in one batch (lane l of slab s holds candidate 32 s + l)
+        // and compares against them by broadcast shuffles, so the count is a
+        // few hundred shuffles with no shared-memory round trip in between.
         if (n <= kRankMax) {
-            constexpr int RC = KMAX > 64 ? 16 : 8;  // candidates cached per lane
-            Cand reg[RC];
+            constexpr int SL = kRankMax / 32;  // slabs of 32 candidates
+            if (warp * 32 < n) {               // warp-uniform
+                const Cand mine = tid < n ? sm.cand[tid] : pad;
+                Cand slab[SL];
 #pragma unroll
-            for (int j = 0; j < RC; ++j) reg[j] = lane + 32 * j < n ? sm.cand[lane + 32 * j] : pad;
-            for (int i = warp; i < n; i += NW) {
-                Cand c;
-                if (i < 32 * RC) {
-                    const int slot = i >> 5;  // uniform over the warp
-                    Cand h = reg[0];
-#pragma unroll
-                    for (int j = 1; j < RC; ++j)
-                        if (slot == j) h = reg[j];
-                    c.v = __shfl_sync(kFullMask, h.v, i & 31);
-                    c.j = __shfl_sync(kFullMask, h.j, i & 31);
-                } else {
-                    c = sm.cand[i];
-                }
+                for (int s = 0; s < SL; ++s) slab[s] = 32 * s + lane < n ? sm.cand[32 * s + lane] : pad;
                 int r = 0;
 #pragma unroll
-                for (int j = 0; j < RC; ++j) r += beats(reg[j], c);
-                for (int q = 32 * RC + lane; q < n; q += 32) r += beats(sm.cand[q], c);
-                r = __reduce_add_sync(kFullMask, r);
-                if (lane == 0 && r < K) sm.list[r] = c;
+                for (int s = 0; s < SL; ++s) {
+                    if (32 * s < n) {  // uniform
+#pragma unroll 8
+                        for (int q = 0; q < 32; ++q) {
+                            const float v = __shfl_sync(kFullMask, slab[s].v, q);
+                            const int jj = __shfl_sync(kFullMask, slab[s].j, q);
+                            r += beats(v, jj, mine.v, mine.j);
+                        }
+                    }
+                }
+                if (tid < n && r < K) sm.list[r] = mine;
             }
         } else {
             // more candidates (large K): the K best, best first, by a bitonic
