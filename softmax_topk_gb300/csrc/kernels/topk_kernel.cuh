@@ -23,9 +23,11 @@
 //     many threads of every warp hold one), so nothing below it can be in the
 //     top K;
 //   pass 2 (L2): only the blocks whose key reaches the threshold's are read
-//     again (about one in a hundred for random data), and their elements at
-//     or above it become the candidates, a warp reserving its slots in the
-//     shared-memory buffer with one atomic;
+//     again (about one in a hundred for random data): each warp lists its own
+//     in its share of a shared-memory list and rereads them one per lane (no
+//     CTA barrier in between), and their elements at or above the threshold
+//     become the candidates, a warp reserving its slots in the shared-memory
+//     buffer with one atomic;
 //   selection: up to 256 candidates, each one's rank is the number of
 //     candidates that beat it (one thread per candidate, comparing against
 //     register-held slabs of all candidates by broadcast shuffles) and rank
@@ -405,9 +407,12 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
         for (int w = 1; w < NW; ++w) T = fminf(T, sm.warp_thr[w]);
         const uint32_t tk = threshold_key(T);
 
-        // ---- the blocks whose key reaches T's, listed (one atomic per warp).
-        // The keys are read in one batch: shared-memory round trips are slow
-        // while the SM's other CTA streams.
+        // ---- the blocks whose key reaches T's, listed per warp in the warp's
+        // share of the list, then read again (L2) by the same warp, one block
+        // per lane, their elements >= T becoming the candidates; no CTA barrier
+        // in between.  The keys are read in one batch: shared-memory round
+        // trips are slow while the SM's other CTA streams.
+        constexpr int WCAP = FCAP / NW;  // list entries per warp
         {
             uint32_t hit = 0;  // bit q * U + k: slot k of group q reaches the threshold
 #pragma unroll
@@ -432,76 +437,79 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 const int t = __shfl_up_sync(kFullMask, incl, o);
                 if (lane >= o) incl += t;
             }
-            int base = 0;
-            if (lane == 31 && incl > 0) base = atomicAdd(nflag, incl);
-            int pos = __shfl_sync(kFullMask, base, 31) + incl - mine;
-            for (uint32_t h = hit; h != 0; h &= h - 1) {
-                const int s = __ffs(h) - 1, q = s / U, k = s % U;
-                const int c_end = min(nchunks, (q + 1) * G);
-                for (int c = q * G; c < c_end; ++c) {
-                    const int b = g.b0 + c * CHUNK + k * THREADS + tid;
-                    if (b < g.b1) {
-                        if (pos < FCAP) dyn.flagged[pos] = b;
-                        ++pos;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        const int nf = *nflag;
-
-        // ---- pass 2 (L2): the listed blocks again, one per thread; their
-        // elements >= T are the candidates
-        if (nf <= FCAP) {
-            for (int i0 = 0; i0 < nf; i0 += THREADS) {  // uniform
-                const int i = i0 + tid;
-                float v[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-                int b = 0;
-                uint32_t live = 0;
-                if (i < nf) {
-                    b = dyn.flagged[i];
-                    if (b >= g.full_lo && b < g.full_hi) {
-                        const uint4 w = ld_policy_v4(xb + 4 * int64_t(b), policy);
-                        v[0] = __uint_as_float(w.x);
-                        v[1] = __uint_as_float(w.y);
-                        v[2] = __uint_as_float(w.z);
-                        v[3] = __uint_as_float(w.w);
-                        live = 0xfu;
-                    } else {
-#pragma unroll
-                        for (int l = 0; l < 4; ++l) {
-                            const int64_t col = 4 * int64_t(b) + l - g.head;
-                            const bool in = col >= 0 && col < cols;
-                            if (in) v[l] = g.xr[col];
-                            live |= uint32_t(in) << l;
+            const int wn = __shfl_sync(kFullMask, incl, 31);  // the warp's flagged blocks
+            int* wl = dyn.flagged + warp * WCAP;
+            int pos = incl - mine;
+            if (mine > 0) {
+                for (uint32_t h = hit; h != 0; h &= h - 1) {
+                    const int s = __ffs(h) - 1, q = s / U, k = s % U;
+                    const int c_end = min(nchunks, (q + 1) * G);
+                    for (int c = q * G; c < c_end; ++c) {
+                        const int b = g.b0 + c * CHUNK + k * THREADS + tid;
+                        if (b < g.b1) {
+                            if (pos < WCAP) wl[pos] = b;
+                            ++pos;
                         }
                     }
                 }
-                uint32_t hitmask = 0;  // bit l: element l is a candidate
+            }
+            if (wn > WCAP) {
+                if (lane == 0) atomicOr(nflag, 1);  // this warp's list overflowed
+            } else {
+                __syncwarp();
+                for (int i0 = 0; i0 < wn; i0 += 32) {  // uniform over the warp
+                    const int i = i0 + lane;
+                    float v[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+                    int b = 0;
+                    uint32_t live = 0;
+                    if (i < wn) {
+                        b = wl[i];
+                        if (b >= g.full_lo && b < g.full_hi) {
+                            const uint4 w = ld_policy_v4(xb + 4 * int64_t(b), policy);
+                            v[0] = __uint_as_float(w.x);
+                            v[1] = __uint_as_float(w.y);
+                            v[2] = __uint_as_float(w.z);
+                            v[3] = __uint_as_float(w.w);
+                            live = 0xfu;
+                        } else {
 #pragma unroll
-                for (int l = 0; l < 4; ++l) hitmask |= uint32_t(v[l] >= T) << l;
-                hitmask &= live;
-                const int cnt = __popc(hitmask);
-                int incl = cnt;
+                            for (int l = 0; l < 4; ++l) {
+                                const int64_t col = 4 * int64_t(b) + l - g.head;
+                                const bool in = col >= 0 && col < cols;
+                                if (in) v[l] = g.xr[col];
+                                live |= uint32_t(in) << l;
+                            }
+                        }
+                    }
+                    uint32_t hitmask = 0;  // bit l: element l is a candidate
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int t = __shfl_up_sync(kFullMask, incl, o);
-                    if (lane >= o) incl += t;
-                }
-                int base = 0;
-                if (lane == 31 && incl > 0) base = atomicAdd(counter, incl);
-                int pos = __shfl_sync(kFullMask, base, 31) + incl - cnt;
+                    for (int l = 0; l < 4; ++l) hitmask |= uint32_t(v[l] >= T) << l;
+                    hitmask &= live;
+                    const int cnt = __popc(hitmask);
+                    int cincl = cnt;
 #pragma unroll
-                for (int l = 0; l < 4; ++l) {
-                    if ((hitmask >> l) & 1u) {
-                        if (pos < CAP) sm.cand[pos] = Cand{v[l], int(4u * uint32_t(b) + uint32_t(l) - uint32_t(g.head))};
-                        ++pos;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int t = __shfl_up_sync(kFullMask, cincl, o);
+                        if (lane >= o) cincl += t;
+                    }
+                    int base = 0;
+                    if (lane == 31 && cincl > 0) base = atomicAdd(counter, cincl);
+                    int cpos = __shfl_sync(kFullMask, base, 31) + cincl - cnt;
+#pragma unroll
+                    for (int l = 0; l < 4; ++l) {
+                        if ((hitmask >> l) & 1u) {
+                            if (cpos < CAP)
+                                sm.cand[cpos] = Cand{v[l], int(4u * uint32_t(b) + uint32_t(l) -
+                                                              uint32_t(g.head))};
+                            ++cpos;
+                        }
                     }
                 }
             }
         }
         __syncthreads();
-        int n = nf <= FCAP ? *counter : CAP + 1;
+        // a warp whose list overflowed sends the row to the exact path
+        int n = *nflag == 0 ? *counter : CAP + 1;
 
         if (n > CAP) {
             // ---- exact path (heavy ties at T; rare): the K-th largest key of the

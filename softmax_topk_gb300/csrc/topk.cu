@@ -15,7 +15,7 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkVpt = 4;      // 16-byte blocks per thread per chunk
 constexpr int kTopkCap = 2048;   // candidates
 constexpr int kTopkGroups = 4;   // block keys kept per thread slot (groups of chunks)
-constexpr int kTopkFcap = 2048;  // blocks read again in pass 2
+constexpr int kTopkFcap = 4096;  // blocks read again in pass 2 (256 per warp)
 constexpr int kTopkDynBytes =
     int(sizeof(TopkDynSmem<kTopkThreads, kTopkVpt, kTopkGroups, kTopkFcap>));
 // Two builds: K <= 64 with clusters of up to 8 CTAs per row, and
