@@ -31,9 +31,12 @@
 //   selection: up to 256 candidates, each one's rank is the number of
 //     candidates that beat it (one thread per candidate, comparing against
 //     register-held slabs of all candidates by broadcast shuffles) and rank
-//     r < K puts it in slot r of the list; more candidates
-//     (large K) are sorted by a CTA-wide bitonic sort of 64-bit keys (logit
-//     order key, then column).  If the candidates overflow the buffer (heavy
+//     r < K puts it in slot r of the list; more candidates are first cut to
+//     the K best by a radix select on their order keys (four 8-bit digit
+//     rounds, the lowest columns taken among ties at the K-th key) when
+//     K <= 64, and sorted whole by a CTA-wide bitonic sort of 64-bit keys
+//     (logit order key, then column) for larger K.  If the candidates
+//     overflow the buffer (heavy
 //     ties at the threshold), an exact path finds the K-th largest key of the
 //     segment by bisection and admits the ties at it in column order;
 //   output: the CTA's (m, d) is the (+)-fold of its threads' states.  With
@@ -69,8 +72,8 @@ struct __align__(8) Cand {
 };
 
 constexpr int kNoIndex = INT_MAX;
-// Candidate counts up to this are ranked by counting (n^2 / 32 comparisons
-// per warp); more are sorted (bitonic, log^2 n stages).
+// Candidate counts up to this are ranked by counting; more are cut to the K
+// best by a radix select (K <= 64) or sorted (larger K).
 constexpr int kRankMax = 256;
 
 __device__ __forceinline__ bool beats(float v1, int j1, float v2, int j2) {
@@ -196,6 +199,95 @@ __device__ __forceinline__ void bitonic_select(Cand* cand, int n, Cand* list, in
     }
 }
 
+// The K best of the n candidates cand[0..n) (K <= n <= THREADS * EMAX, by
+// "beats"), moved unordered into cand[0..K).  A radix select finds the K-th
+// largest order key (four rounds of 8-bit digits, histograms in shared
+// memory), then the candidates above it and the lowest-column ties at it are
+// compacted into out[0..K) and copied back.  work: at least 256 + 8 ints of
+// shared memory; out: room for K candidates.  Every thread of the CTA must
+// call it.
+template <int THREADS, int EMAX>
+__device__ __forceinline__ void radix_select_compact(Cand* cand, int n, int K, int* work, Cand* out) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    int* hist = work;             // 256 bins
+    int* ctl = work + 256;        // [0] digit, [1] count above it, [2] > count, [3] tie count
+    uint32_t key[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int i = e * THREADS + tid;
+        key[e] = i < n ? order_key(cand[i].v + 0.0f) : 0u;  // -0 keyed as +0, as beats() compares
+    }
+    uint32_t prefix = 0, mask = 0;
+    int kleft = K;  // how many still to take among the keys matching the prefix
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += THREADS) hist[b] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            const int i = e * THREADS + tid;
+            if (i < n && (key[e] & mask) == prefix) atomicAdd(&hist[(key[e] >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (tid < 32) {  // the digit holding the kleft-th largest key: lane l scans bins 8 l .. 8 l + 7
+            int c[8], s = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                c[q] = hist[8 * lane + q];
+                s += c[q];
+            }
+            int x = s;  // inclusive suffix sum over lanes lane .. 31
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_down_sync(kFullMask, x, o);
+                if (lane + o < 32) x += v;
+            }
+            int run = x - s;  // keys in the bins of higher lanes
+#pragma unroll
+            for (int q = 7; q >= 0; --q) {
+                if (run < kleft && run + c[q] >= kleft) {
+                    ctl[0] = 8 * lane + q;
+                    ctl[1] = run;
+                }
+                run += c[q];
+            }
+        }
+        __syncthreads();
+        const uint32_t d = uint32_t(ctl[0]);
+        kleft -= ctl[1];
+        prefix |= d << shift;
+        mask |= 255u << shift;
+        __syncthreads();  // ctl is rewritten next round
+    }
+    // prefix is the K-th largest key; K - kleft candidates lie above it and
+    // kleft of its ties (the lowest columns) complete the K
+    if (tid == 0) {
+        ctl[2] = 0;
+        ctl[3] = 0;
+    }
+    __syncthreads();
+    const int n_gt = K - kleft;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int i = e * THREADS + tid;
+        if (i < n && key[e] > prefix) out[atomicAdd(&ctl[2], 1)] = cand[i];
+    }
+    // ties at the K-th key: each counts the ties with a lower column
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int i = e * THREADS + tid;
+        if (i < n && key[e] == prefix) {
+            const int j = cand[i].j;
+            int lower = 0;
+            for (int q = 0; q < n; ++q)
+                lower += order_key(cand[q].v + 0.0f) == prefix && cand[q].j < j;
+            if (lower < kleft) out[n_gt + lower] = cand[i];
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < K; i += THREADS) cand[i] = out[i];
+    __syncthreads();
+}
+
 template <int THREADS>
 __device__ __forceinline__ int block_sum(int v, int* scratch) {
     v = __reduce_add_sync(kFullMask, v);
@@ -281,7 +373,8 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                  int64_t rows, int cols, int K, int S, KernelCtl ctl) {
     constexpr int NW = THREADS / 32;
     constexpr int CHUNK = THREADS * U;  // 16-byte blocks per chunk
-    static_assert(CAP % THREADS == 0 && CAP >= 128 && KMAX <= THREADS, "buffer sizes");
+    static_assert(CAP % THREADS == 0 && CAP >= 128 && KMAX <= THREADS && KMAX <= kRankMax,
+                  "buffer sizes");
     __shared__ __align__(16) TopkSmem<THREADS, KMAX, CAP, MAXC> sm;
     extern __shared__ __align__(16) unsigned char dyn_raw[];
     auto& dyn = *reinterpret_cast<TopkDynSmem<THREADS, U, GROUPS, FCAP>*>(dyn_raw);
@@ -547,13 +640,22 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             __syncthreads();
         }
 
-        // ---- selection.  Up to kRankMax candidates: thread t ranks candidate
-        // t by counting the candidates that beat it; rank r < K puts it in slot
-        // r of the list.  Each warp holding candidates loads all of them into
+        // ---- selection.  More than kRankMax candidates are sorted (the large-K
+        // build) or first cut to the K best by a radix select on their order
+        // keys (K <= 64).  Up to kRankMax, thread t ranks candidate t by
+        // counting the candidates that beat it; rank r < K puts it in slot r
+        // of the list.  Each warp holding candidates loads all of them into
         // registers in one batch (lane l of slab s holds candidate 32 s + l)
         // and compares against them by broadcast shuffles, so the count is a
         // few hundred shuffles with no shared-memory round trip in between.
-        if (n <= kRankMax) {
+        if constexpr (KMAX <= 64) {
+            if (n > kRankMax) {  // uniform
+                radix_select_compact<THREADS, CAP / THREADS>(sm.cand, n, K, dyn.flagged + 1024,
+                                                             reinterpret_cast<Cand*>(dyn.flagged));
+                n = K;
+            }
+        }
+        if (n <= kRankMax) {  // uniform
             constexpr int SL = kRankMax / 32;  // slabs of 32 candidates
             if (warp * 32 < n) {               // warp-uniform
                 const Cand mine = tid < n ? sm.cand[tid] : pad;
@@ -574,9 +676,9 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 }
                 if (tid < n && r < K) sm.list[r] = mine;
             }
-        } else {
-            // more candidates (large K): the K best, best first, by a bitonic
-            // sort; zeros come back as +0 and take their sign from the row
+        } else if constexpr (KMAX > 64) {
+            // K up to 256: a bitonic sort of all candidates gives the list
+            // (zeros come back as +0 and take their sign from the row)
             bitonic_select<THREADS, CAP / THREADS>(sm.cand, n, sm.list, K);
             __syncthreads();
             if (tid < K && tid < n && sm.list[tid].v == 0.f) sm.list[tid].v = g.xr[sm.list[tid].j];

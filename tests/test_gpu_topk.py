@@ -168,11 +168,12 @@ def test_plain_topk_ties_and_inf(st):
         _run_plain(st, x, K, f"plain ties K={K}")
 
 
-@pytest.mark.parametrize("K", [200, 256])
+@pytest.mark.parametrize("K", [8, 64, 200, 256])
 def test_sorted_selection_zero_ties(st, K):
-    """More candidates than the counting rank takes (the sort path): rows of
-    -|x| with 600 zeros, half of them -0.0, so the K best are all zeros, tied,
-    and must come in column order with their own sign bits."""
+    """More candidates than the counting rank takes (the radix cut for K <= 64,
+    the sort above): rows of -|x| with 600 zeros, half of them -0.0, so the K
+    best are all zeros, tied at the K-th key, and must be the lowest columns,
+    in column order, with their own sign bits."""
     g = torch.Generator(device="cuda")
     g.manual_seed(17)
     rows, cols = 4, 20000
