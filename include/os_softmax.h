@@ -31,8 +31,11 @@
  *     probability exactly +0; a row whose entries are ALL -inf has no defined
  *     softmax and its outputs are unspecified (NaN in practice).
  *   - Arithmetic: fp32 throughout (bf16 inputs widened exactly, fp32
- *     accumulation, bf16 outputs rounded to nearest even).  The exponential is
- *     the library's own fp32 routine on the FMA pipe (no ex2.approx).
+ *     accumulation, bf16 outputs rounded to nearest even).  Per-element
+ *     exponentials are e^(x - m) = 2^(x log2e - M_hi) (1 - M_lo ln 2) with
+ *     the SFU's 2^x (ex2.approx) and m log2e = M_hi + M_lo split exactly by
+ *     an FMA; a value that carries a whole row (a merge's rescale factor, a
+ *     TopK output value) uses the library's own exponential (os_exp_f32).
  *   - Work runs on the device current at the call (cudaGetDevice); the
  *     pointers and the stream must belong to it.  There is no CPU fallback.
  */
@@ -236,10 +239,13 @@ os_status os_softmax_plan(int64_t rows, int64_t cols, os_dtype in_dtype, os_dtyp
 os_status os_topk_plan(int64_t rows, int64_t cols, int32_t K, os_plan *plan);
 
 /*
- * out[i] = e^(z[i]) for n fp32 values with the library's own exponential, the
- * routine every kernel above uses (Cody-Waite reduction z = n ln2 + r, a
- * degree-6 minimax polynomial for e^r, 2^n written into the exponent field;
- * no ex2.approx).  Defined for z <= 88: within about 1 ulp of e^z for
+ * out[i] = e^(z[i]) for n fp32 values with the library's own exponential
+ * (Cody-Waite reduction z = n ln2 + r, a degree-6 minimax polynomial for e^r,
+ * 2^n written into the exponent field; no ex2.approx).  The kernels above use
+ * it where one value carries a whole row (the rescale factors of the merges,
+ * the TopK output values); their per-element exponentials are the SFU's
+ * 2^x with the maximum split into a high part and an FMA residual.  Defined
+ * for z <= 88: within about 1 ulp of e^z for
  * z >= -87.33, 0 or a value below FLT_MIN for smaller z, exactly +0 for
  * z = -inf.  Exposed so the routine can be tested on its own.
  *   z, out  device pointers to n fp32 values (may be the same buffer).
