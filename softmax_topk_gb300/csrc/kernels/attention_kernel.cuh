@@ -117,6 +117,13 @@ __device__ __forceinline__ int work_unit(int u, int nq, bool causal, int& bh, in
     return qa == qb ? 1 : 2;
 }
 
+// 32 bytes to global memory in one store (p 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                    "r"(w[6]), "r"(w[7]) : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -401,15 +408,30 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
         umma::mbar_arrive(&bars.o_empty);
         const float inv_l = 1.f / l;
         if (row_q < n) {
+            // one row per thread: 32-byte stores when O is 32-byte aligned
+            // (rows are D * 2 bytes, so then every row is), else 16-byte ones;
+            // each warp-wide store touches 32 rows, so fewer, wider stores
+            // shorten this tail of the item
             __nv_bfloat16* orow = o + (int64_t(bh) * n + row_q) * D;
+            if ((reinterpret_cast<uintptr_t>(o) & 31) == 0) {
 #pragma unroll
-            for (int v = 0; v < D / 8; ++v) {
-                uint4 w;
-                w.x = pack_bf16x2(ov[8 * v + 0] * inv_l, ov[8 * v + 1] * inv_l);
-                w.y = pack_bf16x2(ov[8 * v + 2] * inv_l, ov[8 * v + 3] * inv_l);
-                w.z = pack_bf16x2(ov[8 * v + 4] * inv_l, ov[8 * v + 5] * inv_l);
-                w.w = pack_bf16x2(ov[8 * v + 6] * inv_l, ov[8 * v + 7] * inv_l);
-                *reinterpret_cast<uint4*>(orow + 8 * v) = w;
+                for (int v = 0; v < D / 16; ++v) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        w[c] = pack_bf16x2(ov[16 * v + 2 * c] * inv_l, ov[16 * v + 2 * c + 1] * inv_l);
+                    st_global_v8(orow + 16 * v, w);
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < D / 8; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16x2(ov[8 * v + 0] * inv_l, ov[8 * v + 1] * inv_l);
+                    w.y = pack_bf16x2(ov[8 * v + 2] * inv_l, ov[8 * v + 3] * inv_l);
+                    w.z = pack_bf16x2(ov[8 * v + 4] * inv_l, ov[8 * v + 5] * inv_l);
+                    w.w = pack_bf16x2(ov[8 * v + 6] * inv_l, ov[8 * v + 7] * inv_l);
+                    *reinterpret_cast<uint4*>(orow + 8 * v) = w;
+                }
             }
             if (lse) lse[int64_t(bh) * n + row_q] = (m + __log2f(l)) * kLn2;
         }

@@ -174,18 +174,21 @@ def test_four_dim_tensors(st):
     assert torch.equal(o.view(6, 200, 64), o_ref) and torch.equal(lse.view(6, 200), l_ref)
 
 
-def test_output_does_not_touch_neighbours(st):
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("start", [4096, 4104])
+def test_output_does_not_touch_neighbours(st, d, start):
     """Outputs written into the middle of a larger buffer leave the guard
-    regions on both sides untouched (ragged n)."""
-    bh, n, d = 3, 131, 64
+    regions on both sides untouched (ragged n); the output starts 32-byte
+    aligned (wide row stores) or only 16-byte aligned (start = 4104 bf16)."""
+    bh, n = 3, 131
     q, k, v = _rand(bh, n, d, seed=13)
-    big = torch.full((bh * n * d + 2 * 4096,), 7.0, device="cuda", dtype=torch.bfloat16)
-    out = big[4096:4096 + bh * n * d].view(bh, n, d)
+    big = torch.full((bh * n * d + 2 * 4096 + 8,), 7.0, device="cuda", dtype=torch.bfloat16)
+    out = big[start:start + bh * n * d].view(bh, n, d)
     lbig = torch.full((bh * n + 2 * 64,), -3.0, device="cuda", dtype=torch.float32)
     lout = lbig[64:64 + bh * n].view(bh, n)
     st.attention(q, k, v, out=out, lse=lout)
     torch.cuda.synchronize()
-    assert torch.all(big[:4096] == 7.0) and torch.all(big[4096 + bh * n * d:] == 7.0)
+    assert torch.all(big[:start] == 7.0) and torch.all(big[start + bh * n * d:] == 7.0)
     assert torch.all(lbig[:64] == -3.0) and torch.all(lbig[64 + bh * n:] == -3.0)
     q64, k64, v64 = _np(q), _np(k), _np(v)
     ro, rl = oracle.attention(q64, k64, v64)
