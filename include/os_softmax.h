@@ -32,10 +32,11 @@
  *     softmax and its outputs are unspecified (NaN in practice).
  *   - Arithmetic: fp32 throughout (bf16 inputs widened exactly, fp32
  *     accumulation, bf16 outputs rounded to nearest even).  Per-element
- *     exponentials are e^(x - m) = 2^(x log2e - M_hi) (1 - M_lo ln 2) with
- *     the SFU's 2^x (ex2.approx) and m log2e = M_hi + M_lo split exactly by
- *     an FMA; a value that carries a whole row (a merge's rescale factor, a
- *     TopK output value) uses the library's own exponential (os_exp_f32).
+ *     exponentials are the SFU's 2^x (ex2.approx) of (x - m) log2 e, with
+ *     log2 e carried in two fp32 parts where the output is fp32 (the TopK
+ *     normaliser instead splits m log2 e exactly with an FMA residual); a
+ *     value that carries a whole row (a merge's rescale factor, a TopK
+ *     output value) uses the library's own exponential (os_exp_f32).
  *   - Work runs on the device current at the call (cudaGetDevice); the
  *     pointers and the stream must belong to it.  There is no CPU fallback.
  */
