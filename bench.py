@@ -633,9 +633,21 @@ def cpu_baseline(target_seconds: float) -> dict:
     if t < target_seconds / 4:  # grow the sample toward the target CPU time
         frac = min(1.0, frac * target_seconds / max(t, 1e-3) / 2)
         t, b, desc = oracle_sample_run(frac, target_seconds=target_seconds / 2)
-    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(t, 2),
-            "sample": f"{desc} (fraction {frac:.5f} of each step workload's rows)"}
+    out = {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+           "kind": "oracle", "seconds": round(t, 2),
+           "sample": f"{desc} (fraction {frac:.5f} of each step workload's rows)"}
+    # the same oracle on one host thread, on a smaller sample of the same rows
+    cores = oracle.num_threads()
+    frac1 = frac / max(1, cores)
+    oracle.set_num_threads(1)
+    try:
+        t1, b1, desc1 = oracle_sample_run(frac1, target_seconds=target_seconds / 4)
+    finally:
+        oracle.set_num_threads(cores)
+    out["single_thread"] = {"value": round(b1 / t1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                            "seconds": round(t1, 2),
+                            "sample": f"{desc1} (fraction {frac1:.6f} of each step workload's rows)"}
+    return out
 
 
 def run_reference(args):

@@ -62,6 +62,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     """Load the oracle library (or another build of the same source at ``path``)."""
     lib = ctypes.CDLL(path or build())
     lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
     lib.oracle_row_stats_f64.argtypes = [_dbl_p, _dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64]
     lib.oracle_softmax_f64.argtypes = [_dbl_p, _dbl_p, ctypes.c_int64, ctypes.c_int64]
     lib.oracle_online_stats_f64.argtypes = [_dbl_p, ctypes.c_int64, _dbl_p, _dbl_p]
@@ -107,6 +108,12 @@ def _p(a: np.ndarray, t=_dbl_p):
 
 def num_threads(lib: ctypes.CDLL | None = None) -> int:
     return (lib or _get()).oracle_num_threads()
+
+
+def set_num_threads(n: int, lib: ctypes.CDLL | None = None) -> None:
+    """Threads of the oracle's row loops from now on (timing only: the
+    arithmetic of a row does not depend on it)."""
+    (lib or _get()).oracle_set_num_threads(int(n))
 
 
 def softmax(x, lib: ctypes.CDLL | None = None) -> np.ndarray:

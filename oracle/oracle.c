@@ -58,6 +58,16 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads of the row loops from now on (n >= 1); no effect on the arithmetic
+ * of a row.  A build without OpenMP always runs one. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* (m, d) of one row by definition: first the maximum, then the shifted sum. */
 static void row_stats(const double *x, int64_t n, double *m_out, double *d_out) {
     double m = -INFINITY;

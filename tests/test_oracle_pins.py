@@ -464,6 +464,25 @@ def test_oracle_threads_reported():
     assert oracle.num_threads() >= 1
 
 
+def test_oracle_results_do_not_depend_on_threads():
+    """Rows are independent: one thread and the default count give the same
+    bits (the single-thread timing in the bench runs the same arithmetic)."""
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((37, 1001)) * 3.0
+    x[5, 100:200] = -np.inf
+    cores = oracle.num_threads()
+    ref_y, ref_tk = oracle.softmax(x), oracle.topk(x, 9)
+    oracle.set_num_threads(1)
+    try:
+        assert oracle.num_threads() == 1 or cores == 1
+        y, tk = oracle.softmax(x), oracle.topk(x, 9)
+    finally:
+        oracle.set_num_threads(cores)
+    assert oracle.num_threads() == cores
+    assert np.array_equal(y, ref_y)
+    assert np.array_equal(tk[0], ref_tk[0]) and np.array_equal(tk[1], ref_tk[1])
+
+
 def test_exhaustive_helper_itself():
     # the helper is tested on a case small enough to check by hand
     assert _exhaustive_topk([1.0, 3.0, 3.0, 2.0], 4) == [1, 2, 3, 0]
