@@ -19,8 +19,8 @@ output inside the timed region), `roofline` of the dominant kernel,
 `cpu_baseline` (the float64 oracle on the host cores on a bounded sample),
 `clocks` (nvidia-smi samples taken during the timed region).
 
-`--impl reference` times the oracle alone (the reference arm of this build:
-the method's own definition run on the host cores), on the same metric.
+`--impl reference` times the oracle alone (the reference arm: the method's
+own definition run on the host cores), on the same metric.
 """
 from __future__ import annotations
 

@@ -31,7 +31,7 @@
  *              section 4, "Softmax and top-k fusion": select on the logits u,
  *              then v = e^(u - m_V) / d_V).  Selection is a full sort of the
  *              row by (x descending, index ascending); the pages leave ties
- *              open and this build breaks them toward the lower index.
+ *              open, and they go to the lower index.
  *   attention: softmax(scale Q K^T) V and L = m + ln d per query row, with
  *              an optional causal mask (see oracle_attention_f64).
  *

@@ -256,7 +256,7 @@ __device__ __forceinline__ void radix_select_compact(Cand* cand, int n, int K, i
         kleft -= ctl[1];
         prefix |= d << shift;
         mask |= 255u << shift;
-        __syncthreads();  // ctl is rewritten next round
+        __syncthreads();  // ctl is rewritten by the next digit round
     }
     // prefix is the K-th largest key; K - kleft candidates lie above it and
     // kleft of its ties (the lowest columns) complete the K

@@ -22,7 +22,7 @@ Attention (batch x heads x seq_len x head_dim, Q, K, V bf16, all N(0, 1)):
                                 with and without the causal mask
   attention_1x2x300x64_bf16     small case for the oracle (ragged tile),     seed 1008
 
-Readings of the workload text (each is listed with its reason in the design doc):
+Readings of the workload text:
   * "N(0, s)": s is the standard deviation, x = s * randn.
   * "4 spikes at +40 at random positions": row r gets one spike in each quarter
     of its columns, at a uniformly drawn offset inside the quarter, so the 4
