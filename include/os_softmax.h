@@ -102,7 +102,9 @@ typedef struct {
  * y = softmax(x) row by row.
  *   x         device pointer, rows*cols elements of in_dtype, read only.
  *   y         device pointer, rows*cols elements of out_dtype, written.
- *             Must not overlap x (OS_ERR_ALIAS).
+ *             Either y == x with out_dtype == in_dtype (in place: x is
+ *             overwritten by its softmax) or no overlap with x at all; any
+ *             other overlap is OS_ERR_ALIAS.
  *   in_dtype, out_dtype: OS_F32 or OS_BF16, in any combination.
  * Pointers must be aligned to their element size (OS_ERR_ALIGN); 16-byte
  * alignment of both and cols a multiple of 16/sizeof(in) give 128-bit access.

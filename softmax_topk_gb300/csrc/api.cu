@@ -101,7 +101,11 @@ os_status softmax_entry(const void* x, void* y, int64_t rows, int64_t cols, os_d
     if (reinterpret_cast<uintptr_t>(x) % elem_bytes(in) ||
         reinterpret_cast<uintptr_t>(y) % elem_bytes(out))
         return OS_ERR_ALIGN;
-    if (overlaps(x, rows * cols * elem_bytes(in), y, rows * cols * elem_bytes(out)))
+    // exactly in place (y == x, one dtype) is allowed: every kernel family
+    // reads each element of a row before the same thread or CTA writes it;
+    // any other overlap is not
+    const bool in_place = x == y && in == out;
+    if (!in_place && overlaps(x, rows * cols * elem_bytes(in), y, rows * cols * elem_bytes(out)))
         return OS_ERR_ALIAS;
     if (period > 0) {
         const int64_t nv = (cols + elems_per_vector(in) - 1) / elems_per_vector(in);

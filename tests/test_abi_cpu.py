@@ -71,7 +71,8 @@ def test_softmax_argument_errors(lib):
     assert f(A, None, 4, 8, F32, F32, 0, None) == NULL
     assert f(A + 2, B, 4, 8, F32, F32, 0, None) == ALIGN
     assert f(A, B + 1, 4, 8, F32, BF16, 0, None) == ALIGN
-    assert f(A, A, 4, 8, F32, F32, 0, None) == ALIAS
+    assert f(A, A + 4, 4, 8, F32, F32, 0, None) == ALIAS          # shifted by one element
+    assert f(A, A, 4, 8, F32, BF16, 0, None) == ALIAS             # in place needs one dtype
     assert f(A, A + 4 * 31, 4, 8, F32, F32, 0, None) == ALIAS     # last element shared
     # rows == 0 is a no-op, even with NULL pointers
     assert f(None, None, 0, 8, F32, F32, 0, None) == OK
@@ -127,7 +128,8 @@ def test_causal_argument_errors(lib):
     assert f(A, B, 4, 8, 4, -1, F32, F32, None) == SHAPE
     assert f(A, B, 4, 8, 4, 0, 2, F32, None) == DTYPE
     assert f(None, B, 4, 8, 4, 0, F32, F32, None) == NULL
-    assert f(A, A, 4, 8, 4, 0, F32, F32, None) == ALIAS
+    assert f(A, A + 4, 4, 8, 4, 0, F32, F32, None) == ALIAS
+    assert f(A, A, 4, 8, 4, 0, BF16, F32, None) == ALIAS
     assert f(None, None, 0, 8, 4, 0, F32, F32, None) == OK
 
 

@@ -71,6 +71,47 @@ def test_cols_sweep_forced_path(st, cols, path, pair):
     _check(st, x, pair[1], path, f"{path} {pair} cols={cols}")
 
 
+@pytest.mark.parametrize("cols", [7, 64, 1000, 4097, 8193, 32000, 50257, 131073, 262145])
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_in_place_matches_out_of_place(st, cols, path, dt):
+    """y == x with one dtype: the input is overwritten with exactly the bits
+    the same kernel writes to a separate output."""
+    rows = 3 if cols > 100000 else 9
+    x = _inputs(rows, cols, dt, seed=cols + 29)
+    try:
+        ref = st.softmax(x, path=path)
+    except st.OsError as e:
+        if e.name == "OS_ERR_PATH":
+            pytest.skip(f"{path} cannot hold {tuple(x.shape)}")
+        raise
+    z = x.clone()
+    y = st.softmax(z, path=path, out=z)
+    torch.cuda.synchronize()
+    assert y.data_ptr() == z.data_ptr()
+    assert torch.equal(z, ref), f"in place differs: {path} {dt} cols={cols}"
+
+
+@pytest.mark.parametrize("cols", [4096, 16384, 32000, 131072])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_in_place_persistent_many_rows(st, cols, dt):
+    """In place with more rows than resident CTAs (persistent CTAs and
+    clusters walk several rows; the bulk-copy ring prefetches later rows
+    while earlier ones are written), AUTO path, and the causal variant."""
+    rows = 700
+    x = _inputs(rows, cols, dt, seed=cols + 31)
+    ref = st.softmax(x)
+    z = x.clone()
+    st.softmax(z, out=z)
+    torch.cuda.synchronize()
+    assert torch.equal(z, ref)
+    ref_c = st.softmax_causal(x, period=333, offset=5)
+    z = x.clone()
+    st.softmax_causal(z, period=333, offset=5, out=z)
+    torch.cuda.synchronize()
+    assert torch.equal(z, ref_c)
+
+
 SOFTMAX_WORKLOADS = [n for n, w in workloads.WORKLOADS.items() if w.op == "softmax"]
 
 
@@ -246,7 +287,7 @@ def test_plans_of_the_workloads(st):
 def test_bad_calls_raise(st):
     x = torch.randn(4, 100, device="cuda")
     with pytest.raises(st.OsError) as e:
-        st.os_softmax_fwd(x.data_ptr(), x.data_ptr(), 4, 100, 0, 0, None)
+        st.os_softmax_fwd(x.data_ptr(), x.data_ptr() + 4, 4, 100, 0, 0, None)
     assert e.value.name == "OS_ERR_ALIAS"
     with pytest.raises(st.OsError) as e:
         st.softmax(torch.randn(2, 5000, device="cuda"), path="warp")
