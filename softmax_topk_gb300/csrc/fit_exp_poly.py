@@ -1,5 +1,7 @@
-"""Derivation of the polynomial used by the library's accurate fp32 exponential
-(exp1 in kernels/ops.cuh: os_exp_f32, merge rescale factors, TopK values).
+"""Derivation of the polynomials of the library's fp32 exponentials in
+kernels/ops.cuh: e^r for exp1 (os_exp_f32, merge rescale factors, TopK
+values), and 2^f for the per-element exponentials of fp32 softmax results
+(exp_pair, second part of this file).
 
 The kernels evaluate e^z as 2^n * p(r) with n = rint(z * log2 e) and
 r = z - n ln2 (Cody & Waite, "Software Manual for the Elementary Functions",
@@ -25,9 +27,9 @@ A = 0.3466 + 2e-4
 DEGREE = 6
 
 
-def lawson_fit(degree: int, iters: int = 60):
-    r = np.cos(np.linspace(0.0, np.pi, 4001)) * A
-    f = np.exp(r)
+def lawson_fit(degree: int, iters: int = 60, fn=np.exp, half_width: float = A):
+    r = np.cos(np.linspace(0.0, np.pi, 4001)) * half_width
+    f = fn(r)
     basis = np.stack([r ** k for k in range(1, degree + 1)], axis=1) / f[:, None]
     target = (f - 1.0) / f
     w = np.ones_like(r)
@@ -40,9 +42,21 @@ def lawson_fit(degree: int, iters: int = 60):
     return np.concatenate([[1.0], c]), float(err.max())
 
 
+# 2^f on [-1/2, 1/2] (the per-element exponential of fp32 results):
+# e^z = 2^n 2^f with n = rint(z log2 e) and f = z log2 e - n, so the fit is of
+# 2^f itself, again relative and with p(0) = 1 exactly; degree 5 gives about
+# 9e-8 (1.1e-7 once the coefficients are rounded to fp32).
+DEGREE_2F = 5
+
+
 if __name__ == "__main__":
     coeffs, err = lawson_fit(DEGREE)
-    print(f"degree {DEGREE}: max relative error {err:.3e}")
+    print(f"e^r, degree {DEGREE}: max relative error {err:.3e}")
     for k, c in enumerate(coeffs):
         c32 = np.float32(c)
         print(f"c{k} = {c32!r}  (0x{int(c32.view(np.uint32)):08x})")
+    coeffs, err = lawson_fit(DEGREE_2F, iters=80, fn=np.exp2, half_width=0.5)
+    print(f"2^f, degree {DEGREE_2F}: max relative error {err:.3e}")
+    for k, c in enumerate(coeffs):
+        c32 = np.float32(c)
+        print(f"e{k} = {c32!r}  (0x{int(c32.view(np.uint32)):08x})")

@@ -118,35 +118,73 @@ __device__ __forceinline__ float exp1(float z) {
     return p * pow2_from_rounded(t);
 }
 
-// ------------------------------------------------------------------ exp (SFU)
-// The streaming loops take e^z as 2^(z log2 e) with the special-function
-// unit's base-2 exponential (PTX ex2.approx.ftz.f32): one SFU instruction
-// per element and two FMA-pipe operations per pair, against the dozen of the
-// polynomial above.  Blackwell Ultra doubled the SFU's ex2 rate for exactly
-// this use, which leaves these kernels bound by HBM instead of by issue.
-// ex2 maps -inf to +0, NaN to NaN, and flushes results below 2^-126 to +0.
-// Error of e^z: the product t = z log2 e is rounded once (relative error of
-// the result <= 2^-24 |z|); the accurate form splits log2 e into two fp32
-// constants so that the constant's own rounding adds nothing; ex2 adds a few
-// ulp.  The softmax tests bound the result over z in [-87, 0].
+// ------------------------------------------------------------------ exp (pairs)
+// The per-element exponentials of the softmax passes, the two lanes of a
+// packed f32x2 at a time.
+//
+// fp32 results of the two-pass streaming kernel: on the FMA pipe only, no
+// ex2.approx (exp_pair_fma):
+//   n  = rint(z log2e)                 u = z log2e + 1.5*2^23 (one FMA)
+//   f  = (z log2e - n) + z log2e_lo    two FMAs; |f| <= 1/2 plus ~2e-6
+//   p  = 1 + f (e1 + f (e2 + ...))     2^f, degree-5 minimax fit on [-1/2, 1/2]
+//   e^z = p * 2^n                      2^n from u's bits (integer multiply-add)
+// z is clamped to >= -88 first (-inf included): then n >= -127, and n = -127
+// makes 2^n exactly +0, so e^-inf = +0 and results below 2^-126 are zero or
+// tiny.  log2 e is carried as kLog2e + kLog2eLo, so the reduced argument is
+// accurate to about 2^-25 whatever |z|, and the relative error of e^z is the
+// polynomial's (1.1e-7 with its fp32 coefficients, from
+// csrc/fit_exp_poly.py) plus the rounding of its evaluation.
+//
+// Everything else (results rounded to bf16 afterwards; the register,
+// on-chip and statistics kernels): the special-function unit's 2^x (PTX
+// ex2.approx.ftz.f32; -inf -> +0, results below 2^-126 -> +0), a few ulp of
+// fp32.  The polynomial costs about ten FMA-pipe instructions per pair
+// against two SFU instructions: measured, a quarter of the throughput of the
+// bf16 streaming kernel (eight elements per 16-byte vector, an exponential
+// per element in each pass) and of the on-chip kernel on 4096-column rows,
+// and nothing on fp32 streaming rows.
+namespace expc {
+constexpr float kLog2eLo = 1.925963034e-08f;  // log2 e - kLog2e
+constexpr float kZFloor = -88.0f;             // z log2 e <= -126.96: n = -127, 2^n = +0
+// 2^f = 1 + f (e1 + f (e2 + ...)), max relative error 1.1e-7
+constexpr float e5_1 = 0.693147f, e5_2 = 0.24022242f, e5_3 = 0.055507336f,
+                e5_4 = 0.009671513f, e5_5 = 0.0013264726f;
+}  // namespace expc
+
 __device__ __forceinline__ float ex2_sfu(float t) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
     return r;
 }
 
-namespace expc {
-constexpr float kLog2eLo = 1.925963034e-08f;  // log2 e - kLog2e
-}  // namespace expc
-
-// e^z of a pair: accurate (FAST = false, fp32 results) or with log2 e rounded
-// to fp32 (FAST = true, for results rounded to bf16 afterwards).
+// e^z of a pair on the SFU: accurate (FAST = false: log2 e carried in two
+// fp32 parts, for fp32 results) or with log2 e rounded to fp32 (FAST = true,
+// for results rounded to bf16 afterwards).  Error of e^z: the product t =
+// z log2 e rounded once (2^-24 |z| relative) plus ex2's few ulp.
 template <bool FAST>
 __device__ __forceinline__ float2 exp_pair(float2 z) {
     float2 t;
     if constexpr (FAST) t = mul2(z, splat2(expc::kLog2e));
     else t = fma2(z, splat2(expc::kLog2e), mul2(z, splat2(expc::kLog2eLo)));
     return make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
+}
+
+// e^z of a pair (z <= 0, -inf allowed) on the FMA pipe, no ex2.approx: the
+// polynomial form described above, for fp32 results of the two-pass
+// streaming kernel (and the three-pass baseline measured against it).
+__device__ __forceinline__ float2 exp_pair_fma(float2 z) {
+    using namespace expc;
+    z = make_float2(fmaxf(z.x, kZFloor), fmaxf(z.y, kZFloor));
+    const float2 u = fma2(z, splat2(kLog2e), splat2(kRound));
+    const float2 neg_n = fma2(u, splat2(-1.0f), splat2(kRound));  // exact
+    float2 f = fma2(z, splat2(kLog2e), neg_n);
+    f = fma2(z, splat2(kLog2eLo), f);
+    float2 p = fma2(splat2(e5_5), f, splat2(e5_4));
+    p = fma2(p, f, splat2(e5_3));
+    p = fma2(p, f, splat2(e5_2));
+    p = fma2(p, f, splat2(e5_1));
+    p = fma2(p, f, splat2(1.0f));
+    return mul2(p, make_float2(pow2_from_rounded(u.x), pow2_from_rounded(u.y)));
 }
 
 // e^z / d of a pair for bf16 results, folded into one exponent:

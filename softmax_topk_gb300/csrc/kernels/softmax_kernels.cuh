@@ -582,12 +582,17 @@ __device__ __forceinline__ void store_stream_chunk(TO* ys, int c, int len, int b
     }
 }
 
-// sum over N entries of e^(z_i), z given
-template <int N, bool FAST>
+// sum over N entries of e^(z_i), z given: on the SFU (exp_pair<FAST>), or on
+// the FMA pipe without ex2.approx (FMA_EXP, for fp32 results of the
+// two-pass streaming kernel and the three-pass baseline)
+template <int N, bool FAST, bool FMA_EXP = false>
 __device__ __forceinline__ float exp_sum_z(const float* z) {
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < N; i += 2) acc = add2(acc, exp_pair<FAST>(make_float2(z[i], z[i + 1])));
+    for (int i = 0; i < N; i += 2) {
+        const float2 zz = make_float2(z[i], z[i + 1]);
+        acc = add2(acc, FMA_EXP ? exp_pair_fma(zz) : exp_pair<FAST>(zz));
+    }
     return acc.x + acc.y;
 }
 
@@ -604,7 +609,8 @@ __device__ __forceinline__ float exp_sum_z(const float* z) {
 // memory by the thread that loaded them, and pass 2 takes them from there.
 // With one CTA per row there is no exchange between SMs at all: each row
 // costs one __syncthreads-level merge.
-// bf16 outputs fold 1/d into the exponent (one FMA and one ex2 per element).
+// bf16 outputs fold 1/d into the exponent (2^(z log2 e - log2 d), one
+// exponential per element).
 // ALIGNED (rows start on 16-byte boundaries) selects 128-bit loads and stores;
 // otherwise the same register layout is filled element by element.  Chunks
 // lying wholly inside the CTA's range skip the per-vector range checks.
@@ -653,7 +659,7 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
             const float m_new = fmaxf(m, ch.max());
             float z[EPC];
             ch.shifted(m_new, z);
-            d = d * rescale(m, m_new) + exp_sum_z<EPC, FAST>(z);
+            d = d * rescale(m, m_new) + exp_sum_z<EPC, FAST, !FAST>(z);
             m = m_new;
         }
         const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m, d, parity, rank);
@@ -674,7 +680,7 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
             for (int i = 0; i < EPC; i += 2) {
                 const float2 z = make_float2(e[i], e[i + 1]);
                 const float2 p = FAST ? exp_pair_div(z, neg_log2_d)
-                                      : mul2(exp_pair<false>(z), inv_d);
+                                      : mul2(exp_pair_fma(z), inv_d);
                 e[i] = p.x;
                 e[i + 1] = p.y;
             }
@@ -735,7 +741,7 @@ safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
                                                             int(threadIdx.x));
             float z[EPC];
             ch.shifted(m, z);
-            d += exp_sum_z<EPC, FAST>(z);
+            d += exp_sum_z<EPC, FAST, !FAST>(z);
         }
         d = block_reduce(d, false);
         const float2 inv_d = splat2(1.0f / d);
@@ -749,7 +755,7 @@ safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
 #pragma unroll
             for (int i = 0; i < EPC; i += 2) {
                 const float2 z = make_float2(e[i], e[i + 1]);
-                const float2 p = FAST ? exp_pair_div(z, neg_log2_d) : mul2(exp_pair<false>(z), inv_d);
+                const float2 p = FAST ? exp_pair_div(z, neg_log2_d) : mul2(exp_pair_fma(z), inv_d);
                 e[i] = p.x;
                 e[i + 1] = p.y;
             }
