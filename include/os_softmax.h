@@ -32,11 +32,13 @@
  *     softmax and its outputs are unspecified (NaN in practice).
  *   - Arithmetic: fp32 throughout (bf16 inputs widened exactly, fp32
  *     accumulation, bf16 outputs rounded to nearest even).  Per-element
- *     exponentials are the SFU's 2^x (ex2.approx) of (x - m) log2 e, with
- *     log2 e carried in two fp32 parts where the output is fp32 (the TopK
- *     normaliser instead splits m log2 e exactly with an FMA residual); a
- *     value that carries a whole row (a merge's rescale factor, a TopK
- *     output value) uses the library's own exponential (os_exp_f32).
+ *     exponentials: fp32 results of the two-pass streaming kernel use the
+ *     library's own FMA-pipe exponential (no ex2.approx: base-2 reduction
+ *     and a degree-5 polynomial); bf16 results and the register, on-chip,
+ *     statistics and TopK kernels use the SFU's 2^x (ex2.approx) of
+ *     (x - m) log2 e, log2 e in two fp32 parts for fp32 results.  A value
+ *     that carries a whole row (a merge's rescale factor, a TopK output
+ *     value) uses the library's accurate exponential (os_exp_f32).
  *   - Work runs on the device current at the call (cudaGetDevice); the
  *     pointers and the stream must belong to it.  There is no CPU fallback.
  */
