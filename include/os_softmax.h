@@ -258,6 +258,19 @@ os_status os_topk_plan(int64_t rows, int64_t cols, int32_t K, os_plan *plan);
 os_status os_exp_f32(const float *z, float *out, int64_t n, os_stream_t stream);
 
 /*
+ * out[i] = e^(z[i]) for n fp32 values with the per-element exponential of the
+ * two-pass streaming kernel's fp32 results: two values at a time on packed
+ * fp32 FMAs, no ex2.approx (n = rint(z log2 e), f = z log2 e - n with log2 e
+ * in two fp32 parts, a degree-5 minimax polynomial for 2^f, 2^n written
+ * into the exponent field).  Defined for z <= 0, the softmax domain
+ * x - max: within 3e-7 relative of e^z for z >= -87.33, 0 or a value below
+ * FLT_MIN for smaller z, exactly +0 for z = -inf and exactly 1 for z = 0.
+ * Exposed so the routine can be tested on its own; arguments and checks as
+ * os_exp_f32 (n may be odd).
+ */
+os_status os_exp_pairs_f32(const float *z, float *out, int64_t n, os_stream_t stream);
+
+/*
  * Device-side waits.  Kernels that stage rows in shared memory wait on
  * hardware barriers for their bulk copies; every such wait is bounded (by
  * default 1 s).  A wait that gives up does not hang or fault the GPU: the

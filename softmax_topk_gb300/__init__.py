@@ -3,7 +3,7 @@
 The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
 ``os_softmax_fwd``, ``os_softmax_topk``, ``os_topk``, ``os_softmax_causal_fwd``,
 ``os_softmax_stats``, ``os_topk_sample``, ``os_attention_fwd``, ``os_softmax_fwd_path``,
-``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_device_status``,
+``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_exp_pairs_f32``, ``os_device_status``,
 ``os_set_wait_timeout_ns``, ``os_set_fault_injection``, ``os_status_string``.  They take raw
 device pointers (ints) and a raw stream handle, exactly like the C functions,
 and raise ``OsError`` on a non-OK status.
@@ -72,6 +72,7 @@ def _load() -> ctypes.CDLL:
     lib.os_softmax_plan.argtypes = [i64, i64, st, st, st, ctypes.POINTER(Plan)]
     lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
     lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
+    lib.os_exp_pairs_f32.argtypes = [vp, vp, i64, vp]
     lib.os_device_status.argtypes = [vp]
     lib.os_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.os_set_fault_injection.argtypes = [i32]
@@ -80,7 +81,8 @@ def _load() -> ctypes.CDLL:
     for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_topk",
                  "os_softmax_causal_fwd", "os_softmax_stats", "os_topk_sample", "os_attention_fwd",
                  "os_softmax_plan",
-                 "os_topk_plan", "os_exp_f32", "os_device_status", "os_set_wait_timeout_ns",
+                 "os_topk_plan", "os_exp_f32", "os_exp_pairs_f32", "os_device_status",
+                 "os_set_wait_timeout_ns",
                  "os_set_fault_injection"):
         getattr(lib, name).restype = st
     return lib
@@ -144,6 +146,10 @@ def os_attention_fwd(q: int, k: int, v: int, o: int, lse: int | None, bh: int, n
 
 def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
     _check(_lib.os_exp_f32(z, out, n, stream), "os_exp_f32")
+
+
+def os_exp_pairs_f32(z: int, out: int, n: int, stream: int | None) -> None:
+    _check(_lib.os_exp_pairs_f32(z, out, n, stream), "os_exp_pairs_f32")
 
 
 def os_device_status(stream: int | None) -> None:
@@ -329,14 +335,17 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     return out, lse
 
 
-def exp(z):
-    """e^z elementwise (fp32 CUDA tensor) with the library's own exponential."""
+def exp(z, pairs: bool = False):
+    """e^z elementwise (fp32 CUDA tensor) with the library's own exponential:
+    the accurate scalar routine, or (pairs=True, z <= 0) the per-element
+    exponential of the streaming kernel's fp32 results."""
     import torch
     if not z.is_cuda or z.dtype != torch.float32 or not z.is_contiguous():
         raise ValueError("z must be a contiguous float32 CUDA tensor")
     out = torch.empty_like(z)
+    fn = os_exp_pairs_f32 if pairs else os_exp_f32
     with _OnDevice(z.device):
-        os_exp_f32(z.data_ptr(), out.data_ptr(), z.numel(), _stream_handle(z))
+        fn(z.data_ptr(), out.data_ptr(), z.numel(), _stream_handle(z))
     return out
 
 

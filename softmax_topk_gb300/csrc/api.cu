@@ -291,6 +291,16 @@ os_status os_exp_f32(const float* z, float* out, int64_t n, os_stream_t stream) 
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
 }
 
+os_status os_exp_pairs_f32(const float* z, float* out, int64_t n, os_stream_t stream) {
+    if (n < 0) return OS_ERR_SHAPE;
+    if (n == 0) return OS_OK;
+    if (!z || !out) return OS_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(z) % 4 || reinterpret_cast<uintptr_t>(out) % 4)
+        return OS_ERR_ALIGN;
+    const cudaError_t e = os::launch_exp_pairs(z, out, n, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
+}
+
 os_status os_device_status(os_stream_t stream) {
     unsigned int* word = status_word();
     if (!word) return OS_ERR_CUDA;

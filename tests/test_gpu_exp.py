@@ -1,4 +1,6 @@
-"""The library's own fp32 exponential against float64 exp and CUDA's expf."""
+"""The library's own fp32 exponentials against float64 exp and CUDA's expf:
+the accurate scalar routine (os_exp_f32) and the per-element exponential of
+the streaming kernel's fp32 results (os_exp_pairs_f32)."""
 import numpy as np
 import pytest
 import torch
@@ -56,3 +58,36 @@ def test_in_place(st):
     ref = st.exp(z)
     st.os_exp_f32(z.data_ptr(), z.data_ptr(), z.numel(), torch.cuda.current_stream().cuda_stream)
     assert torch.equal(z, ref)
+
+
+def test_pairs_error_bound_on_the_softmax_domain(st):
+    """The streaming kernel's exponential: degree-5 fit (1.1e-7) plus the
+    rounding of its evaluation, within 3e-7 relative on z in [-87.33, 0]."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    z = torch.cat([-torch.rand(1 << 22, generator=g, device="cuda") * 87.33,
+                   -torch.rand(1 << 20, generator=g, device="cuda") * 2.0,
+                   -torch.rand(1 << 16, generator=g, device="cuda") * 1e-3,
+                   torch.linspace(-87.33, 0.0, (1 << 20) + 1, device="cuda")])
+    got = st.exp(z, pairs=True)
+    torch.cuda.synchronize()
+    z64 = z.double().cpu().numpy()
+    want = np.exp(z64)
+    rel = np.abs(got.cpu().numpy().astype(np.float64) - want) / want
+    assert rel.max() <= 3e-7, f"max rel {rel.max():.3e} at z={z64[np.argmax(rel)]}"
+
+
+def test_pairs_special_values_and_odd_length(st):
+    z = torch.tensor([0.0, -0.0, -np.inf, -88.0, -87.5, -100.0, -1e30, -87.33, -1.0],
+                     device="cuda")  # odd length: the last value is paired with 0
+    got = st.exp(z, pairs=True).cpu().numpy()
+    assert got[0] == 1.0 and got[1] == 1.0
+    assert got[2] == 0.0 and not np.signbit(got[2])
+    assert 0.0 <= got[3] <= FLT_MIN and 0.0 <= got[4] <= FLT_MIN
+    assert got[5] == 0.0 and got[6] == 0.0
+    assert got[7] >= FLT_MIN
+    assert abs(float(got[8]) - np.exp(-1.0)) <= 3e-7 * np.exp(-1.0)
+    w = -torch.rand(1001, device="cuda") * 50
+    ref = st.exp(w, pairs=True)
+    st.os_exp_pairs_f32(w.data_ptr(), w.data_ptr(), w.numel(), torch.cuda.current_stream().cuda_stream)
+    assert torch.equal(w, ref)
