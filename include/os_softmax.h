@@ -192,7 +192,6 @@ os_status os_softmax_stats(const void *x, float *m, float *d, float *lse, int64_
 os_status os_topk_sample(const float *vals, const int32_t *idx, const float *u, int32_t *out,
                          int64_t rows, int32_t K, os_stream_t stream);
 
-/* Human-readable name of a status code (static string, never NULL). */
 /* Attention forward on the tensor cores ("6.2 FlashAttention V2", section 6.1,
  * forward algorithm; the (m, d, o) recurrence of the "Online normalizer
  * calculation for softmax" notes, FlashAttention section):
@@ -218,6 +217,7 @@ os_status os_attention_fwd(const void *q, const void *k, const void *v, void *o,
                            int64_t bh, int64_t n, int32_t head_dim, float scale, int32_t causal,
                            os_stream_t stream);
 
+/* Human-readable name of a status code (static string, never NULL). */
 const char *os_status_string(os_status status);
 
 /*
