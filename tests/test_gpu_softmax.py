@@ -92,6 +92,29 @@ def test_in_place_matches_out_of_place(st, cols, path, dt):
     assert torch.equal(z, ref), f"in place differs: {path} {dt} cols={cols}"
 
 
+@pytest.mark.parametrize("cols", [100, 3001, 32000, 131073])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_in_place_unaligned_rows(st, cols, dt):
+    """In place on a buffer that starts one element past a 16-byte boundary
+    (rows filled element by element), every path that holds the shape."""
+    rows = 5
+    src = _inputs(rows, cols, dt, seed=cols + 37)
+    for path in PATHS:
+        buf = torch.zeros(rows * cols + 8, dtype=src.dtype, device="cuda")
+        x = buf[1:1 + rows * cols].view(rows, cols)
+        x.copy_(src)
+        try:
+            ref = st.softmax(x, path=path)
+        except st.OsError as e:
+            if e.name == "OS_ERR_PATH":
+                continue
+            raise
+        st.softmax(x, path=path, out=x)
+        torch.cuda.synchronize()
+        assert torch.equal(x, ref), f"in place differs: {path} {dt} cols={cols} (unaligned)"
+        assert torch.all(buf[:1] == 0) and torch.all(buf[1 + rows * cols:] == 0)
+
+
 @pytest.mark.parametrize("cols", [4096, 16384, 32000, 131072])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_in_place_persistent_many_rows(st, cols, dt):
