@@ -130,6 +130,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
         self.path = tempfile.mktemp(suffix=".csv")
         self.proc = None
         try:
@@ -141,6 +142,29 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    @staticmethod
+    def _parse(lines) -> list:
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        return rows
+
+    def _query_once(self) -> list:
+        try:
+            out = subprocess.run(["nvidia-smi", f"--id={self.gpu_index}",
+                                  f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits"],
+                                 capture_output=True, text=True, timeout=30).stdout
+        except (OSError, subprocess.TimeoutExpired):
+            return []
+        return self._parse(out.splitlines())
+
     def stop(self, t0: float, t1: float) -> dict | None:
         if self.proc is None:
             return None
@@ -150,22 +174,15 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                try:
-                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
-                except ValueError:
-                    continue
+            rows = self._parse(f)
         os.unlink(self.path)
         inside = [r for r in rows if t0 - 1 <= r[0] <= t1 + 1]
         window = "timed region"
         if not inside:
             inside, window = rows, "whole run"
+        if not inside:  # a timed region shorter than the sampling period
+            inside, window = self._query_once(), "right after the timed region"
         if not inside:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
