@@ -135,3 +135,21 @@ def test_causal_argument_errors(st):
             st.os_softmax_causal_fwd(x.data_ptr(), y.data_ptr(), 4, 64, period, offset,
                                      st.OS_F32, st.OS_F32, None)
         assert e.value.name == "OS_ERR_SHAPE"
+
+
+def test_stats_outputs_do_not_touch_neighbours(st):
+    """m, d and lse written into the middle of guard-filled buffers (warp and
+    CTA families): the guard bands stay untouched."""
+    G = 512
+    for rows, cols, dtype in ((300, 700, "f32"), (50, 40000, "bf16")):
+        x = _inputs(rows, cols, dtype, seed=cols)
+        bufs = [torch.full((rows + 2 * G,), 3.5, device="cuda") for _ in range(3)]
+        m, d, lse = (b[G:G + rows] for b in bufs)
+        st.os_softmax_stats(x.data_ptr(), m.data_ptr(), d.data_ptr(), lse.data_ptr(), rows, cols,
+                            st.OS_F32 if dtype == "f32" else st.OS_BF16,
+                            torch.cuda.current_stream().cuda_stream)
+        rm, rd, rl = st.softmax_stats(x)
+        torch.cuda.synchronize()
+        for b in bufs:
+            assert torch.all(b[:G] == 3.5) and torch.all(b[G + rows:] == 3.5)
+        assert torch.equal(m, rm) and torch.equal(d, rd) and torch.equal(lse, rl)

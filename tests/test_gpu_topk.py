@@ -236,3 +236,33 @@ def test_topk_sample_frequencies(st):
                           torch.tensor([[5, 6, 7]] * 2, dtype=torch.int32, device="cuda"),
                           torch.tensor([0.0, 1.0], device="cuda"))
     assert edge.tolist() == [6, 7]
+
+
+@pytest.mark.parametrize("K", [8, 64, 256])
+def test_outputs_do_not_touch_neighbours(st, K):
+    """vals and idx written into the middle of guard-filled buffers (fused
+    and plain TopK, several rows per CTA and clusters), then the sampler's
+    output likewise: the guard bands stay untouched and the results match
+    a run into fresh buffers."""
+    G = 1024
+    for rows, cols in ((3, 300007), (40, 50257), (700, 3001)):
+        x = _rand(rows, cols, seed=rows * 7 + K)
+        for fn in (st.os_softmax_topk, st.os_topk):
+            vb = torch.full((rows * K + 2 * G,), 7.0, device="cuda")
+            ib = torch.full((rows * K + 2 * G,), -5, dtype=torch.int32, device="cuda")
+            vals, idx = vb[G:G + rows * K], ib[G:G + rows * K]
+            fn(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, cols, K,
+               torch.cuda.current_stream().cuda_stream)
+            ref_v, ref_i = (st.softmax_topk(x, K) if fn is st.os_softmax_topk else st.topk(x, K))
+            torch.cuda.synchronize()
+            assert torch.all(vb[:G] == 7.0) and torch.all(vb[G + rows * K:] == 7.0)
+            assert torch.all(ib[:G] == -5) and torch.all(ib[G + rows * K:] == -5)
+            assert torch.equal(vals.view(rows, K), ref_v) and torch.equal(idx.view(rows, K), ref_i)
+        vals, idx = st.softmax_topk(x, K)
+        u = torch.rand(rows, device="cuda")
+        ob = torch.full((rows + 2 * G,), -9, dtype=torch.int32, device="cuda")
+        out = ob[G:G + rows]
+        st.topk_sample(vals, idx, u, out=out)
+        torch.cuda.synchronize()
+        assert torch.all(ob[:G] == -9) and torch.all(ob[G + rows:] == -9)
+        assert torch.equal(out, st.topk_sample(vals, idx, u))
