@@ -153,7 +153,7 @@ warp_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
     const int lane_in_row = threadIdx.x % L;
     const int64_t warp = (int64_t(blockIdx.x) * THREADS + threadIdx.x) / 32;
     const int64_t nwarps = int64_t(gridDim.x) * THREADS / 32;
-    const int64_t nv = (cols + EPV - 1) / EPV;
+    const int64_t nv = (int64_t(cols) + EPV - 1) / EPV;
 
     for (int64_t base = warp * RPW; base < rows; base += nwarps * RPW) {
         const int64_t row = base + (threadIdx.x % 32) / L;
@@ -247,7 +247,7 @@ onchip_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
     __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
-    const int64_t nv = (cols + EPV - 1) / EPV;
+    const int64_t nv = (int64_t(cols) + EPV - 1) / EPV;
     const int64_t v0 = int64_t(rank) * THREADS * VPT + threadIdx.x;
     if (CLUSTER > 1) cluster_sync();  // every CTA of the cluster is running before DSMEM use
 
@@ -362,7 +362,7 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
-    const int slice = ((cols + CLUSTER - 1) / CLUSTER + EPV - 1) / EPV * EPV;
+    const int slice = int(((int64_t(cols) + CLUSTER - 1) / CLUSTER + EPV - 1) / EPV * EPV);
     const int begin = int(rank) * slice;
     const int len = max(0, min(cols - begin, slice));
     const uint32_t bytes = uint32_t(len) * uint32_t(sizeof(TI));
@@ -525,7 +525,9 @@ struct VecLimits {
 };
 template <int EPV>
 __device__ __forceinline__ VecLimits vec_limits(int len, int begin, int lim) {
-    return {min(len, max(0, lim / EPV - begin)), min(len, max(0, (lim + EPV - 1) / EPV - begin))};
+    // (lim + EPV - 1) / EPV in 64 bits: lim can be 2^31 - 1
+    const int lim_v = int((int64_t(lim) + EPV - 1) / EPV);
+    return {min(len, max(0, lim / EPV - begin)), min(len, max(0, lim_v - begin))};
 }
 
 // Vectors t + k*GROUP (k < UNROLL) of chunk c of a CTA's range that starts
@@ -626,7 +628,7 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
     extern __shared__ uint4 kept[];  // [NS][UNROLL][THREADS]: the row's first chunks, raw
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
-    const int nv = (cols + EPV - 1) / EPV;
+    const int nv = int((int64_t(cols) + EPV - 1) / EPV);  // cols can be 2^31 - 1
     const int per_cta = (nv + CLUSTER - 1) / CLUSTER;
     const int begin = int(rank) * per_cta;
     const int len = max(0, min(per_cta, nv - begin));  // vectors of this CTA
@@ -704,7 +706,7 @@ safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int
     constexpr int STEP = THREADS * UNROLL;
     __shared__ float red[2][NW];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int len = (cols + EPV - 1) / EPV;
+    const int len = int((int64_t(cols) + EPV - 1) / EPV);  // cols can be 2^31 - 1
     const int nchunks = (len + STEP - 1) / STEP;
     const uint64_t normal = l2_policy_evict_normal();
     int rb = 0;  // alternate reduction buffers: one barrier per reduction
@@ -782,7 +784,7 @@ stats_rows_kernel(const TI* __restrict__ x, float* __restrict__ m_out, float* __
     const int t = int(threadIdx.x) % GROUP;
     const int64_t g0 = int64_t(blockIdx.x) * GPC + threadIdx.x / GROUP;
     const int64_t ng = int64_t(gridDim.x) * GPC;
-    const int len = (cols + EPV - 1) / EPV;
+    const int len = int((int64_t(cols) + EPV - 1) / EPV);  // cols can be 2^31 - 1
     const int nchunks = (len + STEP - 1) / STEP;
     const VecLimits vl = vec_limits<EPV>(len, 0, cols);
     const uint64_t policy = l2_policy_evict_first();  // read once

@@ -617,24 +617,26 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             for (int bit = 31; bit >= 0; --bit) {
                 const uint32_t probe = t | (1u << bit);
                 int cnt = 0;
-                for (int e = c_lo + tid; e < c_hi; e += THREADS) cnt += order_key(xr[e]) >= probe;
+                // 64-bit element indices: c_hi can be 2^31 - 1, and e + THREADS must not wrap
+                for (int64_t e = int64_t(c_lo) + tid; e < c_hi; e += THREADS)
+                    cnt += order_key(xr[e]) >= probe;
                 if (block_sum<THREADS>(cnt, sm.scratch) >= need) t = probe;
             }
             int admitted = 0;
-            for (int base = c_lo; base < c_hi; base += THREADS) {
-                const int e = base + tid;
+            for (int64_t base = c_lo; base < c_hi; base += THREADS) {
+                const int64_t e = base + tid;
                 const bool above = e < c_hi && order_key(xr[e]) > t;
                 int round_total = 0;
                 const int p = admitted + block_exclusive_scan<THREADS>(above, sm.scratch, round_total);
-                if (above) sm.cand[p] = Cand{xr[e], e};
+                if (above) sm.cand[p] = Cand{xr[e], int(e)};
                 admitted += round_total;
             }
-            for (int base = c_lo; base < c_hi && admitted < need; base += THREADS) {  // uniform
-                const int e = base + tid;
+            for (int64_t base = c_lo; base < c_hi && admitted < need; base += THREADS) {  // uniform
+                const int64_t e = base + tid;
                 const bool tie = e < c_hi && order_key(xr[e]) == t;
                 int round_total = 0;
                 const int p = admitted + block_exclusive_scan<THREADS>(tie, sm.scratch, round_total);
-                if (tie && p < need) sm.cand[p] = Cand{xr[e], e};
+                if (tie && p < need) sm.cand[p] = Cand{xr[e], int(e)};
                 admitted += round_total;
             }
             n = need;
