@@ -277,15 +277,24 @@ os_status os_exp_pairs_f32(const float *z, float *out, int64_t n, os_stream_t st
  * kernel finishes with garbage in the affected outputs and records the event
  * in a per-device status word.
  *
- * os_device_status synchronises `stream`, then returns OS_ERR_TIMEOUT if any
- * kernel of this library on the current device gave up a wait since the
- * previous call (and clears the word), OS_OK otherwise.
+ * os_device_status reads and clears the word in one atomic exchange (a
+ * one-thread kernel on `stream`), synchronises `stream`, and returns
+ * OS_ERR_TIMEOUT if any kernel of this library on the current device gave up
+ * a wait since the previous call, OS_OK otherwise.  A kernel on another stream
+ * that records a timeout concurrently is reported by this call or the next,
+ * never lost.  Host callers are serialised inside the call.
+ *
+ * Two bounds apply.  The data wait (a copy or a peer's message that a CTA
+ * needs before it can go on) is bounded by os_set_wait_timeout_ns.  The drain
+ * wait (a CTA whose data wait gave up waits, before it exits, for its own
+ * bulk copies still in flight so none lands after it has gone) has its own
+ * fixed bound of 4 s, which no setting shortens.
  */
 os_status os_device_status(os_stream_t stream);
 
 /*
  * Testing controls, process-wide, read at every launch.
- *   os_set_wait_timeout_ns: bound of each device-side wait, 1 us .. 10 s
+ *   os_set_wait_timeout_ns: bound of each device-side data wait, 1 ms .. 10 s
  *     (OS_ERR_SHAPE outside that range).
  *   os_set_fault_injection: 0 = off (default); 1 = in every following launch
  *     one CTA withholds data that another CTA waits for, so that wait must run

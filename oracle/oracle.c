@@ -126,23 +126,25 @@ void oracle_causal_mask_f64(const double *x, double *out, int64_t rows, int64_t 
             out[r * cols + c] = c > (r % period) + offset ? -INFINITY : x[r * cols + c];
 }
 
-/* Top-K sampling from the K (value, index) pairs of each row (values >= 0):
- * the smallest k with p_0 + ... + p_k > u (p_0 + ... + p_{K-1}), the sums in
- * index order; when no k qualifies (u >= 1) the last one.  The drawn column
- * idx[r*K + k] goes to out[r].  The decision is an integer taken from floating
- * point, so it is taken in the library's precision: every partial sum and the
- * product with u rounded to fp32 (the values and u are fp32 numbers). */
+/* Top-K sampling from the K (value, index) pairs of each row (values >= 0),
+ * by the inverse of the cumulative distribution of the renormalised values:
+ * the smallest k with p_0 + ... + p_k > u (p_0 + ... + p_{K-1}), the partial
+ * sums taken in index order in double; when no k qualifies (u >= 1) the last
+ * one.  The drawn column idx[r*K + k] goes to out[r].  ("Online normalizer
+ * calculation for softmax" (notes), section 4, names sampling from the top-K
+ * probabilities as the consumer of the fused pass; the draw itself is this
+ * plain definition.) */
 void oracle_topk_sample_f64(const double *vals, const int32_t *idx, const double *u,
                             int32_t *out, int64_t rows, int32_t K) {
     for (int64_t r = 0; r < rows; ++r) {
         const double *p = vals + r * K;
-        volatile float total = 0.0f;
-        for (int32_t k = 0; k < K; ++k) total = total + (float)p[k];
-        volatile float target = (float)u[r] * total;
+        double total = 0.0;
+        for (int32_t k = 0; k < K; ++k) total += p[k];
+        const double target = u[r] * total;
         int32_t pick = K - 1;
-        volatile float run = 0.0f;
+        double run = 0.0;
         for (int32_t k = 0; k < K; ++k) {
-            run = run + (float)p[k];
+            run += p[k];
             if (run > target) {
                 pick = k;
                 break;

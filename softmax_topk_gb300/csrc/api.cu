@@ -8,9 +8,18 @@
 #include "internal.h"
 
 // Device status word (one per device the library runs on): kernels OR in
-// os::kErrWaitTimeout when a bounded wait gives up.  Read and cleared by
-// os_device_status.
+// os::kErrWaitTimeout when a bounded wait gives up.  Read and cleared in one
+// atomic exchange by os_device_status, whose result lands in the second word.
 __device__ unsigned int os_device_status_word;
+__device__ unsigned int os_device_status_taken;
+
+// The status word's value at the moment it is cleared: a timeout recorded by a
+// kernel on another stream lands either before the exchange (and is reported
+// now) or after it (and is reported by the next call), never lost between a
+// read and a separate clear.
+__global__ void status_exchange_kernel() {
+    os_device_status_taken = atomicExch(&os_device_status_word, 0u);
+}
 
 namespace {
 
@@ -302,21 +311,24 @@ os_status os_exp_pairs_f32(const float* z, float* out, int64_t n, os_stream_t st
 }
 
 os_status os_device_status(os_stream_t stream) {
-    unsigned int* word = status_word();
-    if (!word) return OS_ERR_CUDA;
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return OS_ERR_CUDA;
+    if (!status_word()) return OS_ERR_CUDA;
+    // one host caller at a time per process: the exchange's result word is shared
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    status_exchange_kernel<<<1, 1, 0, s>>>();
+    if (cudaGetLastError() != cudaSuccess) return OS_ERR_CUDA;
     unsigned int v = 0;
-    if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return OS_ERR_CUDA;
-    if (v == 0) return OS_OK;
-    const unsigned int zero = 0;
-    if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    if (cudaMemcpyFromSymbolAsync(&v, os_device_status_taken, sizeof(v), 0,
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return OS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return OS_ERR_CUDA;
+    if (v == 0) return OS_OK;
     return (v & os::kErrWaitTimeout) ? OS_ERR_TIMEOUT : OS_ERR_CUDA;
 }
 
 os_status os_set_wait_timeout_ns(uint64_t ns) {
-    if (ns < 1000 || ns > 10000000000ull) return OS_ERR_SHAPE;
+    if (ns < 1000000ull || ns > 10000000000ull) return OS_ERR_SHAPE;
     g_timeout_ns.store(ns);
     return OS_OK;
 }

@@ -257,6 +257,27 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return v;
 }
 
+// Coherent (not read-only-path) forms of the two loads above, for inputs that
+// the same launch may overwrite: softmax exactly in place, where y == x.
+// Every softmax kernel reads an element before the thread that read it (or,
+// for rows staged in shared memory, its CTA) writes that element, and the
+// written value depends on the value read, so no load can be moved past the
+// store to its own address (so these need neither `volatile` nor a memory
+// clobber, and the compiler keeps its freedom to schedule them).
+__device__ __forceinline__ uint4 ld_coherent_policy_v4(const void* p, uint64_t policy) {
+    uint4 v;
+    asm("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(policy));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_coherent_v4(const void* p) {
+    uint4 v;
+    asm("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 
@@ -411,17 +432,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // (and at most 2^24 polls).  On giving up, records kErrWaitTimeout in the
 // device status word and returns false; the caller carries on with whatever
 // is in the buffer, so a lost copy corrupts outputs but never hangs the GPU.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  const KernelCtl& ctl) {
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint64_t* bar, uint32_t parity,
+                                                     unsigned long long timeout_ns,
+                                                     unsigned int* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1; it < (1u << 24); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > ctl.timeout_ns) break;
+        if (global_ns() - t0 > timeout_ns) break;
     }
-    atomicOr(ctl.err, kErrWaitTimeout);
+    atomicOr(err, kErrWaitTimeout);
     return false;
 }
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  const KernelCtl& ctl) {
+    return mbar_wait_bounded_ns(bar, parity, ctl.timeout_ns, ctl.err);
+}
+
+// Bound of the wait, before a CTA exits, for its own bulk copies still in
+// flight (only after a data wait gave up).  Fixed and long: a copy that has
+// been issued lands within microseconds, and a CTA must not exit while one
+// can still write its shared memory; the caller-set data-wait bound (which
+// may be as short as a millisecond) does not apply here.
+constexpr unsigned long long kDrainTimeoutNs = 4000000000ull;
 
 // CTA-wide bounded wait: thread 0 polls (the other threads sleep in the CTA
 // barrier instead of spinning), then the result is shared through flag[which]

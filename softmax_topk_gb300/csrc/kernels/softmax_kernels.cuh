@@ -53,7 +53,7 @@ __device__ __forceinline__ void load_slot(const TI* row, int64_t v, int cols, bo
                                           float* out) {
     constexpr int EPV = VecTraits<TI>::EPV;
     if (aligned) {
-        unpack(ld_stream_v4(row + v * EPV), out, TI());
+        unpack(ld_coherent_v4(row + v * EPV), out, TI());
     } else {
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
@@ -117,7 +117,7 @@ template <typename TO> constexpr bool fast_exp_for() { return sizeof(TO) == 2; }
 template <typename TI>
 __device__ __forceinline__ void load_slot_policy(const TI* row, int64_t v, uint64_t policy,
                                                  float* out) {
-    unpack(ld_policy_v4(row + v * VecTraits<TI>::EPV, policy), out, TI());
+    unpack(ld_coherent_policy_v4(row + v * VecTraits<TI>::EPV, policy), out, TI());
 }
 
 template <int N>
@@ -147,7 +147,7 @@ __device__ __forceinline__ void scale_all(float* e, float s) {
 // instruction covers 32 consecutive vectors of one row (or 32/L rows).
 template <typename TI, typename TO, int L, int VPT, int THREADS>
 __global__ void __launch_bounds__(THREADS)
-warp_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+warp_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                  int aligned, int64_t period, int64_t offset) {
     constexpr int EPV = VecTraits<TI>::EPV, EPT = VPT * EPV, RPW = 32 / L;
     const int lane_in_row = threadIdx.x % L;
@@ -241,7 +241,7 @@ __device__ __forceinline__ float2 merge_row_state(RowMergeSmem<THREADS, CLUSTER>
 // thread t owns slots rank*S + t + k*THREADS.
 template <typename TI, typename TO, int THREADS, int VPT, int CLUSTER>
 __global__ void __launch_bounds__(THREADS, 1)
-onchip_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+onchip_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                    int aligned) {
     constexpr int EPV = VecTraits<TI>::EPV, EPT = VPT * EPV;
     __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
@@ -348,7 +348,7 @@ struct TmaRing {
 
 template <typename TI, typename TO, int THREADS, int EPT, int CLUSTER, int STAGES>
 __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 128))
-tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+tma_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                 KernelCtl ctl) {
     using Ring = TmaRing<TI, THREADS, EPT, STAGES>;
     constexpr int EPV = Ring::EPV, VPT = Ring::VPT, NW = THREADS / 32;
@@ -443,11 +443,14 @@ tma_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int 
         }
     }
     // Loads can be left in flight only after a wait gave up: wait for each
-    // stage's last issued load (bounded) so nothing lands after the CTA exits.
+    // stage's last issued load (under the fixed drain bound, not the
+    // caller's data-wait bound) so nothing lands after the CTA exits.
     if (tid == 0 && failed) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s)
-            if (issued[s] > 0) mbar_wait_bounded(&full[s], uint32_t((issued[s] - 1) & 1), ctl);
+            if (issued[s] > 0)
+                mbar_wait_bounded_ns(&full[s], uint32_t((issued[s] - 1) & 1), kDrainTimeoutNs,
+                                     ctl.err);
     }
     if (CLUSTER > 1) cluster_sync();  // no CTA leaves while a peer may still address it
 }
@@ -545,7 +548,7 @@ __device__ __forceinline__ void load_stream_chunk(const TI* xs, int c, VecLimits
     for (int k = 0; k < UNROLL; ++k) {
         const int v = v0 + k * GROUP;
         if (ALIGNED && (full || v < vl.full)) {
-            ch.raw[k] = ld_policy_v4(xs + v * EPV, policy);
+            ch.raw[k] = ld_coherent_policy_v4(xs + v * EPV, policy);
         } else if (full || v < vl.any) {
             TI tmp[EPV];
 #pragma unroll
@@ -618,7 +621,7 @@ __device__ __forceinline__ float exp_sum_z(const float* z) {
 // lying wholly inside the CTA's range skip the per-vector range checks.
 template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER, bool ALIGNED>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
-stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols,
+stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                    int64_t period, int64_t offset) {
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV;
     constexpr bool FAST = fast_exp_for<TO>();
@@ -700,7 +703,7 @@ stream_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, i
 // (OS_PATH_SAFE), never chosen by AUTO.  One persistent CTA per row.
 template <typename TI, typename TO, int THREADS, int UNROLL, bool ALIGNED>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
-safe_rows_kernel(const TI* __restrict__ x, TO* __restrict__ y, int64_t rows, int cols) {
+safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV, NW = THREADS / 32;
     constexpr bool FAST = fast_exp_for<TO>();
     constexpr int STEP = THREADS * UNROLL;

@@ -608,7 +608,9 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
         if (n > CAP) {
             // ---- exact path (heavy ties at T; rare): the K-th largest key of the
             // segment by bisection over its columns, read again from memory;
-            // then the keys above it in any order and the ties at it in column order
+            // then the keys above it in any order and the ties at it in column order.
+            // -0 is keyed as +0 (x + 0 is +0 for both zeros), as beats() compares,
+            // so a tie between the two zeros goes to the lower column.
             const int c_lo = int(max(int64_t(0), 4 * int64_t(g.b0) - g.head));
             const int c_hi = int(min(int64_t(cols), 4 * int64_t(g.b1) - g.head));
             const float* xr = g.xr;
@@ -619,13 +621,13 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                 int cnt = 0;
                 // 64-bit element indices: c_hi can be 2^31 - 1, and e + THREADS must not wrap
                 for (int64_t e = int64_t(c_lo) + tid; e < c_hi; e += THREADS)
-                    cnt += order_key(xr[e]) >= probe;
+                    cnt += order_key(xr[e] + 0.0f) >= probe;
                 if (block_sum<THREADS>(cnt, sm.scratch) >= need) t = probe;
             }
             int admitted = 0;
             for (int64_t base = c_lo; base < c_hi; base += THREADS) {
                 const int64_t e = base + tid;
-                const bool above = e < c_hi && order_key(xr[e]) > t;
+                const bool above = e < c_hi && order_key(xr[e] + 0.0f) > t;
                 int round_total = 0;
                 const int p = admitted + block_exclusive_scan<THREADS>(above, sm.scratch, round_total);
                 if (above) sm.cand[p] = Cand{xr[e], int(e)};
@@ -633,7 +635,7 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             }
             for (int64_t base = c_lo; base < c_hi && admitted < need; base += THREADS) {  // uniform
                 const int64_t e = base + tid;
-                const bool tie = e < c_hi && order_key(xr[e]) == t;
+                const bool tie = e < c_hi && order_key(xr[e] + 0.0f) == t;
                 int round_total = 0;
                 const int p = admitted + block_exclusive_scan<THREADS>(tie, sm.scratch, round_total);
                 if (tie && p < need) sm.cand[p] = Cand{xr[e], int(e)};

@@ -186,6 +186,8 @@ def test_exp_argument_errors(lib):
 
 def test_testing_controls_validate(lib):
     assert lib.os_set_wait_timeout_ns(0) == SHAPE
+    assert lib.os_set_wait_timeout_ns(999_999) == SHAPE     # below the 1 ms floor
+    assert lib.os_set_wait_timeout_ns(10 ** 6) == OK
     assert lib.os_set_wait_timeout_ns(20 * 10 ** 9) == SHAPE
     assert lib.os_set_wait_timeout_ns(10 ** 9) == OK
     assert lib.os_set_fault_injection(5) == SHAPE

@@ -192,6 +192,72 @@ def test_sorted_selection_zero_ties(st, K):
     assert_topk_equal(fv.cpu().numpy(), fi.cpu().numpy(), rv, ri, f"fused zero ties K={K}")
 
 
+def _signed_zero_rows(rows, cols, seed, zeros=None):
+    """Rows of zeros with random signs (zeros=None), or rows of negative
+    values holding `zeros` random-sign zeros at random columns."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    if zeros is None:
+        sign = torch.randint(0, 2, (rows, cols), generator=g, device="cuda").bool()
+        return torch.where(sign, torch.tensor(-0.0, device="cuda"), torch.tensor(0.0, device="cuda"))
+    x = -torch.randn(rows, cols, generator=g, device="cuda").abs() - 1e-3
+    for r in range(rows):
+        pos = torch.randperm(cols, generator=g, device="cuda")[:zeros]
+        half = zeros // 2
+        x[r, pos[:half]] = 0.0
+        x[r, pos[half:]] = -0.0
+    return x
+
+
+def _check_fused_and_plain(st, x, K, label):
+    _run(st, x, K, f"fused {label}")
+    _run_plain(st, x, K, f"plain {label}")
+    vals, idx = st.topk(x, K)
+    want = torch.gather(x, 1, idx.long())
+    assert torch.equal(vals.view(torch.int32), want.view(torch.int32)), f"sign of zero lost: {label}"
+
+
+# (rows, cols): 320 rows run one CTA per row; 16 rows of 50257 split each row
+# over a cluster; 5000 and 7003 columns with more than 2048 zeros overflow the
+# candidate buffer, so the row takes the exact path
+@pytest.mark.parametrize("shape", [(320, 5000), (16, 50257), (7, 7003)])
+@pytest.mark.parametrize("K", [8, 64, 256])
+def test_exact_path_signed_zero_ties(st, shape, K):
+    """More than 2048 candidates tied at zero, half of them -0.0: the exact
+    path must rank -0 and +0 as one value and take the lowest columns, fused
+    and plain, one CTA per row and clusters; plain values keep their signs."""
+    rows, cols = shape
+    plan = st.os_topk_plan(rows, cols, K)
+    x = _signed_zero_rows(rows, cols, seed=rows + cols + K)
+    _check_fused_and_plain(st, x, K, f"all zeros {rows}x{cols} K={K} S={plan['cluster']}")
+    x = _signed_zero_rows(rows, cols, seed=rows * cols + K, zeros=min(cols - 1, 4000))
+    _check_fused_and_plain(st, x, K, f"4000 zeros {rows}x{cols} K={K} S={plan['cluster']}")
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_exact_path_misaligned_ragged(st, offset):
+    """The exact path on rows that start inside a 16-byte block and end in a
+    partial block (4-byte offsets, odd row length), through the raw C entry
+    points, fused and plain."""
+    rows, cols, K = 5, 6001, 64
+    buf = torch.empty(rows * cols + 8, device="cuda")
+    x = buf[offset:offset + rows * cols].view(rows, cols)
+    x.copy_(_signed_zero_rows(rows, cols, seed=offset * 11))
+    rv, ri = oracle.topk(x.double().cpu().numpy(), K)
+    for fn in (st.os_softmax_topk, st.os_topk):
+        vals = torch.empty(rows, K, device="cuda")
+        idx = torch.empty(rows, K, dtype=torch.int32, device="cuda")
+        fn(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, cols, K,
+           torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), ri), f"offset {offset} {fn.__name__}"
+        if fn is st.os_softmax_topk:
+            assert_topk_equal(vals.cpu().numpy(), idx.cpu().numpy(), rv, ri, f"offset {offset}")
+        else:
+            want = torch.gather(x, 1, idx.long())
+            assert torch.equal(vals.view(torch.int32), want.view(torch.int32))
+
+
 @pytest.mark.parametrize("K", [8, 64])
 def test_unfused_pipeline_matches_fused(st, K):
     """softmax then TopK of the probabilities (the unfused pipeline) against the
@@ -207,10 +273,26 @@ def test_unfused_pipeline_matches_fused(st, K):
 
 
 # ------------------------------------------------------------------ top-K sampling
+def _sample_window(vals, u):
+    """The fp32 rounding window of each row's draw: the kernel rounds each of
+    its K partial sums and the product u * total to fp32, so every compared
+    quantity is within (K + 1) 2^-24 of the total of its exact value (all
+    values are >= 0).  Returns the exact partial sums, the exact targets and
+    the window half-width per row."""
+    v = vals.astype(np.float64)
+    K = v.shape[1]
+    total = v.sum(axis=1)
+    return np.cumsum(v, axis=1), u * total, 2 * (K + 1) * 2.0 ** -24 * total
+
+
 @pytest.mark.parametrize("K", [1, 8, 64, 256])
 def test_topk_sample_matches_oracle(st, K):
-    """Fused TopK, then one draw per row; the oracle draws from the same
-    (value, index) pairs and the same u, so the columns must agree exactly."""
+    """Fused TopK, then one draw per row; the float64 oracle draws from the
+    same (value, index) pairs and the same u.  Every row whose target is not
+    within fp32 rounding of a cumulative-sum boundary must agree exactly;
+    on the (few, counted) ambiguous rows the kernel's pick must be a position
+    the rounding window allows: its partial sum reaches the target and the
+    one before does not, each up to the window."""
     w = workloads.WORKLOADS["topk_256x50257_f32"]
     x = workloads.make(w, device="cuda")
     g = torch.Generator(device="cuda")
@@ -218,10 +300,39 @@ def test_topk_sample_matches_oracle(st, K):
     u = torch.rand(w.rows, generator=g, device="cuda")
     samples, vals, idx = st.softmax_topk_sample(x, K, u)
     torch.cuda.synchronize()
-    want = oracle.topk_sample(vals.double().cpu().numpy(), idx.cpu().numpy(),
-                              u.double().cpu().numpy())
-    assert np.array_equal(samples.cpu().numpy(), want)
-    assert np.all(np.any(idx.cpu().numpy() == samples.cpu().numpy()[:, None], axis=1))
+    v, ix, uu = vals.double().cpu().numpy(), idx.cpu().numpy(), u.double().cpu().numpy()
+    got = samples.cpu().numpy()
+    want = oracle.topk_sample(v, ix, uu)
+    run, target, win = _sample_window(v, uu)
+    amb = np.abs(run - target[:, None]).min(axis=1) <= win
+    assert np.array_equal(got[~amb], want[~amb]), \
+        f"K={K}: {int((got[~amb] != want[~amb]).sum())} unambiguous rows differ"
+    for r in np.nonzero(amb)[0]:
+        k = int(np.nonzero(ix[r] == got[r])[0][0])
+        below = run[r, k - 1] if k > 0 else 0.0
+        assert below <= target[r] + win[r], (r, k)
+        assert k == K - 1 or run[r, k] > target[r] - win[r], (r, k)
+    print(f"K={K}: {int(amb.sum())} of {w.rows} rows within fp32 rounding of a boundary, "
+          f"{int((got[amb] != want[amb]).sum())} of them drawn differently")
+    assert np.all(np.any(ix == got[:, None], axis=1))
+
+
+def test_topk_sample_near_boundaries(st):
+    """Non-dyadic values with u placed a clear margin (1e-5 of the total) on
+    either side of each cumulative-sum boundary: the float64 oracle and the
+    fp32 kernel must pick the same entry."""
+    p = np.array([0.1, 0.2, 0.3, 0.4], dtype=np.float32)
+    bounds = np.cumsum(p.astype(np.float64))[:-1] / p.astype(np.float64).sum()
+    us = np.concatenate([bounds - 1e-5, bounds + 1e-5]).astype(np.float32)
+    rows = len(us)
+    vals = torch.tensor(np.tile(p, (rows, 1)), device="cuda")
+    idx = (torch.arange(4, dtype=torch.int32, device="cuda") + 20).repeat(rows, 1).contiguous()
+    u = torch.tensor(us, device="cuda")
+    out = st.topk_sample(vals, idx, u).cpu().numpy()
+    want = oracle.topk_sample(np.tile(p.astype(np.float64), (rows, 1)), idx.cpu().numpy(),
+                              us.astype(np.float64))
+    assert np.array_equal(out, want)
+    assert list(out) == [20, 21, 22, 21, 22, 23]
 
 
 def test_topk_sample_frequencies(st):

@@ -41,9 +41,11 @@ MUTANTS = {
     "causal_mask_ignores_period": ("c > (r % period) + offset ? -INFINITY",
                                    "c > r + offset ? -INFINITY"),
     "sample_ge_instead_of_gt": ("if (run > target) {", "if (run >= target) {"),
-    "sample_compares_single_value": ("run = run + (float)p[k];", "run = (float)p[k];"),
-    "sample_unnormalised_target": ("volatile float target = (float)u[r] * total;",
-                                   "volatile float target = (float)u[r];"),
+    "sample_compares_single_value": ("run += p[k];", "run = p[k];"),
+    "sample_unnormalised_target": ("const double target = u[r] * total;",
+                                   "const double target = u[r];"),
+    "sample_total_skips_last": ("for (int32_t k = 0; k < K; ++k) total += p[k];",
+                                "for (int32_t k = 0; k + 1 < K; ++k) total += p[k];"),
     "attention_drops_scale": ("s[j] = scale * acc;", "s[j] = acc;"),
     "attention_mask_excludes_diagonal": ("const int64_t seen = causal ? i + 1 : n;",
                                          "const int64_t seen = causal ? i : n;"),

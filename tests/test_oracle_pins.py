@@ -272,14 +272,18 @@ def pin_causal_mask_rows(lib):
 # ---------------------------------------------------------------- top-K sampling
 def pin_topk_sample_frequencies(lib):
     """With u on a grid of N midpoints the draws split in proportion to the
-    values (dyadic values: exactly); zero-probability entries are never drawn,
+    values (exactly: no cumulative sum lies near a grid point); zero-probability
+    entries are never drawn,
     also at u = 0; scaling all values changes nothing; u = 1 gives the last."""
     N = 1024
     u = (np.arange(N) + 0.5) / N
     for p, want in (([0.5, 0.25, 0.125, 0.125], [512, 256, 128, 128]),
                     ([1.0, 0.5, 0.25, 0.25], [512, 256, 128, 128]),
                     ([0.5, 0.0, 0.5], [512, 0, 512]),
-                    ([0.75, 0.25], [768, 256])):
+                    ([0.75, 0.25], [768, 256]),
+                    # not dyadic: the cumulative sums 0.1, 0.3, 0.6 fall between grid
+                    # points (102.4, 307.2, 614.4 of 1024), far from any rounding
+                    ([0.1, 0.2, 0.3, 0.4], [102, 205, 307, 410])):
         K = len(p)
         vals = np.tile(np.array(p), (N, 1))
         idx = np.tile(np.arange(K, dtype=np.int32) + 10, (N, 1))
