@@ -32,11 +32,14 @@
  *     softmax and its outputs are unspecified (NaN in practice).
  *   - Arithmetic: fp32 throughout (bf16 inputs widened exactly, fp32
  *     accumulation, bf16 outputs rounded to nearest even).  Per-element
- *     exponentials: fp32 results of the two-pass streaming kernel use the
- *     library's own FMA-pipe exponential (no ex2.approx: base-2 reduction
- *     and a degree-5 polynomial); bf16 results and the register, on-chip,
- *     statistics and TopK kernels use the SFU's 2^x (ex2.approx) of
- *     (x - m) log2 e, log2 e in two fp32 parts for fp32 results.  A value
+ *     exponentials: the two-pass streaming kernel (every row longer than
+ *     4096 16-byte vectors, and the three-pass baseline) uses the library's
+ *     own FMA-pipe exponential for every output dtype (no ex2.approx:
+ *     base-2 reduction, a degree-5 polynomial for fp32 results and a
+ *     degree-3 one for bf16 results, 2^n added to the exponent field); the
+ *     register, on-chip, statistics and TopK kernels use the SFU's 2^x
+ *     (ex2.approx) of (x - m) log2 e, log2 e in two fp32 parts for fp32
+ *     results.  A value
  *     that carries a whole row (a merge's rescale factor, a TopK output
  *     value) uses the library's accurate exponential (os_exp_f32).
  *   - Work runs on the device current at the call (cudaGetDevice); the
@@ -81,11 +84,19 @@ typedef enum {
                            in registers across the cluster; one HBM read */
     OS_PATH_STREAM = 3, /* two passes over the row (running (m, d), then
                            normalise); any row length */
-    OS_PATH_SAFE = 4    /* baseline: the three-pass safe softmax (maximum;
+    OS_PATH_SAFE = 4,   /* baseline: the three-pass safe softmax (maximum;
                            sum of e^(x - m); normalise), each pass reading the
                            row from memory ("Online normalizer calculation for
                            softmax", section 2); any row length; never chosen
                            by AUTO */
+    OS_PATH_STREAM_POLY = 5 /* OS_PATH_STREAM with the library's FMA-pipe
+                           exponential for every output dtype (no
+                           ex2.approx anywhere in the kernel).  For fp32
+                           results this is the STREAM kernel itself; for bf16
+                           results it replaces the SFU's 2^x (STREAM's and
+                           AUTO's choice there, about 25 % faster on GB300)
+                           by degree-2 (normaliser) and degree-3 (outputs)
+                           fits of 2^f; never chosen by AUTO */
 } os_path;
 
 /* Launch configuration chosen for a call (see os_softmax_plan / os_topk_plan). */
@@ -248,8 +259,7 @@ os_status os_topk_plan(int64_t rows, int64_t cols, int32_t K, os_plan *plan);
  * (Cody-Waite reduction z = n ln2 + r, a degree-6 minimax polynomial for e^r,
  * 2^n written into the exponent field; no ex2.approx).  The kernels above use
  * it where one value carries a whole row (the rescale factors of the merges,
- * the TopK output values); their per-element exponentials are the SFU's
- * 2^x with the maximum split into a high part and an FMA residual.  Defined
+ * the TopK output values).  Defined
  * for z <= 88: within about 1 ulp of e^z for
  * z >= -87.33, 0 or a value below FLT_MIN for smaller z, exactly +0 for
  * z = -inf.  Exposed so the routine can be tested on its own.
@@ -260,15 +270,25 @@ os_status os_exp_f32(const float *z, float *out, int64_t n, os_stream_t stream);
 /*
  * out[i] = e^(z[i]) for n fp32 values with the per-element exponential of the
  * two-pass streaming kernel's fp32 results: two values at a time on packed
- * fp32 FMAs, no ex2.approx (n = rint(z log2 e), f = z log2 e - n with log2 e
- * in two fp32 parts, a degree-5 minimax polynomial for 2^f, 2^n written
- * into the exponent field).  Defined for z <= 0, the softmax domain
- * x - max: within 3e-7 relative of e^z for z >= -87.33, 0 or a value below
- * FLT_MIN for smaller z, exactly +0 for z = -inf and exactly 1 for z = 0.
- * Exposed so the routine can be tested on its own; arguments and checks as
- * os_exp_f32 (n may be odd).
+ * fp32 FMAs, no ex2.approx (n = rint(z log2 e) from one FMA with a rounding
+ * constant, f = z log2 e - n with log2 e in two fp32 parts, a degree-5
+ * minimax polynomial for 2^f, n + 66 added to its exponent field by an
+ * integer shift-add, then one multiply by 2^-66, which the kernel shares with
+ * its 1/d).  Defined for z <= 0, the softmax domain x - max: within 3e-7
+ * relative of e^z for z >= -87.33, 0 or a value below FLT_MIN for smaller z
+ * (exactly +0 below -110 and for z = -inf), exactly 1 for z = 0.  Exposed so
+ * the routine can be tested on its own; arguments and checks as os_exp_f32
+ * (n may be odd).
  */
 os_status os_exp_pairs_f32(const float *z, float *out, int64_t n, os_stream_t stream);
+
+/*
+ * The same for the streaming kernel's bf16 results, before their rounding to
+ * bf16: log2 e in one fp32 part and a degree-3 polynomial for 2^f (1.0e-4),
+ * so within 1.2e-4 relative of e^z for z >= -87.33 (bf16 itself rounds at
+ * 2^-9 = 2.0e-3); the other properties as os_exp_pairs_f32.
+ */
+os_status os_exp_pairs_coarse_f32(const float *z, float *out, int64_t n, os_stream_t stream);
 
 /*
  * Device-side waits.  Kernels that stage rows in shared memory wait on

@@ -3,7 +3,8 @@
 The C ABI (include/os_softmax.h) is wrapped with ctypes under the same names:
 ``os_softmax_fwd``, ``os_softmax_topk``, ``os_topk``, ``os_softmax_causal_fwd``,
 ``os_softmax_stats``, ``os_topk_sample``, ``os_attention_fwd``, ``os_softmax_fwd_path``,
-``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_exp_pairs_f32``, ``os_device_status``,
+``os_softmax_plan``, ``os_topk_plan``, ``os_exp_f32``, ``os_exp_pairs_f32``,
+``os_exp_pairs_coarse_f32``, ``os_device_status``,
 ``os_set_wait_timeout_ns``, ``os_set_fault_injection``, ``os_status_string``.  They take raw
 device pointers (ints) and a raw stream handle, exactly like the C functions,
 and raise ``OsError`` on a non-OK status.
@@ -27,8 +28,9 @@ LIB_PATH = os.path.join(_HERE, "lib", "libos_softmax.so")
 
 OS_F32, OS_BF16 = 0, 1
 OS_PATH_AUTO, OS_PATH_WARP, OS_PATH_ONCHIP, OS_PATH_STREAM, OS_PATH_SAFE = 0, 1, 2, 3, 4
+OS_PATH_STREAM_POLY = 5
 PATHS = {"auto": OS_PATH_AUTO, "warp": OS_PATH_WARP, "onchip": OS_PATH_ONCHIP,
-         "stream": OS_PATH_STREAM, "safe": OS_PATH_SAFE}
+         "stream": OS_PATH_STREAM, "safe": OS_PATH_SAFE, "stream_poly": OS_PATH_STREAM_POLY}
 STATUS = ["OS_OK", "OS_ERR_NULL", "OS_ERR_SHAPE", "OS_ERR_DTYPE", "OS_ERR_K", "OS_ERR_ALIAS",
           "OS_ERR_CUDA", "OS_ERR_TIMEOUT", "OS_ERR_PATH", "OS_ERR_ALIGN", "OS_ERR_VALUE"]
 KMAX = 256
@@ -73,6 +75,7 @@ def _load() -> ctypes.CDLL:
     lib.os_topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(Plan)]
     lib.os_exp_f32.argtypes = [vp, vp, i64, vp]
     lib.os_exp_pairs_f32.argtypes = [vp, vp, i64, vp]
+    lib.os_exp_pairs_coarse_f32.argtypes = [vp, vp, i64, vp]
     lib.os_device_status.argtypes = [vp]
     lib.os_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.os_set_fault_injection.argtypes = [i32]
@@ -81,7 +84,8 @@ def _load() -> ctypes.CDLL:
     for name in ("os_softmax_fwd", "os_softmax_fwd_path", "os_softmax_topk", "os_topk",
                  "os_softmax_causal_fwd", "os_softmax_stats", "os_topk_sample", "os_attention_fwd",
                  "os_softmax_plan",
-                 "os_topk_plan", "os_exp_f32", "os_exp_pairs_f32", "os_device_status",
+                 "os_topk_plan", "os_exp_f32", "os_exp_pairs_f32", "os_exp_pairs_coarse_f32",
+                 "os_device_status",
                  "os_set_wait_timeout_ns",
                  "os_set_fault_injection"):
         getattr(lib, name).restype = st
@@ -150,6 +154,10 @@ def os_exp_f32(z: int, out: int, n: int, stream: int | None) -> None:
 
 def os_exp_pairs_f32(z: int, out: int, n: int, stream: int | None) -> None:
     _check(_lib.os_exp_pairs_f32(z, out, n, stream), "os_exp_pairs_f32")
+
+
+def os_exp_pairs_coarse_f32(z: int, out: int, n: int, stream: int | None) -> None:
+    _check(_lib.os_exp_pairs_coarse_f32(z, out, n, stream), "os_exp_pairs_coarse_f32")
 
 
 def os_device_status(stream: int | None) -> None:
@@ -335,15 +343,16 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     return out, lse
 
 
-def exp(z, pairs: bool = False):
+def exp(z, pairs: bool = False, coarse: bool = False):
     """e^z elementwise (fp32 CUDA tensor) with the library's own exponential:
     the accurate scalar routine, or (pairs=True, z <= 0) the per-element
-    exponential of the streaming kernel's fp32 results."""
+    exponential of the streaming kernel's fp32 results, or (pairs=True,
+    coarse=True) that of its bf16 results before their rounding."""
     import torch
     if not z.is_cuda or z.dtype != torch.float32 or not z.is_contiguous():
         raise ValueError("z must be a contiguous float32 CUDA tensor")
     out = torch.empty_like(z)
-    fn = os_exp_pairs_f32 if pairs else os_exp_f32
+    fn = (os_exp_pairs_coarse_f32 if coarse else os_exp_pairs_f32) if pairs else os_exp_f32
     with _OnDevice(z.device):
         fn(z.data_ptr(), out.data_ptr(), z.numel(), _stream_handle(z))
     return out

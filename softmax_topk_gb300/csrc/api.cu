@@ -88,7 +88,7 @@ bool shape_ok(int64_t rows, int64_t cols) {
 os_status softmax_checks(int64_t rows, int64_t cols, os_dtype in, os_dtype out, os_path path) {
     if (!valid_dtype(in) || !valid_dtype(out)) return OS_ERR_DTYPE;
     if (!shape_ok(rows, cols)) return OS_ERR_SHAPE;
-    if (path < OS_PATH_AUTO || path > OS_PATH_SAFE) return OS_ERR_PATH;
+    if (path < OS_PATH_AUTO || path > OS_PATH_STREAM_POLY) return OS_ERR_PATH;
     return OS_OK;
 }
 
@@ -119,7 +119,8 @@ os_status softmax_entry(const void* x, void* y, int64_t rows, int64_t cols, os_d
     if (period > 0) {
         const int64_t nv = (cols + elems_per_vector(in) - 1) / elems_per_vector(in);
         if (path == OS_PATH_AUTO) path = nv <= 256 ? OS_PATH_WARP : OS_PATH_STREAM;
-        if (path != OS_PATH_WARP && path != OS_PATH_STREAM) return OS_ERR_PATH;
+        if (path != OS_PATH_WARP && path != OS_PATH_STREAM && path != OS_PATH_STREAM_POLY)
+            return OS_ERR_PATH;
     }
     const bool ptrs_aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
                               reinterpret_cast<uintptr_t>(y) % 16 == 0;
@@ -212,7 +213,7 @@ os_status os_topk_plan(int64_t rows, int64_t cols, int32_t K, os_plan* plan) {
     return os::plan_topk(rows, cols, K, plan);
 }
 
-os_status topk_entry(const float* x, float* vals, int32_t* idx, int64_t rows, int64_t cols,
+static os_status topk_entry(const float* x, float* vals, int32_t* idx, int64_t rows, int64_t cols,
                      int32_t K, bool plain, os_stream_t stream) {
     os_status st = topk_checks(rows, cols, K);
     if (st != OS_OK) return st;
@@ -300,14 +301,23 @@ os_status os_exp_f32(const float* z, float* out, int64_t n, os_stream_t stream) 
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
 }
 
-os_status os_exp_pairs_f32(const float* z, float* out, int64_t n, os_stream_t stream) {
+static os_status exp_pairs_entry(const float* z, float* out, int64_t n, int degree, os_stream_t stream) {
     if (n < 0) return OS_ERR_SHAPE;
     if (n == 0) return OS_OK;
     if (!z || !out) return OS_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(z) % 4 || reinterpret_cast<uintptr_t>(out) % 4)
         return OS_ERR_ALIGN;
-    const cudaError_t e = os::launch_exp_pairs(z, out, n, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = os::launch_exp_pairs(z, out, n, degree,
+                                               reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OS_OK : OS_ERR_CUDA;
+}
+
+os_status os_exp_pairs_f32(const float* z, float* out, int64_t n, os_stream_t stream) {
+    return exp_pairs_entry(z, out, n, 5, stream);
+}
+
+os_status os_exp_pairs_coarse_f32(const float* z, float* out, int64_t n, os_stream_t stream) {
+    return exp_pairs_entry(z, out, n, 3, stream);
 }
 
 os_status os_device_status(os_stream_t stream) {

@@ -1,7 +1,8 @@
 """Derivation of the polynomials of the library's fp32 exponentials in
 kernels/ops.cuh: e^r for exp1 (os_exp_f32, merge rescale factors, TopK
-values), and 2^f for the per-element exponentials of fp32 softmax results
-(exp_pair, second part of this file).
+values), and 2^f for the per-element exponentials of the streaming softmax
+kernels (exp_biased_pair, second part of this file: degree 5 for fp32
+results, degree 3 for bf16 results).
 
 The kernels evaluate e^z as 2^n * p(r) with n = rint(z * log2 e) and
 r = z - n ln2 (Cody & Waite, "Software Manual for the Elementary Functions",
@@ -47,6 +48,9 @@ def lawson_fit(degree: int, iters: int = 60, fn=np.exp, half_width: float = A):
 # 2^f itself, again relative and with p(0) = 1 exactly; degree 5 gives about
 # 9e-8 (1.1e-7 once the coefficients are rounded to fp32).
 DEGREE_2F = 5
+# Where results are rounded to bf16 (relative rounding 2^-9), degree 3 on the
+# same interval is enough: about 1.0e-4 with fp32 coefficients.
+DEGREE_2F_BF16 = 3
 
 
 if __name__ == "__main__":
@@ -55,8 +59,9 @@ if __name__ == "__main__":
     for k, c in enumerate(coeffs):
         c32 = np.float32(c)
         print(f"c{k} = {c32!r}  (0x{int(c32.view(np.uint32)):08x})")
-    coeffs, err = lawson_fit(DEGREE_2F, iters=80, fn=np.exp2, half_width=0.5)
-    print(f"2^f, degree {DEGREE_2F}: max relative error {err:.3e}")
-    for k, c in enumerate(coeffs):
-        c32 = np.float32(c)
-        print(f"e{k} = {c32!r}  (0x{int(c32.view(np.uint32)):08x})")
+    for deg in (DEGREE_2F, DEGREE_2F_BF16):
+        coeffs, err = lawson_fit(deg, iters=80, fn=np.exp2, half_width=0.5)
+        print(f"2^f, degree {deg}: max relative error {err:.3e}")
+        for k, c in enumerate(coeffs):
+            c32 = np.float32(c)
+            print(f"e{deg}_{k} = {c32!r}  (0x{int(c32.view(np.uint32)):08x})")

@@ -30,7 +30,9 @@ cudaError_t launch_topk(const os_plan& p, const float* x, float* vals, int32_t* 
                         cudaStream_t stream);
 
 cudaError_t launch_exp(const float* z, float* out, int64_t n, cudaStream_t stream);
-cudaError_t launch_exp_pairs(const float* z, float* out, int64_t n, cudaStream_t stream);
+// degree 5: the fp32 results' exponential; 3: the bf16 results'
+cudaError_t launch_exp_pairs(const float* z, float* out, int64_t n, int degree,
+                             cudaStream_t stream);
 
 // one column per row drawn from its K (value, index) pairs, u[r] in [0, 1)
 cudaError_t launch_topk_sample(const float* vals, const int32_t* idx, const float* u, int32_t* out,

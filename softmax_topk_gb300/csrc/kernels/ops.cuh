@@ -119,37 +119,139 @@ __device__ __forceinline__ float exp1(float z) {
 }
 
 // ------------------------------------------------------------------ exp (pairs)
-// The per-element exponentials of the softmax passes, the two lanes of a
-// packed f32x2 at a time.
+// The per-element exponentials of the two-pass streaming kernel (and of the
+// three-pass baseline measured against it), the two lanes of a packed f32x2
+// at a time, on the FMA and integer pipes only (no ex2.approx):
 //
-// fp32 results of the two-pass streaming kernel: on the FMA pipe only, no
-// ex2.approx (exp_pair_fma):
-//   n  = rint(z log2e)                 u = z log2e + 1.5*2^23 (one FMA)
-//   f  = (z log2e - n) + z log2e_lo    two FMAs; |f| <= 1/2 plus ~2e-6
-//   p  = 1 + f (e1 + f (e2 + ...))     2^f, degree-5 minimax fit on [-1/2, 1/2]
-//   e^z = p * 2^n                      2^n from u's bits (integer multiply-add)
-// z is clamped to >= -88 first (-inf included): then n >= -127, and n = -127
-// makes 2^n exactly +0, so e^-inf = +0 and results below 2^-126 are zero or
-// tiny.  log2 e is carried as kLog2e + kLog2eLo, so the reduced argument is
-// accurate to about 2^-25 whatever |z|, and the relative error of e^z is the
-// polynomial's (1.1e-7 with its fp32 coefficients, from
-// csrc/fit_exp_poly.py) plus the rounding of its evaluation.
+//   z := max(z, -110)                  (-inf included)
+//   u  = z log2e + (1.5*2^23 + 66)     one FMA; the rounding constant makes u
+//                                      hold n + 66 in its low bits, n = rint(z log2e)
+//   f  = z log2e - n                   two FMAs (the constant minus u is -n
+//                                      exactly); fp32 results add z log2e_lo
+//   p  = 2^f                           minimax fit on [-1/2, 1/2]: degree 5
+//                                      (1.1e-7) for fp32 results, degree 3
+//                                      (1.0e-4) for bf16 results
+//   q  = p 2^(n + 66)                  n + 66 added to p's exponent field: one
+//                                      integer shift-add of u's bits
 //
-// Everything else (results rounded to bf16 afterwards; the register,
-// on-chip and statistics kernels): the special-function unit's 2^x (PTX
-// ex2.approx.ftz.f32; -inf -> +0, results below 2^-126 -> +0), a few ulp of
-// fp32.  The polynomial costs about ten FMA-pipe instructions per pair
-// against two SFU instructions: measured, a quarter of the throughput of the
-// bf16 streaming kernel (eight elements per 16-byte vector, an exponential
-// per element in each pass) and of the on-chip kernel on 4096-column rows,
-// and nothing on fp32 streaming rows.
+// The caller multiplies q by 2^-66 -- and the output pass by 2^-66 / d, so
+// the normalisation costs nothing extra -- or sums q first (pass 1 sums a
+// chunk, then scales once).  The +66 keeps q a normal number for every
+// z >= -110 (n >= -159, so the exponent field of q stays >= 2); the clamp
+// makes e^-inf (and anything below e^-110) come out as 0 or a subnormal
+// after the scale, below FLT_MIN as e^z itself is.  e^0 is exactly 1.
 namespace expc {
 constexpr float kLog2eLo = 1.925963034e-08f;  // log2 e - kLog2e
-constexpr float kZFloor = -88.0f;             // z log2 e <= -126.96: n = -127, 2^n = +0
-// 2^f = 1 + f (e1 + f (e2 + ...)), max relative error 1.1e-7
+constexpr float kZClamp = -110.0f;
+constexpr float kBiasedRound = 12582978.0f;   // 1.5 * 2^23 + 66
+constexpr float kUnbias = 1.35525271560688054e-20f;  // 2^-66
+// 2^f = 1 + f (e1 + f (e2 + ...)) on [-1/2, 1/2], max relative error 1.1e-7
 constexpr float e5_1 = 0.693147f, e5_2 = 0.24022242f, e5_3 = 0.055507336f,
                 e5_4 = 0.009671513f, e5_5 = 0.0013264726f;
+// the same, degree 3, max relative error 1.0e-4 (results rounded to bf16,
+// whose own rounding is 2^-8 relative)
+constexpr float e3_1 = 0.69328296f, e3_2 = 0.24221098f, e3_3 = 0.055008918f;
+// degree 2, max relative error 2.0e-3: the normaliser sum of rows whose
+// results are rounded to bf16 (it adds at most 2.0e-3 to every result's
+// error, which with the degree-3 output pass and bf16's rounding stays below
+// 6e-3)
+constexpr float e2_1 = 0.70294195f, e2_2 = 0.23986399f;
+constexpr float kLn2 = 0.693147182f;
 }  // namespace expc
+
+// 2^f of a pair for |f| <= 1/2 by the fit of degree DEG (2, 3 or 5).
+template <int DEG>
+__device__ __forceinline__ float2 exp2_poly(float2 f) {
+    using namespace expc;
+    float2 p;
+    if constexpr (DEG == 5) {
+        p = fma2(splat2(e5_5), f, splat2(e5_4));
+        p = fma2(p, f, splat2(e5_3));
+        p = fma2(p, f, splat2(e5_2));
+        p = fma2(p, f, splat2(e5_1));
+    } else if constexpr (DEG == 3) {
+        p = fma2(splat2(e3_3), f, splat2(e3_2));
+        p = fma2(p, f, splat2(e3_1));
+    } else {
+        static_assert(DEG == 2, "fitted degrees");
+        p = fma2(splat2(e2_2), f, splat2(e2_1));
+    }
+    return fma2(p, f, splat2(1.0f));
+}
+
+// p * 2^k where u = 1.5 * 2^23 + k (an integer-valued float, |k| < 2^22):
+// p's bits plus u's bits times 2^23, one integer multiply-add.
+__device__ __forceinline__ float add_exponent(float p, float u) {
+    uint32_t r;
+    asm("mad.lo.u32 %0, %1, 8388608, %2;" : "=r"(r) : "r"(__float_as_uint(u)), "r"(__float_as_uint(p)));
+    return __uint_as_float(r);
+}
+
+// q = 2^(z log2 e + 66) of a pair, -126 <= z <= 43 after the clamp; DEG 5
+// (fp32 results) or 3 (bf16).  CLAMP = false: the caller has already bounded
+// z from below (at -110 or lower, but not below -126), e.g. on packed bf16
+// inputs.  Above, z up to 43 keeps q (and a sum of 32 such) finite.
+template <int DEG, bool CLAMP = true>
+__device__ __forceinline__ float2 exp_biased_pair(float2 z) {
+    using namespace expc;
+    if constexpr (CLAMP) z = make_float2(fmaxf(z.x, kZClamp), fmaxf(z.y, kZClamp));
+    const float2 K = splat2(kBiasedRound);
+    const float2 u = fma2(z, splat2(kLog2e), K);
+    const float2 neg_n = fma2(u, splat2(-1.0f), K);  // exact: both near 1.5 * 2^23
+    float2 f = fma2(z, splat2(kLog2e), neg_n);
+    if constexpr (DEG == 5) f = fma2(z, splat2(kLog2eLo), f);
+    const float2 p = exp2_poly<DEG>(f);
+    // u's bits are those of 1.5 * 2^23 plus n + 66; times 2^23 (modulo 2^32)
+    // the constant part leaves the word and n + 66 lands on the exponent field
+    return make_float2(add_exponent(p.x, u.x), add_exponent(p.y, u.y));
+}
+
+// The two bf16 values of a word as exact fp32 values, by byte permutes (on
+// the integer pipe, off the FMA pipe that the exponential keeps busy).
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(lo) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0x3244;" : "=r"(hi) : "r"(w));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+
+// Shift m folded into the exponential: for a reference m (finite, |m| <
+// 2^21), 2^((x - m) log2 e) = q(x) * frac with q(x) = 2^(x log2 e + c_int +
+// 66) from exp_folded_pair and k = 1.5 * 2^23 + 66 + c_int, where
+// -m log2 e = c_int + c_frac (c_int an integer, |c_frac| <= 1/2 + 2^-20,
+// m log2 e carried in two fp32 parts) and frac = 2^c_frac * 2^-66.  log2 e's
+// own fp32 rounding enters only through (x - m).
+struct FoldedShift {
+    float2 k;
+    float frac;
+};
+__device__ __forceinline__ FoldedShift folded_shift(float m) {
+    using namespace expc;
+    const float b_hi = m * kLog2e;
+    const float b_lo = fmaf(m, kLog2e, -b_hi);  // exact residual of the product
+    const float c_int = rintf(-b_hi);
+    const float c_frac = (-b_hi - c_int) - b_lo;
+    return {splat2(kBiasedRound + c_int), exp1(c_frac * kLn2) * kUnbias};
+}
+
+// q = 2^(x log2 e + c_int + 66) of a pair of inputs x (not x - m), for
+// -126 <= x - m <= 43 (the caller clamps below): the rounding constant k of
+// folded_shift(m) takes the place of the subtraction of m.  DEG 2 or 3.
+template <int DEG>
+__device__ __forceinline__ float2 exp_folded_pair(float2 x, float2 k) {
+    using namespace expc;
+    const float2 u = fma2(x, splat2(kLog2e), k);
+    const float2 neg_n = fma2(u, splat2(-1.0f), k);  // exact
+    const float2 f = fma2(x, splat2(kLog2e), neg_n);   // x log2 e - rint(x log2 e)
+    const float2 p = exp2_poly<DEG>(f);
+    return make_float2(add_exponent(p.x, u.x), add_exponent(p.y, u.y));
+}
+
+// e^z of a pair (z <= 0, -inf allowed) for fp32 results: the form above,
+// unbiased.  os_exp_pairs_f32 exposes it for its accuracy test.
+__device__ __forceinline__ float2 exp_pair_fma(float2 z) {
+    return mul2(exp_biased_pair<5>(z), splat2(expc::kUnbias));
+}
 
 __device__ __forceinline__ float ex2_sfu(float t) {
     float r;
@@ -157,9 +259,10 @@ __device__ __forceinline__ float ex2_sfu(float t) {
     return r;
 }
 
-// e^z of a pair on the SFU: accurate (FAST = false: log2 e carried in two
-// fp32 parts, for fp32 results) or with log2 e rounded to fp32 (FAST = true,
-// for results rounded to bf16 afterwards).  Error of e^z: the product t =
+// e^z of a pair on the SFU (the register, on-chip and statistics kernels):
+// accurate (FAST = false: log2 e carried in two fp32 parts, for fp32 results)
+// or with log2 e rounded to fp32 (FAST = true, for results rounded to bf16
+// afterwards).  Error of e^z: the product t =
 // z log2 e rounded once (2^-24 |z| relative) plus ex2's few ulp.
 template <bool FAST>
 __device__ __forceinline__ float2 exp_pair(float2 z) {
@@ -169,26 +272,8 @@ __device__ __forceinline__ float2 exp_pair(float2 z) {
     return make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
 }
 
-// e^z of a pair (z <= 0, -inf allowed) on the FMA pipe, no ex2.approx: the
-// polynomial form described above, for fp32 results of the two-pass
-// streaming kernel (and the three-pass baseline measured against it).
-__device__ __forceinline__ float2 exp_pair_fma(float2 z) {
-    using namespace expc;
-    z = make_float2(fmaxf(z.x, kZFloor), fmaxf(z.y, kZFloor));
-    const float2 u = fma2(z, splat2(kLog2e), splat2(kRound));
-    const float2 neg_n = fma2(u, splat2(-1.0f), splat2(kRound));  // exact
-    float2 f = fma2(z, splat2(kLog2e), neg_n);
-    f = fma2(z, splat2(kLog2eLo), f);
-    float2 p = fma2(splat2(e5_5), f, splat2(e5_4));
-    p = fma2(p, f, splat2(e5_3));
-    p = fma2(p, f, splat2(e5_2));
-    p = fma2(p, f, splat2(e5_1));
-    p = fma2(p, f, splat2(1.0f));
-    return mul2(p, make_float2(pow2_from_rounded(u.x), pow2_from_rounded(u.y)));
-}
-
-// e^z / d of a pair for bf16 results, folded into one exponent:
-// 2^(z log2 e - log2 d), with neg_log2_d = -log2 d.
+// e^z / d of a pair on the SFU for results rounded to bf16, folded into one
+// exponent: 2^(z log2 e - log2 d), with neg_log2_d = -log2 d.
 __device__ __forceinline__ float2 exp_pair_div(float2 z, float neg_log2_d) {
     const float2 t = fma2(z, splat2(expc::kLog2e), splat2(neg_log2_d));
     return make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
@@ -467,6 +552,14 @@ __device__ __forceinline__ bool cta_wait_bounded(uint64_t* bar, uint32_t parity,
     if (threadIdx.x == 0) flag[which] = mbar_wait_bounded(bar, parity, ctl) ? 1 : 0;
     __syncthreads();
     return flag[which] != 0;
+}
+
+// Asks L2 to fetch [src, src + bytes) from memory ahead of its use, with an
+// eviction policy; nothing reaches this SM and nothing waits for it.  src
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
+                 :: "l"(src), "r"(bytes), "l"(policy) : "memory");
 }
 
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.

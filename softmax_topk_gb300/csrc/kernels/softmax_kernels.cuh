@@ -111,8 +111,6 @@ __device__ __forceinline__ float exp_sum(const float* e, float m) {
     return acc.x + acc.y;
 }
 
-template <typename TO> constexpr bool fast_exp_for() { return sizeof(TO) == 2; }
-
 // Load vector slot v with an L2 eviction policy (aligned rows only).
 template <typename TI>
 __device__ __forceinline__ void load_slot_policy(const TI* row, int64_t v, uint64_t policy,
@@ -518,7 +516,101 @@ struct Chunk {
             }
         }
     }
+
+    // f(pair index, q) for the chunk's pairs, q = 2^((x - m) log2 e + 66)
+    // (exp_biased_pair), m finite and every x <= m + 30.  PACKED (bf16
+    // inputs, |m| < kPackedClampMaxAbs): each word is first clamped from
+    // below at lo2 (packed_clamp_bound(m)) with one packed max, so x - m lies
+    // in [-126, 30]; otherwise x - m is clamped at -110 in fp32.  Either way
+    // a clamped entry (e^-inf included) comes out as exactly +0 once scaled.
+    template <int DEG, bool PACKED, typename F>
+    __device__ __forceinline__ void for_each_biased(float m, uint32_t lo2, F&& f) const {
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+            const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+            if constexpr (sizeof(TI) == 2) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t v = PACKED ? max_bf16x2(w[i], lo2) : w[i];
+                    f(k * 4 + i, exp_biased_pair<DEG, !PACKED>(sub_bf16x2(v, m)));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float2 z = add2(make_float2(__uint_as_float(w[2 * i]),
+                                                      __uint_as_float(w[2 * i + 1])), splat2(-m));
+                    f(k * 2 + i, exp_biased_pair<DEG, true>(z));
+                }
+            }
+        }
+    }
+
+    // bf16 inputs, the shift folded into the exponential: f(pair index, q)
+    // with q = 2^(x log2 e + c_int + 66) (exp_folded_pair with the constant k
+    // of folded_shift(m)), each word first clamped from below at lo2
+    // (packed_clamp_bound(m), |m| < kPackedClampMaxAbs) by one packed max.
+    template <int DEG, typename F>
+    __device__ __forceinline__ void for_each_folded(uint32_t lo2, float2 kk, F&& f) const {
+        static_assert(sizeof(TI) == 2, "bf16 inputs");
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+            const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                f(k * 4 + i, exp_folded_pair<DEG>(unpack_bf16x2(max_bf16x2(w[i], lo2)), kk));
+        }
+    }
+
+    template <int DEG>
+    __device__ __forceinline__ float folded_sum(uint32_t lo2, float2 kk) const {
+        float2 acc = make_float2(0.f, 0.f);
+        for_each_folded<DEG>(lo2, kk, [&](int, float2 q) { acc = add2(acc, q); });
+        return acc.x + acc.y;
+    }
+
+    template <int DEG>
+    __device__ __forceinline__ void folded_scaled(uint32_t lo2, float2 kk, float2 scale,
+                                                  float* e) const {
+        for_each_folded<DEG>(lo2, kk, [&](int j, float2 q) {
+            const float2 y = mul2(q, scale);
+            e[2 * j] = y.x;
+            e[2 * j + 1] = y.y;
+        });
+    }
+
+    // Pass 1: the sum of q over the chunk.
+    template <int DEG, bool PACKED>
+    __device__ __forceinline__ float biased_sum(float m, uint32_t lo2) const {
+        float2 acc = make_float2(0.f, 0.f);
+        for_each_biased<DEG, PACKED>(m, lo2, [&](int, float2 q) { acc = add2(acc, q); });
+        return acc.x + acc.y;
+    }
+
+    // Pass 2: e[2j], e[2j + 1] = q * scale, scale = 2^-66 / d.
+    template <int DEG, bool PACKED>
+    __device__ __forceinline__ void biased_scaled(float m, uint32_t lo2, float2 scale,
+                                                  float* e) const {
+        for_each_biased<DEG, PACKED>(m, lo2, [&](int j, float2 q) {
+            const float2 y = mul2(q, scale);
+            e[2 * j] = y.x;
+            e[2 * j + 1] = y.y;
+        });
+    }
 };
+
+// Packed lower bound of bf16 inputs for a (finite) reference m: m - 118
+// rounded to bf16 in both halves.  For |m| < kPackedClampMaxAbs the rounding
+// moves it by at most 8, so the bound lies at x - m in [-126, -110]: above
+// -132, where 2^((x - m) log2 e + 66) would leave the exponent range, and
+// below -110, where e^(x - m) / d is under 2^-150 and the scaled result is +0.
+constexpr float kPackedClampMaxAbs = 2048.0f;
+__device__ __forceinline__ uint32_t packed_clamp_bound(float m) {
+    return pack_bf16x2(m - 118.0f, m - 118.0f);
+}
+
+// How far a value may lie above a thread's pass-1 reference before the
+// reference moves (e^30: sums of 2^((x - m) log2 e + 66) stay finite).
+constexpr float kRefWindow = 30.0f;
 
 // Which vectors of a CTA's range [begin, begin + len) hold columns below a
 // limit `lim` (the row length, or its causal limit): [0, full) wholly,
@@ -587,18 +679,39 @@ __device__ __forceinline__ void store_stream_chunk(TO* ys, int c, int len, int b
     }
 }
 
-// sum over N entries of e^(z_i), z given: on the SFU (exp_pair<FAST>), or on
-// the FMA pipe without ex2.approx (FMA_EXP, for fp32 results of the
-// two-pass streaming kernel and the three-pass baseline)
-template <int N, bool FAST, bool FMA_EXP = false>
+// sum over N entries of e^(z_i), z given, on the SFU (statistics kernel)
+template <int N, bool FAST>
 __device__ __forceinline__ float exp_sum_z(const float* z) {
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < N; i += 2) {
-        const float2 zz = make_float2(z[i], z[i + 1]);
-        acc = add2(acc, FMA_EXP ? exp_pair_fma(zz) : exp_pair<FAST>(zz));
-    }
+    for (int i = 0; i < N; i += 2) acc = add2(acc, exp_pair<FAST>(make_float2(z[i], z[i + 1])));
     return acc.x + acc.y;
+}
+
+// Degree of the FMA-pipe exponential's 2^f fit by output type: 3 where the
+// results are rounded to bf16, 5 for fp32 results.
+template <typename TO> constexpr int exp_degree() { return sizeof(TO) == 2 ? 3 : 5; }
+
+// sum over N entries of 2^(z_i log2 e + 66), z given (z <= 0): the streaming
+// kernels' pass-1 sum before its one scale by 2^-66 (exp_biased_pair)
+template <int N, int DEG>
+__device__ __forceinline__ float exp_biased_sum(const float* z) {
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) acc = add2(acc, exp_biased_pair<DEG>(make_float2(z[i], z[i + 1])));
+    return acc.x + acc.y;
+}
+
+// y = e^z / d for the N entries of e[] (z in place): q = 2^(z log2 e + 66),
+// times the row's scale 2^-66 / d.
+template <int N, int DEG>
+__device__ __forceinline__ void exp_scale_all(float* e, float2 scale) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        const float2 p = mul2(exp_biased_pair<DEG>(make_float2(e[i], e[i + 1])), scale);
+        e[i] = p.x;
+        e[i + 1] = p.y;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -614,17 +727,22 @@ __device__ __forceinline__ float exp_sum_z(const float* z) {
 // memory by the thread that loaded them, and pass 2 takes them from there.
 // With one CTA per row there is no exchange between SMs at all: each row
 // costs one __syncthreads-level merge.
-// bf16 outputs fold 1/d into the exponent (2^(z log2 e - log2 d), one
-// exponential per element).
+// Every per-element exponential is the FMA-pipe form exp_biased_pair (no
+// ex2.approx): pass 1 sums a chunk's biased values and scales the sum once,
+// pass 2 multiplies each by the row's 2^-66 / d (one product per element
+// normalises and unbiases together).
 // ALIGNED (rows start on 16-byte boundaries) selects 128-bit loads and stores;
 // otherwise the same register layout is filled element by element.  Chunks
 // lying wholly inside the CTA's range skip the per-vector range checks.
-template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER, bool ALIGNED>
+template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER, bool ALIGNED, bool SFU>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
 stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                    int64_t period, int64_t offset) {
+    static_assert(!SFU || sizeof(TO) == 2, "the SFU form serves bf16 results only");
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV;
-    constexpr bool FAST = fast_exp_for<TO>();
+    constexpr int DEG = exp_degree<TO>();             // output pass
+    constexpr int DEG1 = sizeof(TO) == 2 ? 2 : DEG;   // normaliser sum
+    constexpr bool FOLD = sizeof(TI) == 2 && sizeof(TO) == 2;  // bf16 -> bf16
     constexpr int STEP = THREADS * UNROLL;  // vectors per chunk
     constexpr int NS = stream_kept_chunks<TI, THREADS, UNROLL>();
     __shared__ RowMergeSmem<THREADS, CLUSTER> sm;
@@ -652,24 +770,65 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
             load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, begin, lim, policy, ch,
                                                             int(threadIdx.x));
         };
-        // pass 1: running (m, d), one rescale per chunk of UNROLL vectors
+        // pass 1: per thread a state (m, d) with d = sum e^(x - m) over the
+        // elements seen.  m is a reference that moves (d rescaled once) only
+        // when a chunk's maximum exceeds it by more than kRefWindow, which
+        // after the first chunks is rare; the (+) merge takes any such state.
         float m = kNegInf, d = 0.f;
-        for (int c = 0; c < live; ++c) {
-            Chunk<TI, UNROLL> ch;
-            load_chunk(c, keep, ch);
+        float ms = 0.f;                               // finite_shift(m)
+        uint32_t lo2 = packed_clamp_bound(0.f);       // bf16 inputs' packed clamp
+        bool packed = sizeof(TI) == 2;                // |ms| < kPackedClampMaxAbs
+        FoldedShift fs = {splat2(expc::kBiasedRound), expc::kUnbias};  // folded_shift(ms)
+        auto fold_in = [&](const Chunk<TI, UNROLL>& ch, int c) {
             if (c < NS) {  // kept on chip for pass 2 (thread-private slots)
 #pragma unroll
                 for (int k = 0; k < UNROLL; ++k) kept[(c * UNROLL + k) * THREADS + threadIdx.x] = ch.raw[k];
             }
-            const float m_new = fmaxf(m, ch.max());
-            float z[EPC];
-            ch.shifted(m_new, z);
-            d = d * rescale(m, m_new) + exp_sum_z<EPC, FAST, !FAST>(z);
-            m = m_new;
+            const float cm = ch.max();
+            if (__any_sync(kFullMask, cm > m + kRefWindow)) {  // warp-uniform branch
+                if (cm > m + kRefWindow) {
+                    d *= rescale(m, cm);  // m = -inf: d is 0 and stays 0
+                    m = cm;
+                    ms = cm;
+                    lo2 = packed_clamp_bound(cm);
+                    packed = sizeof(TI) == 2 && fabsf(cm) < kPackedClampMaxAbs;
+                    if (FOLD && packed) fs = folded_shift(cm);
+                }
+            }
+            if (__all_sync(kFullMask, packed)) {  // warp-uniform
+                if constexpr (FOLD) d = fmaf(ch.template folded_sum<DEG1>(lo2, fs.k), fs.frac, d);
+                else d = fmaf(ch.template biased_sum<DEG1, true>(ms, lo2), expc::kUnbias, d);
+            } else {
+                d = fmaf(ch.template biased_sum<DEG1, false>(ms, lo2), expc::kUnbias, d);
+            }
+        };
+        for (int c = 0; c < live; ++c) {
+            Chunk<TI, UNROLL> ch;
+            load_chunk(c, keep, ch);
+            if constexpr (SFU) {  // running maximum, one rescale per chunk, ex2 per element
+                if (c < NS) {
+#pragma unroll
+                    for (int k = 0; k < UNROLL; ++k) kept[(c * UNROLL + k) * THREADS + threadIdx.x] = ch.raw[k];
+                }
+                const float m_new = fmaxf(m, ch.max());
+                float z[EPC];
+                ch.shifted(m_new, z);
+                d = d * rescale(m, m_new) + exp_sum_z<EPC, true>(z);
+                m = m_new;
+            } else {
+                fold_in(ch, c);
+            }
         }
         const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m, d, parity, rank);
-        const float2 inv_d = splat2(1.0f / md.y);
-        const float neg_log2_d = -__log2f(md.y);  // bf16 results: 2^(z log2 e - log2 d)
+        const float inv_d = 1.0f / md.y;
+        const float2 scale = splat2(expc::kUnbias * inv_d);  // 2^-66 / d, exact product
+        const float ms2 = finite_shift(md.x);
+        const uint32_t lo2r = packed_clamp_bound(ms2);
+        const bool packed2 = sizeof(TI) == 2 && fabsf(ms2) < kPackedClampMaxAbs;  // uniform
+        FoldedShift fs2 = {splat2(expc::kBiasedRound), expc::kUnbias};
+        if (FOLD && packed2) fs2 = folded_shift(ms2);
+        const float2 fscale = splat2(fs2.frac * inv_d);  // 2^(c_frac - 66) / d
+        const float neg_log2_d = SFU ? -__log2f(md.y) : 0.f;  // SFU: 2^(z log2 e - log2 d)
         // pass 2, last chunk first: y = e^(x - m) / d
         for (int c = nchunks - 1; c >= 0; --c) {
             Chunk<TI, UNROLL> ch;
@@ -680,14 +839,19 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                 load_chunk(c, drop, ch);  // masked chunks: -inf without a load, written as 0
             }
             float e[EPC];
-            ch.shifted(md.x, e);
+            if constexpr (SFU) {
+                ch.shifted(md.x, e);
 #pragma unroll
-            for (int i = 0; i < EPC; i += 2) {
-                const float2 z = make_float2(e[i], e[i + 1]);
-                const float2 p = FAST ? exp_pair_div(z, neg_log2_d)
-                                      : mul2(exp_pair_fma(z), inv_d);
-                e[i] = p.x;
-                e[i + 1] = p.y;
+                for (int i = 0; i < EPC; i += 2) {
+                    const float2 p = exp_pair_div(make_float2(e[i], e[i + 1]), neg_log2_d);
+                    e[i] = p.x;
+                    e[i + 1] = p.y;
+                }
+            } else if (packed2) {
+                if constexpr (FOLD) ch.template folded_scaled<DEG>(lo2r, fs2.k, fscale, e);
+                else ch.template biased_scaled<DEG, true>(ms2, lo2r, scale, e);
+            } else {
+                ch.template biased_scaled<DEG, false>(ms2, lo2r, scale, e);
             }
             store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, len, begin, cols, e);
         }
@@ -701,11 +865,12 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
 // d = sum e^(x - m), pass 3 y = e^(x - m) / d, each pass reading the row from
 // global memory with ordinary (L2-allocating) loads.  A measurement baseline
 // (OS_PATH_SAFE), never chosen by AUTO.  One persistent CTA per row.
-template <typename TI, typename TO, int THREADS, int UNROLL, bool ALIGNED>
+template <typename TI, typename TO, int THREADS, int UNROLL, bool ALIGNED, bool SFU>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
 safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
+    static_assert(!SFU || sizeof(TO) == 2, "the SFU form serves bf16 results only");
     constexpr int EPV = VecTraits<TI>::EPV, EPC = UNROLL * EPV, NW = THREADS / 32;
-    constexpr bool FAST = fast_exp_for<TO>();
+    constexpr int DEG = exp_degree<TO>();
     constexpr int STEP = THREADS * UNROLL;
     __shared__ float red[2][NW];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -746,23 +911,27 @@ safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
                                                             int(threadIdx.x));
             float z[EPC];
             ch.shifted(m, z);
-            d += exp_sum_z<EPC, FAST, !FAST>(z);
+            if constexpr (SFU) d += exp_sum_z<EPC, true>(z);
+            else d += exp_biased_sum<EPC, DEG>(z) * expc::kUnbias;
         }
         d = block_reduce(d, false);
-        const float2 inv_d = splat2(1.0f / d);
-        const float neg_log2_d = -__log2f(d);
+        const float2 scale = splat2(expc::kUnbias * (1.0f / d));
+        const float neg_log2_d = SFU ? -__log2f(d) : 0.f;
         for (int c = 0; c < nchunks; ++c) {  // pass 3: outputs
             Chunk<TI, UNROLL> ch;
             load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, normal, ch,
                                                             int(threadIdx.x));
             float e[EPC];
             ch.shifted(m, e);
+            if constexpr (SFU) {
 #pragma unroll
-            for (int i = 0; i < EPC; i += 2) {
-                const float2 z = make_float2(e[i], e[i + 1]);
-                const float2 p = FAST ? exp_pair_div(z, neg_log2_d) : mul2(exp_pair_fma(z), inv_d);
-                e[i] = p.x;
-                e[i + 1] = p.y;
+                for (int i = 0; i < EPC; i += 2) {
+                    const float2 p = exp_pair_div(make_float2(e[i], e[i + 1]), neg_log2_d);
+                    e[i] = p.x;
+                    e[i + 1] = p.y;
+                }
+            } else {
+                exp_scale_all<EPC, DEG>(e, scale);
             }
             store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, len, 0, cols, e);
         }

@@ -96,21 +96,31 @@ struct SoftmaxFamily {
     static constexpr int STREAM_UNROLL = stream_unroll<TI>();
     using SafeKernel = void (*)(const TI*, TO*, int64_t, int);
     using StreamKernel = void (*)(const TI*, TO*, int64_t, int, int64_t, int64_t);
+    // bf16 results take the SFU exponential in STREAM (and in the SAFE
+    // baseline measured against it); STREAM_POLY and fp32 results the
+    // library's FMA-pipe exponential
+    static constexpr bool SFU_DEFAULT = sizeof(TO) == 2;
     static SafeKernel safe(bool aligned) {
         constexpr int T = kStreamThreads, U = STREAM_UNROLL;
-        return aligned ? safe_rows_kernel<TI, TO, T, U, true> : safe_rows_kernel<TI, TO, T, U, false>;
+        return aligned ? safe_rows_kernel<TI, TO, T, U, true, SFU_DEFAULT>
+                       : safe_rows_kernel<TI, TO, T, U, false, SFU_DEFAULT>;
     }
     static constexpr int stream_smem_bytes() {
         return stream_kept_chunks<TI, kStreamThreads, STREAM_UNROLL>() * kStreamThreads *
                STREAM_UNROLL * 16;
     }
-    static StreamKernel streaming(int cluster, bool aligned) {
+    template <bool SFU>
+    static StreamKernel streaming_as(int cluster, bool aligned) {
         constexpr int T = kStreamThreads, U = STREAM_UNROLL;
         if (aligned)
-            return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, true>
-                                : stream_rows_kernel<TI, TO, T, U, 8, true>;
-        return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, false>
-                            : stream_rows_kernel<TI, TO, T, U, 8, false>;
+            return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, true, SFU>
+                                : stream_rows_kernel<TI, TO, T, U, 8, true, SFU>;
+        return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, false, SFU>
+                            : stream_rows_kernel<TI, TO, T, U, 8, false, SFU>;
+    }
+    static StreamKernel streaming(int cluster, bool aligned, bool poly = false) {
+        if (poly || !SFU_DEFAULT) return streaming_as<false>(cluster, aligned);
+        return streaming_as<SFU_DEFAULT>(cluster, aligned);
     }
 
     // Largest cluster size of the ONCHIP family the current device can run.
@@ -196,7 +206,8 @@ struct SoftmaxFamily {
                 q.grid = min64(rows, kMaxClustersPerLaunch) * q.cluster;
                 break;
             }
-            case OS_PATH_STREAM: {
+            case OS_PATH_STREAM:
+            case OS_PATH_STREAM_POLY: {
                 q.threads = kStreamThreads;
                 q.vectors_per_thread = STREAM_UNROLL;
                 q.cluster = rows >= int64_t(dev->sms) ? 1 : 8;  // measured: 1 CTA per row wins from one row per SM up
@@ -243,8 +254,8 @@ struct SoftmaxFamily {
             if (!prepare_kernel(k, 1, 0)) return cudaErrorInvalidValue;
             return launch_kernel(k, p.grid, p.threads, 1, 0, stream, xi, yo, rows, cols);
         }
-        if (p.path == OS_PATH_STREAM) {
-            StreamKernel k = streaming(p.cluster, aligned);
+        if (p.path == OS_PATH_STREAM || p.path == OS_PATH_STREAM_POLY) {
+            StreamKernel k = streaming(p.cluster, aligned, p.path == OS_PATH_STREAM_POLY);
             const int smem = stream_smem_bytes();
             if (!prepare_kernel(k, p.cluster, smem)) return cudaErrorInvalidValue;
             return launch_kernel(k, p.grid, p.threads, p.cluster, smem, stream, xi, yo, rows, cols,

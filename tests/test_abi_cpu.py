@@ -182,6 +182,10 @@ def test_exp_argument_errors(lib):
     assert lib.os_exp_pairs_f32(None, B, 5, None) == NULL
     assert lib.os_exp_pairs_f32(A, B + 2, 5, None) == ALIGN
     assert lib.os_exp_pairs_f32(None, None, 0, None) == OK
+    assert lib.os_exp_pairs_coarse_f32(A, B, -1, None) == SHAPE
+    assert lib.os_exp_pairs_coarse_f32(None, B, 5, None) == NULL
+    assert lib.os_exp_pairs_coarse_f32(A, B + 2, 5, None) == ALIGN
+    assert lib.os_exp_pairs_coarse_f32(None, None, 0, None) == OK
 
 
 def test_testing_controls_validate(lib):

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 PAIRS = [("f32", "f32"), ("bf16", "bf16"), ("f32", "bf16"), ("bf16", "f32")]
-PATHS = ["auto", "warp", "onchip", "stream", "safe"]
+PATHS = ["auto", "warp", "onchip", "stream", "safe", "stream_poly"]
 COLS = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256,
         257, 511, 512, 513, 1023, 1024, 1025, 2047, 2048, 2049, 4095, 4096, 4097, 8191, 8192,
         8193, 16383, 16384, 16385, 32000, 32768, 32769, 50257, 65535, 65536, 65537, 128256,
@@ -63,7 +63,7 @@ def test_cols_sweep_auto(st, cols, pair):
 
 
 @pytest.mark.parametrize("cols", COLS)
-@pytest.mark.parametrize("path", ["warp", "onchip", "stream", "safe"])
+@pytest.mark.parametrize("path", ["warp", "onchip", "stream", "safe", "stream_poly"])
 @pytest.mark.parametrize("pair", [("f32", "f32"), ("bf16", "bf16")], ids=lambda p: f"{p[0]}-{p[1]}")
 def test_cols_sweep_forced_path(st, cols, path, pair):
     rows = 3 if cols > 100000 else 6
@@ -170,6 +170,42 @@ def test_workload_full_size_all_rows(st, name):
         assert torch.all(y[::128, 0] == 1.0) and torch.all(y[::128, 1:] == 0)
     y2 = st.softmax(x)
     assert torch.equal(y, y2), "two runs on the same input differ"
+
+
+@pytest.mark.parametrize("name", ["softmax_8192x128256_bf16"])
+def test_workload_full_size_poly_path(st, name):
+    """The ex2.approx-free streaming kernel for bf16 results at full size:
+    every row against the oracle, row sums, and agreement with the SFU kernel
+    within both tolerances."""
+    w = workloads.WORKLOADS[name]
+    x = workloads.make(w, device="cuda")
+    y = st.softmax(x, path="stream_poly")
+    torch.cuda.synchronize()
+    block = max(1, (1 << 26) // w.cols)
+    for r0 in range(0, w.rows, block):
+        r1 = min(w.rows, r0 + block)
+        xs = x[r0:r1].double().cpu().numpy()
+        assert_softmax_close(xs, y[r0:r1].double().cpu().numpy(), oracle.softmax(xs), w.dtype,
+                             f"{name} poly rows {r0}..{r1 - 1}")
+    sums = y.double().sum(dim=1)
+    assert float((sums - 1).abs().max()) <= SUM_TOL[w.dtype]
+
+
+@pytest.mark.parametrize("path", ["stream", "stream_poly", "safe"])
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+def test_large_magnitude_rows(st, pair, path):
+    """Rows whose maximum lies far from 0 (|m| from 1000 to 1e6, both signs):
+    the bf16 kernels bound their inputs on packed pairs only while |m| < 2048
+    and take the fp32 bound beyond; the folded shift must carry m log2 e
+    exactly enough either way.  Spread of 60 below the maximum, a few -inf."""
+    rows, cols = 10, 40000
+    rng = np.random.default_rng(23)
+    x64 = -rng.uniform(0.0, 60.0, size=(rows, cols))
+    x64[:, 777] = 0.0
+    x64[:, 100:110] = -np.inf
+    x64 += np.array([1000.0, -1000.0, 2040.0, 2100.0, -2100.0, 5000.0, 3e4, -3e4, 1e6, -1e6])[:, None]
+    x = torch.tensor(x64, dtype=torch.float64).to(DT[pair[0]]).cuda()
+    _check(st, x, pair[1], path, f"large magnitudes {pair} {path}")
 
 
 def test_edge_rows(st):
