@@ -385,14 +385,18 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
     const Cand pad{kNegInf, kNoIndex};
     const uint64_t policy = l2_policy_evict_first();
 
-    if (tid == 0) {
-        mbar_init(&sm.xbar[0], 1);
-        mbar_init(&sm.xbar[1], 1);
-        mbar_init_fence();
-        sm.ncand[0] = sm.ncand[1] = 0;
-        sm.nflag[0] = sm.nflag[1] = 0;
+    // The exchange barriers exist only for a row split over a cluster.  With
+    // one CTA per row nothing here needs a CTA barrier: thread 0 clears a
+    // row's counters before its pass 1, and every other thread first uses
+    // them after the threshold barrier that follows.
+    if (S > 1) {
+        if (tid == 0) {
+            mbar_init(&sm.xbar[0], 1);
+            mbar_init(&sm.xbar[1], 1);
+            mbar_init_fence();
+        }
+        cluster_sync();
     }
-    if (S > 1) cluster_sync(); else __syncthreads();
 
     bool failed = false;  // a wait gave up: outputs are garbage, the status word says so
     int parity = 0;
