@@ -17,7 +17,14 @@ Also printed: `e2e` (the same metric through the public API with pinned host
 buffers: host->device copy of every input and device->host copy of every
 output inside the timed region), `roofline` of the dominant kernel,
 `cpu_baseline` (the float64 oracle on the host cores on a bounded sample),
-`clocks` (nvidia-smi samples taken during the timed region).
+`clocks` (nvidia-smi samples taken during the timed region),
+`per_workload` (each launch of the step, and after the step, in loops of
+their own, the other configurations -- 64x1024 fp32, causal 1048576x128,
+increasing 65536x4096 --, rows that are not whole 16-byte vectors (4096 x 50257
+fp32) and the ex2.approx-free kernel on the bf16 workload),
+`unfused_baselines` (three-pass safe softmax against the online kernel,
+softmax-then-TopK against the fused kernel) and, inside `e2e`, the plain
+pinned copy rates of the host link.
 
 `--impl reference` times the oracle alone (the reference arm: the method's
 own definition run on the host cores), on the same metric.
@@ -271,6 +278,8 @@ def run_ours(args):
     value = multi.whole_job_rate(step_bytes, world, ms_per_step * 1e-3) / 1e9
 
     e2e = run_e2e(st, dev, args) if rank == 0 else None
+    others = time_other_workloads(st, dev, args) if rank == 0 else None
+    baselines = run_baselines(st, dev, args) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
     if rank != 0:
@@ -301,7 +310,7 @@ def run_ours(args):
                    "l2": f"softmax inputs larger than L2; TopK input rotated over {topk_copies} "
                          "copies (> 3x L2)",
                    "parallelism": f"replicas x{world} (rows are independent; no collective)"},
-        "per_workload": per,
+        "per_workload": {**per, **(others or {})},
         "rows_per_s": {k: v["rows_per_s"] for k, v in per.items()},
         "roofline": {"kernel": kernel_name, "workload": dom_label, "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -311,9 +320,9 @@ def run_ours(args):
         "e2e": e2e,
         "clocks": clock_info,
     }
+    line["unfused_baselines"] = baselines
     if args.extra:
         line["extra_workloads"] = run_extra(st, dev, args)
-        line["unfused_baselines"] = run_baselines(st, dev, args)
         line["stats_and_causal"] = run_stats_and_causal(st, dev, args)
         line["attention"] = run_attention(st, dev, args, rank == 0 and world == 1 and
                                           not args.no_cpu_baseline)
@@ -324,14 +333,88 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def kernel_of(st, label: str) -> str:
+OTHER_WORKLOADS = ["softmax_64x1024_f32", "causal_1048576x128_f32", "increasing_65536x4096_f32",
+                   "softmax_4096x50257_f32"]
+
+
+def time_other_workloads(st, dev, args) -> dict:
+    """The configurations outside the step (its parity cases) and the
+    ex2.approx-free kernel on the step's bf16 workload, each timed in a loop
+    of its own after the step: W warm-up launches, then K launches between
+    CUDA events on the launching stream; inputs smaller than 3x L2 rotate over
+    enough copies that no timed launch reads a cache-resident input."""
+    out = {}
+    peak, _ = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    steps = max(args.steps, 10)
+    cases = [(n, "auto") for n in OTHER_WORKLOADS] + [("softmax_8192x128256_bf16", "stream_poly")]
+    for n, path in cases:
+        w = workloads.WORKLOADS[n]
+        x = workloads.make(w, device=dev)
+        nbytes = x.numel() * x.element_size()
+        copies = -(-3 * l2 // nbytes) + 1 if nbytes < 3 * l2 else 1
+        xs = [x] + [x.clone() for _ in range(copies - 1)]
+        y = torch.empty_like(x)
+        ms = _time_ms(lambda i: st.softmax(xs[i % copies], out=y, path=path), dev, steps,
+                      warmup=args.warmup)
+        b = softmax_bytes(w)
+        gbs = b / (ms * 1e-3) / 1e9
+        key = n if path == "auto" else f"{n}_{path}"
+        out[key] = {"ms": round(ms, 5), "gbs": round(gbs, 1), "rows_per_s": round(w.rows / (ms * 1e-3), 1),
+                    "frac_of_measured_hbm": round(gbs / peak, 4),
+                    "frac_of_8tbs_nominal": round(gbs / 8000.0, 4),
+                    "kernel": kernel_of(st, n, path), "input_copies": copies,
+                    "timing": "own loop after the step"}
+        if n == "softmax_64x1024_f32":
+            out[key]["note"] = ("0.5 MB per launch: bound by launch overhead, not by HBM "
+                                "(no roofline target)")
+        del xs, x, y
+    return out
+
+
+def link_rates(dev, nbytes: int = 1 << 30) -> dict:
+    """Plain pinned host<->device copy rates in this process (one copy per
+    direction, then both directions at once on two streams): the bound of
+    the e2e leg, whose every step moves its inputs and results over this link."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t) / reps
+
+    t_h2d = timed(lambda: d.copy_(h, non_blocking=True))
+    t_d2h = timed(lambda: h.copy_(d, non_blocking=True))
+
+    def both():
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+    t_both = timed(both)
+    return {"h2d_gbs": round(nbytes / t_h2d / 1e9, 1), "d2h_gbs": round(nbytes / t_d2h / 1e9, 1),
+            "both_directions_gbs": round(2 * nbytes / t_both / 1e9, 1),
+            "bytes_per_copy": nbytes, "how": "torch copy_ of pinned uint8 buffers, wall clock "
+                                             "over 5 copies after one untimed"}
+
+
+def kernel_of(st, label: str, path: str = "auto") -> str:
     if label.startswith("topk"):
         return "topk_rows_kernel"
     w = workloads.WORKLOADS[label]
     code = st.OS_F32 if w.dtype == "f32" else st.OS_BF16
-    p = st.plan((w.rows, w.cols), code)
+    p = st.plan((w.rows, w.cols), code, path=path)
     fam = {st.OS_PATH_WARP: "warp_rows_kernel", st.OS_PATH_ONCHIP: "onchip_rows_kernel",
-           st.OS_PATH_STREAM: "stream_rows_kernel"}[p["path"]]
+           st.OS_PATH_STREAM: "stream_rows_kernel",
+           st.OS_PATH_STREAM_POLY: "stream_rows_kernel[fma-pipe exp]"}[p["path"]]
     if p["path"] == st.OS_PATH_ONCHIP and p["stages"] > 0:
         fam = "tma_rows_kernel"
     return f"{fam}<{w.dtype},{w.dtype},threads={p['threads']},cluster={p['cluster']}>"
@@ -414,9 +497,17 @@ def run_e2e(st, dev, args):
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
     step_bytes = sum(u[1] for u in step_units())
+    del host_in, host_out, dev_in, dev_out, dev_xt, dev_topk, xt, topk_out, pieces
+    link = link_rates(dev)
+    # the host link alone, at the rates measured above, with both directions
+    # overlapped as the pipeline overlaps them: the bound of this leg
+    link_ms = max((h2d + d2h) / (link["both_directions_gbs"] * 1e9),
+                  h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9)) * 1e3
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "link": link, "link_bound_ms_per_step": round(link_ms, 4),
+            "frac_of_link_bound": round(link_ms / ms, 4)}
 
 
 def run_extra(st, dev, args):
@@ -450,10 +541,10 @@ def run_extra(st, dev, args):
     return out
 
 
-def _time_ms(fn, dev, steps):
+def _time_ms(fn, dev, steps, warmup: int = 3):
     stream = torch.cuda.current_stream(dev)
-    for _ in range(3):
-        fn(0)
+    for i in range(max(3, warmup)):
+        fn(i)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)

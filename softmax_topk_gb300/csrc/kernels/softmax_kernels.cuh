@@ -612,71 +612,141 @@ __device__ __forceinline__ uint32_t packed_clamp_bound(float m) {
 // reference moves (e^30: sums of 2^((x - m) log2 e + 66) stay finite).
 constexpr float kRefWindow = 30.0f;
 
-// Which vectors of a CTA's range [begin, begin + len) hold columns below a
-// limit `lim` (the row length, or its causal limit): [0, full) wholly,
-// [full, any) in part.
-struct VecLimits {
-    int full, any;
-};
-template <int EPV>
-__device__ __forceinline__ VecLimits vec_limits(int len, int begin, int lim) {
-    // (lim + EPV - 1) / EPV in 64 bits: lim can be 2^31 - 1
-    const int lim_v = int((int64_t(lim) + EPV - 1) / EPV);
-    return {min(len, max(0, lim / EPV - begin)), min(len, max(0, lim_v - begin))};
+// A row's vector slots.  Slot u of a row covers its columns
+// [u EPV - head, u EPV - head + EPV): head (0 .. EPV - 1) is the number of
+// elements between the start of the row's first 16-byte block of memory and
+// the row itself, so every slot is one aligned 16-byte block.  Rows whose
+// start is aligned (head = 0) have ceil(cols / EPV) slots; otherwise the
+// first and last slots hold columns of neighbouring rows, which are never
+// read or written.
+template <typename T>
+__device__ __forceinline__ int row_head(const T* row) {
+    return int((reinterpret_cast<uintptr_t>(row) & 15u) / sizeof(T));
 }
 
-// Vectors t + k*GROUP (k < UNROLL) of chunk c of a CTA's range that starts
-// at vector `begin` of the row (xs points at that vector).  Columns at or
-// past `lim` read as -inf; vectors wholly past it are not loaded at all.
+// Which slots of a CTA's range [begin, begin + len) hold columns below a
+// limit `lim` (the row length, or its causal limit): [lo, full) wholly,
+// [0, lo) and [full, any) in part, none from `any` on.
+struct VecLimits {
+    int lo, full, any;
+};
+template <int EPV, bool ALIGNED = false>
+__device__ __forceinline__ VecLimits vec_limits(int len, int begin, int lim, int head) {
+    if constexpr (ALIGNED) {  // head = 0
+        const int lim_v = int((int64_t(lim) + EPV - 1) / EPV);  // lim can be 2^31 - 1
+        return {0, min(len, max(0, lim / EPV - begin)), min(len, max(0, lim_v - begin))};
+    } else {  // in 64 bits: lim + head can pass 2^31
+        const int64_t whole = (int64_t(lim) + head) / EPV;           // slots ending by lim
+        const int64_t some = (int64_t(lim) + head + EPV - 1) / EPV;  // slots starting before lim
+        auto rel = [&](int64_t u) { return int(min(int64_t(len), max(int64_t(0), u - begin))); };
+        return {rel(head > 0 ? 1 : 0), rel(whole), rel(some)};
+    }
+}
+
+// Slots t + k*GROUP (k < UNROLL) of chunk c of a CTA's range that starts at
+// slot `begin` of a row; xs points at that slot's first element (16-byte
+// aligned: the row start minus head, plus begin slots).  Columns at or past `lim` read
+// as -inf; slots wholly inside [0, lim) are read with one 16-byte load, the
+// rest element by element, slots wholly past lim not at all.  ALIGNED: the
+// row starts on a 16-byte boundary (head = 0) and cols is a whole number of
+// slots, so only causal limits leave partial slots.  Vector addresses are a
+// per-row base plus 32-bit slot offsets (slot offsets stay below 2^31:
+// (begin + v) EPV - head < cols + EPV).
 template <typename TI, int GROUP, int UNROLL, bool ALIGNED>
 __device__ __forceinline__ void load_stream_chunk(const TI* xs, int c, VecLimits vl, int begin,
-                                                  int lim, uint64_t policy, Chunk<TI, UNROLL>& ch,
-                                                  int t) {
+                                                  int lim, int head, uint64_t policy,
+                                                  Chunk<TI, UNROLL>& ch, int t) {
     constexpr int EPV = VecTraits<TI>::EPV, STEP = GROUP * UNROLL;
     const int v0 = c * STEP + t;
-    const bool full = c * STEP + STEP <= vl.full;
     const uint32_t neg_inf_word = sizeof(TI) == 2 ? 0xff80ff80u : 0xff800000u;
+    if constexpr (ALIGNED) {
+        const bool full = c * STEP + STEP <= vl.full;
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-        const int v = v0 + k * GROUP;
-        if (ALIGNED && (full || v < vl.full)) {
-            ch.raw[k] = ld_coherent_policy_v4(xs + v * EPV, policy);
-        } else if (full || v < vl.any) {
-            TI tmp[EPV];
+        for (int k = 0; k < UNROLL; ++k) {
+            const int v = v0 + k * GROUP;
+            if (full || v < vl.full) {
+                ch.raw[k] = ld_coherent_policy_v4(xs + v * EPV, policy);
+            } else if (v < vl.any) {  // the slot a causal limit cuts
+                TI tmp[EPV];
 #pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                const int j = (begin + v) * EPV + q;
-                tmp[q] = j < lim ? xs[v * EPV + q] : from_f32<TI>(kNegInf);
+                for (int q = 0; q < EPV; ++q) {
+                    const int j = (begin + v) * EPV + q;
+                    tmp[q] = j < lim ? xs[v * EPV + q] : from_f32<TI>(kNegInf);
+                }
+                ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
+            } else {
+                ch.raw[k] = make_uint4(neg_inf_word, neg_inf_word, neg_inf_word, neg_inf_word);
             }
-            ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
-        } else {
-            ch.raw[k] = make_uint4(neg_inf_word, neg_inf_word, neg_inf_word, neg_inf_word);
+        }
+    } else {
+        const bool full = c * STEP >= vl.lo && c * STEP + STEP <= vl.full;
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+            const int v = v0 + k * GROUP;
+            if (full || (v >= vl.lo && v < vl.full)) {
+                ch.raw[k] = ld_coherent_policy_v4(xs + v * EPV, policy);
+            } else if (v < vl.any) {
+                TI tmp[EPV];
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) {
+                    const int64_t j = int64_t(begin + v) * EPV + q - head;  // column
+                    tmp[q] = j >= 0 && j < lim ? xs[int64_t(v) * EPV + q] : from_f32<TI>(kNegInf);
+                }
+                ch.raw[k] = *reinterpret_cast<const uint4*>(tmp);
+            } else {
+                ch.raw[k] = make_uint4(neg_inf_word, neg_inf_word, neg_inf_word, neg_inf_word);
+            }
         }
     }
 }
 
-// Stores the UNROLL * EPV values e of chunk c (same slots as load_stream_chunk).
+// Stores the UNROLL * EPV values e of chunk c (same slots as load_stream_chunk)
+// through ys (slot `begin` of the output row): columns [0, cols) only; slots wholly inside by vector
+// stores when `vec` (the output row has the input's block phase: the slot's
+// first column is suitably aligned in y too), element by element otherwise.
 template <typename TO, int THREADS, int UNROLL, int EPV, bool ALIGNED>
-__device__ __forceinline__ void store_stream_chunk(TO* ys, int c, int len, int begin, int cols,
-                                                   const float* e) {
+__device__ __forceinline__ void store_stream_chunk(TO* ys, int c, VecLimits vl, int begin,
+                                                   int cols, int head, bool vec, const float* e) {
     constexpr int STEP = THREADS * UNROLL;
     const int v0 = c * STEP + int(threadIdx.x);
-    const bool full = c * STEP + STEP <= len;
+    if constexpr (ALIGNED) {  // every slot is whole: vl.full slots, all stored as vectors
+        const bool full = c * STEP + STEP <= vl.full;
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-        const int v = v0 + k * THREADS;
-        if (full || v < len) {
-            if constexpr (ALIGNED) {
+        for (int k = 0; k < UNROLL; ++k) {
+            const int v = v0 + k * THREADS;
+            if (full || v < vl.full) VecStore<TO, EPV>::run(ys + v * EPV, e + k * EPV);
+        }
+    } else {
+        const bool full = vec && c * STEP >= vl.lo && c * STEP + STEP <= vl.full;
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+            const int v = v0 + k * THREADS;
+            if (full || (vec && v >= vl.lo && v < vl.full)) {
                 VecStore<TO, EPV>::run(ys + v * EPV, e + k * EPV);
-            } else {
+            } else if (v < vl.any) {
 #pragma unroll
                 for (int q = 0; q < EPV; ++q) {
-                    const int j = (begin + v) * EPV + q;
-                    if (j < cols) ys[v * EPV + q] = from_f32<TO>(e[k * EPV + q]);
+                    const int64_t j = int64_t(begin + v) * EPV + q - head;
+                    if (j >= 0 && j < cols) ys[int64_t(v) * EPV + q] = from_f32<TO>(e[k * EPV + q]);
                 }
             }
         }
     }
+}
+
+// Slots per row: every row has the same number, that of the worst head.
+template <int EPV, bool ALIGNED>
+__device__ __forceinline__ int row_slots(int cols) {  // cols can be 2^31 - 1
+    return int((int64_t(cols) + (ALIGNED ? EPV - 1 : 2 * EPV - 2)) / EPV);
+}
+
+// Whether the output row yr can take vector stores for input slots of a row
+// with this head: the slot's first column lands on an address aligned to the
+// store width (EPV outputs, at most 16 bytes).
+template <typename TO, int EPV>
+__device__ __forceinline__ bool out_vec_ok(const TO* yr, int head) {
+    constexpr uintptr_t A = EPV * sizeof(TO) < 16 ? EPV * sizeof(TO) : 16;
+    return ((reinterpret_cast<uintptr_t>(yr) - uintptr_t(head) * sizeof(TO)) & (A - 1)) == 0;
 }
 
 // sum over N entries of e^(z_i), z given, on the SFU (statistics kernel)
@@ -731,9 +801,10 @@ __device__ __forceinline__ void exp_scale_all(float* e, float2 scale) {
 // ex2.approx): pass 1 sums a chunk's biased values and scales the sum once,
 // pass 2 multiplies each by the row's 2^-66 / d (one product per element
 // normalises and unbiases together).
-// ALIGNED (rows start on 16-byte boundaries) selects 128-bit loads and stores;
-// otherwise the same register layout is filled element by element.  Chunks
-// lying wholly inside the CTA's range skip the per-vector range checks.
+// Every slot wholly inside the row moves with one 128-bit load and store;
+// ALIGNED (rows start on 16-byte boundaries and are whole slots) drops the
+// per-row head and output-phase arithmetic.  Chunks lying wholly inside the
+// row skip the per-slot range checks.
 template <typename TI, typename TO, int THREADS, int UNROLL, int CLUSTER, bool ALIGNED, bool SFU>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2 > 0 ? 2048 / THREADS / 2 : 1)
 stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
@@ -749,7 +820,7 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
     extern __shared__ uint4 kept[];  // [NS][UNROLL][THREADS]: the row's first chunks, raw
     const uint32_t rank = CLUSTER > 1 ? cluster_rank() : 0;
     const int64_t cluster_id = blockIdx.x / CLUSTER, nclusters = gridDim.x / CLUSTER;
-    const int nv = int((int64_t(cols) + EPV - 1) / EPV);  // cols can be 2^31 - 1
+    const int nv = row_slots<EPV, ALIGNED>(cols);
     const int per_cta = (nv + CLUSTER - 1) / CLUSTER;
     const int begin = int(rank) * per_cta;
     const int len = max(0, min(per_cta, nv - begin));  // vectors of this CTA
@@ -759,15 +830,21 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
 
     int parity = 0;
     for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
-        const TI* xs = x + row * int64_t(cols) + int64_t(begin) * EPV;
-        TO* ys = y + row * int64_t(cols) + int64_t(begin) * EPV;
+        const TI* xr = x + row * int64_t(cols);
+        TO* yr = y + row * int64_t(cols);
+        const int head = ALIGNED ? 0 : row_head(xr);
+        const bool yvec = ALIGNED || out_vec_ok<TO, EPV>(yr, head);
+        const TI* xs = xr + (int64_t(begin) * EPV - head);  // the CTA's first slot
+        TO* ys = yr + (int64_t(begin) * EPV - head);
         // columns at or past `lim` are masked (-inf, never read): chunks from
         // `live` on hold none of this CTA's unmasked columns
         const int lim = causal_limit(row, cols, period, offset);
-        const VecLimits vl = vec_limits<EPV>(len, begin, lim);
+        const VecLimits vl = vec_limits<EPV, ALIGNED>(len, begin, lim, head);
+        // output slots: for aligned rows every one of the CTA's len slots is whole
+        const VecLimits vo = ALIGNED ? VecLimits{0, len, len} : vec_limits<EPV, ALIGNED>(len, begin, cols, head);
         const int live = (vl.any + STEP - 1) / STEP;
         auto load_chunk = [&](int c, uint64_t policy, Chunk<TI, UNROLL>& ch) {
-            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, begin, lim, policy, ch,
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, begin, lim, head, policy, ch,
                                                             int(threadIdx.x));
         };
         // pass 1: per thread a state (m, d) with d = sum e^(x - m) over the
@@ -802,7 +879,11 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                 d = fmaf(ch.template biased_sum<DEG1, false>(ms, lo2), expc::kUnbias, d);
             }
         };
+        // a warp whose slots of chunk c all lie past the row's last column
+        // (the ragged last chunk) skips it in both passes
+        const int warp_first = int(threadIdx.x) & ~31;
         for (int c = 0; c < live; ++c) {
+            if (c * STEP + warp_first >= vl.any) break;  // warp-uniform; later chunks too
             Chunk<TI, UNROLL> ch;
             load_chunk(c, keep, ch);
             if constexpr (SFU) {  // running maximum, one rescale per chunk, ex2 per element
@@ -831,8 +912,10 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
         const float neg_log2_d = SFU ? -__log2f(md.y) : 0.f;  // SFU: 2^(z log2 e - log2 d)
         // pass 2, last chunk first: y = e^(x - m) / d
         for (int c = nchunks - 1; c >= 0; --c) {
+            if (c * STEP + warp_first >= vo.any) continue;  // nothing to load or store
             Chunk<TI, UNROLL> ch;
-            if (c < NS && c < live) {
+            // kept on chip only if this warp took part in chunk c in pass 1
+            if (c < NS && c * STEP + warp_first < vl.any) {
 #pragma unroll
                 for (int k = 0; k < UNROLL; ++k) ch.raw[k] = kept[(c * UNROLL + k) * THREADS + threadIdx.x];
             } else {
@@ -853,7 +936,7 @@ stream_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
             } else {
                 ch.template biased_scaled<DEG, false>(ms2, lo2r, scale, e);
             }
-            store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, len, begin, cols, e);
+            store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, vo, begin, cols, head, yvec, e);
         }
     }
 }
@@ -874,7 +957,7 @@ safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
     constexpr int STEP = THREADS * UNROLL;
     __shared__ float red[2][NW];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int len = int((int64_t(cols) + EPV - 1) / EPV);  // cols can be 2^31 - 1
+    const int len = row_slots<EPV, ALIGNED>(cols);
     const int nchunks = (len + STEP - 1) / STEP;
     const uint64_t normal = l2_policy_evict_normal();
     int rb = 0;  // alternate reduction buffers: one barrier per reduction
@@ -893,13 +976,17 @@ safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
         return r;
     };
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        const TI* xs = x + row * int64_t(cols);
-        TO* ys = y + row * int64_t(cols);
-        const VecLimits vl = vec_limits<EPV>(len, 0, cols);
+        const TI* xr = x + row * int64_t(cols);
+        TO* yr = y + row * int64_t(cols);
+        const int head = ALIGNED ? 0 : row_head(xr);
+        const bool yvec = ALIGNED || out_vec_ok<TO, EPV>(yr, head);
+        const VecLimits vl = vec_limits<EPV, ALIGNED>(len, 0, cols, head);
+        const TI* xs = xr - head;  // the row's first slot
+        TO* ys = yr - head;
         float m = kNegInf;
         for (int c = 0; c < nchunks; ++c) {  // pass 1: maximum
             Chunk<TI, UNROLL> ch;
-            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, normal, ch,
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, head, normal, ch,
                                                             int(threadIdx.x));
             m = fmaxf(m, ch.max());
         }
@@ -907,7 +994,7 @@ safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
         float d = 0.f;
         for (int c = 0; c < nchunks; ++c) {  // pass 2: normalizer
             Chunk<TI, UNROLL> ch;
-            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, normal, ch,
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, head, normal, ch,
                                                             int(threadIdx.x));
             float z[EPC];
             ch.shifted(m, z);
@@ -919,7 +1006,7 @@ safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
         const float neg_log2_d = SFU ? -__log2f(d) : 0.f;
         for (int c = 0; c < nchunks; ++c) {  // pass 3: outputs
             Chunk<TI, UNROLL> ch;
-            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, normal, ch,
+            load_stream_chunk<TI, THREADS, UNROLL, ALIGNED>(xs, c, vl, 0, cols, head, normal, ch,
                                                             int(threadIdx.x));
             float e[EPC];
             ch.shifted(m, e);
@@ -933,7 +1020,7 @@ safe_rows_kernel(const TI* x, TO* y, int64_t rows, int cols) {
             } else {
                 exp_scale_all<EPC, DEG>(e, scale);
             }
-            store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, len, 0, cols, e);
+            store_stream_chunk<TO, THREADS, UNROLL, EPV, ALIGNED>(ys, c, vl, 0, cols, head, yvec, e);
         }
     }
 }
@@ -956,17 +1043,18 @@ stats_rows_kernel(const TI* __restrict__ x, float* __restrict__ m_out, float* __
     const int t = int(threadIdx.x) % GROUP;
     const int64_t g0 = int64_t(blockIdx.x) * GPC + threadIdx.x / GROUP;
     const int64_t ng = int64_t(gridDim.x) * GPC;
-    const int len = int((int64_t(cols) + EPV - 1) / EPV);  // cols can be 2^31 - 1
+    const int len = row_slots<EPV, ALIGNED>(cols);
     const int nchunks = (len + STEP - 1) / STEP;
-    const VecLimits vl = vec_limits<EPV>(len, 0, cols);
     const uint64_t policy = l2_policy_evict_first();  // read once
     int parity = 0;
     for (int64_t row = g0; row < rows; row += ng, parity ^= 1) {  // uniform per group
-        const TI* xs = x + row * int64_t(cols);
+        const TI* xr = x + row * int64_t(cols);
+        const int head = ALIGNED ? 0 : row_head(xr);
+        const VecLimits vl = vec_limits<EPV, ALIGNED>(len, 0, cols, head);
         float m = kNegInf, d = 0.f;
         for (int c = 0; c < nchunks; ++c) {
             Chunk<TI, UNROLL> ch;
-            load_stream_chunk<TI, GROUP, UNROLL, ALIGNED>(xs, c, vl, 0, cols, policy, ch, t);
+            load_stream_chunk<TI, GROUP, UNROLL, ALIGNED>(xr - head, c, vl, 0, cols, head, policy, ch, t);
             const float m_new = fmaxf(m, ch.max());
             float z[EPC];
             ch.shifted(m_new, z);

@@ -34,3 +34,11 @@ def test_bench_line_keeps_the_contract():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 4 * d["steps"]  # two softmax launches and two TopK per step
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    pw = d["per_workload"]
+    for key in ("softmax_4096x32000_f32", "softmax_8192x128256_bf16", "topk_256x50257_f32_K8",
+                "topk_256x50257_f32_K64", "softmax_64x1024_f32", "causal_1048576x128_f32",
+                "increasing_65536x4096_f32", "softmax_4096x50257_f32",
+                "softmax_8192x128256_bf16_stream_poly"):
+        assert pw[key]["gbs"] > 0 and pw[key]["ms"] > 0, key
+    assert e["link"]["h2d_gbs"] > 0 and e["link"]["d2h_gbs"] > 0 and e["frac_of_link_bound"] > 0
+    assert d["unfused_baselines"]["softmax_4096x32000_f32"]["safe_over_online"] > 0

@@ -304,6 +304,38 @@ def test_misaligned_pointers(st, pair, cols):
     assert float(ybuf[0]) == 0.0 and torch.all(ybuf[1 + rows * cols:] == 0)
 
 
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+@pytest.mark.parametrize("xoff,yoff", [(0, 0), (1, 1), (0, 3), (2, 1), (3, 0)])
+@pytest.mark.parametrize("path", ["auto", "stream", "safe", "stream_poly"])
+def test_rows_not_whole_vectors(st, pair, xoff, yoff, path):
+    """Rows of 50257 and 16387 columns: every row starts at another offset in
+    its 16-byte block, so the kernels peel the partial blocks at both ends and
+    move the rest with 128-bit accesses; the output may have the input's block
+    phase (vector stores) or not (element stores).  300 rows: persistent CTAs
+    walk many rows and every head occurs; guard elements stay untouched."""
+    for cols in (50257, 16387):
+        rows = 300 if cols > 20000 else 40
+        xin, xout = DT[pair[0]], DT[pair[1]]
+        xbuf = torch.empty(rows * cols + 8, dtype=xin, device="cuda")
+        ybuf = torch.full((rows * cols + 8,), 7.0, dtype=xout, device="cuda")
+        x = xbuf[xoff:xoff + rows * cols].view(rows, cols)
+        x.copy_(_inputs(rows, cols, pair[0], seed=cols + xoff))
+        y = ybuf[yoff:yoff + rows * cols].view(rows, cols)
+        in_code = 0 if pair[0] == "f32" else 1
+        out_code = 0 if pair[1] == "f32" else 1
+        try:
+            st.os_softmax_fwd_path(x.data_ptr(), y.data_ptr(), rows, cols, in_code, out_code,
+                                   st.PATHS[path], torch.cuda.current_stream().cuda_stream)
+        except st.OsError as e:
+            assert e.name == "OS_ERR_PATH"
+            continue
+        torch.cuda.synchronize()
+        xx = x.double().cpu().numpy()
+        assert_softmax_close(xx, y.double().cpu().numpy(), oracle.softmax(xx), pair[1],
+                             f"{path} {pair} offsets {xoff}/{yoff} cols={cols}")
+        assert torch.all(ybuf[:yoff] == 7.0) and torch.all(ybuf[yoff + rows * cols:] == 7.0)
+
+
 @pytest.mark.parametrize("cols", [128, 1024, 4096, 32000, 128256, 300000])
 def test_output_guard_bands_untouched(st, cols):
     rows = 7

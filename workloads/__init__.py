@@ -15,6 +15,11 @@ Workloads (rows x cols, dtype, distribution, seed):
                               for c > r % 128,                               seed 1005
   increasing_65536x4096_f32   65536 x 4096 fp32, each row sorted N(0, 1)
                               draws made strictly increasing,                seed 1006
+  softmax_4096x50257_f32      4096 x 50257 fp32, N(0, 2),                    seed 1009
+                              (rows that are not a whole number of 16-byte
+                              vectors: every row starts at another offset
+                              inside its 16-byte block; the row length of the
+                              TopK workload, used as a softmax case)
 
 Attention (batch x heads x seq_len x head_dim, Q, K, V bf16, all N(0, 1)):
 
@@ -74,6 +79,7 @@ WORKLOADS = {
         Workload("topk_256x50257_f32", 256, 50257, "f32", 4.0, 1004, ks=(8, 64), op="topk"),
         Workload("causal_1048576x128_f32", 1048576, 128, "f32", 1.0, 1005, kind="causal"),
         Workload("increasing_65536x4096_f32", 65536, 4096, "f32", 1.0, 1006, kind="increasing"),
+        Workload("softmax_4096x50257_f32", 4096, 50257, "f32", 2.0, 1009),
     ]
 }
 
