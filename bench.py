@@ -23,8 +23,10 @@ their own, the other configurations -- 64x1024 fp32, causal 1048576x128,
 increasing 65536x4096 --, rows that are not whole 16-byte vectors (4096 x 50257
 fp32) and the ex2.approx-free kernel on the bf16 workload),
 `unfused_baselines` (three-pass safe softmax against the online kernel,
-softmax-then-TopK against the fused kernel) and, inside `e2e`, the plain
-pinned copy rates of the host link.
+softmax-then-TopK against the fused kernel), `stats_and_causal` (row
+statistics; causal mask applied in the kernel), `attention` (the tensor-core
+attention forward in TFLOP/s) and, inside `e2e`, the plain pinned copy rates
+of the host link.
 
 `--impl reference` times the oracle alone (the reference arm: the method's
 own definition run on the host cores), on the same metric.
@@ -280,6 +282,8 @@ def run_ours(args):
     e2e = run_e2e(st, dev, args) if rank == 0 else None
     others = time_other_workloads(st, dev, args) if rank == 0 else None
     baselines = run_baselines(st, dev, args) if rank == 0 else None
+    stats_causal = run_stats_and_causal(st, dev, args) if rank == 0 else None
+    attention = run_attention(st, dev, args, False) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
     if rank != 0:
@@ -321,11 +325,14 @@ def run_ours(args):
         "clocks": clock_info,
     }
     line["unfused_baselines"] = baselines
+    line["stats_and_causal"] = stats_causal
+    line["attention"] = attention
     if args.extra:
         line["extra_workloads"] = run_extra(st, dev, args)
-        line["stats_and_causal"] = run_stats_and_causal(st, dev, args)
-        line["attention"] = run_attention(st, dev, args, rank == 0 and world == 1 and
-                                          not args.no_cpu_baseline)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            line["attention"]["cpu_baseline"] = attention_oracle_rate(
+                workloads.ATTENTION_WORKLOADS["attention_4x16x4096x128_bf16"], False,
+                args.cpu_seconds / 3)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -42,3 +42,5 @@ def test_bench_line_keeps_the_contract():
         assert pw[key]["gbs"] > 0 and pw[key]["ms"] > 0, key
     assert e["link"]["h2d_gbs"] > 0 and e["link"]["d2h_gbs"] > 0 and e["frac_of_link_bound"] > 0
     assert d["unfused_baselines"]["softmax_4096x32000_f32"]["safe_over_online"] > 0
+    assert d["stats_and_causal"]["causal_1048576x128_f32"]["read_over_mask"] > 0
+    assert d["attention"]["cases"]["d128_full"]["tflops"] > 0
