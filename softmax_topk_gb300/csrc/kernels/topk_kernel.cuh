@@ -28,14 +28,14 @@
 //     CTA barrier in between), and their elements at or above the threshold
 //     become the candidates, a warp reserving its slots in the shared-memory
 //     buffer with one atomic;
-//   selection: up to 256 candidates, each one's rank is the number of
-//     candidates that beat it (one thread per candidate, comparing against
-//     register-held slabs of all candidates by broadcast shuffles) and rank
-//     r < K puts it in slot r of the list; more candidates are first cut to
-//     the K best by a radix select on their order keys (four 8-bit digit
-//     rounds, the lowest columns taken among ties at the K-th key) when
-//     K <= 64, and sorted whole by a CTA-wide bitonic sort of 64-bit keys
-//     (logit order key, then column) for larger K.  If the candidates
+//   selection: up to 512 candidates (K <= 64; 256 for larger K), each one's
+//     rank is the number of candidates that beat it (one thread per
+//     candidate, comparing against register-held slabs of all candidates by
+//     broadcast shuffles) and rank r < K puts it in slot r of the list; more
+//     candidates are first cut to the K best by a radix select on their
+//     order keys (four 8-bit digit rounds, the lowest columns taken among
+//     ties at the K-th key) when K <= 64, and sorted whole by a CTA-wide
+//     bitonic sort of 64-bit keys (logit order key, then column) for larger K.  If the candidates
 //     overflow the buffer (heavy
 //     ties at the threshold), an exact path finds the K-th largest key of the
 //     segment by bisection and admits the ties at it in column order;
@@ -72,9 +72,14 @@ struct __align__(8) Cand {
 };
 
 constexpr int kNoIndex = INT_MAX;
-// Candidate counts up to this are ranked by counting; more are cut to the K
-// best by a radix select (K <= 64) or sorted (larger K).
-constexpr int kRankMax = 256;
+// Candidate counts up to this are ranked by counting (one thread per
+// candidate, so at most the CTA's width); more are cut to the K best by a
+// radix select (K <= 64) or sorted (larger K, whose rows bring hundreds of
+// candidates, where the sort is faster).
+template <int THREADS, int KMAX>
+constexpr int rank_max() { return KMAX <= 64 ? (THREADS < 512 ? THREADS : 512) : 256; }
+// Candidates compared per batch of register-held slabs (8 slabs of 32).
+constexpr int kSlabBatch = 8;
 
 __device__ __forceinline__ bool beats(float v1, int j1, float v2, int j2) {
     return v1 > v2 || (v1 == v2 && j1 < j2);
@@ -373,8 +378,9 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
                  int64_t rows, int cols, int K, int S, KernelCtl ctl) {
     constexpr int NW = THREADS / 32;
     constexpr int CHUNK = THREADS * U;  // 16-byte blocks per chunk
-    static_assert(CAP % THREADS == 0 && CAP >= 128 && KMAX <= THREADS && KMAX <= kRankMax,
-                  "buffer sizes");
+    constexpr int RANKMAX = rank_max<THREADS, KMAX>();
+    static_assert(CAP % THREADS == 0 && CAP >= 128 && KMAX <= THREADS && KMAX <= RANKMAX &&
+                  RANKMAX <= THREADS, "buffer sizes");
     __shared__ __align__(16) TopkSmem<THREADS, KMAX, CAP, MAXC> sm;
     extern __shared__ __align__(16) unsigned char dyn_raw[];
     auto& dyn = *reinterpret_cast<TopkDynSmem<THREADS, U, GROUPS, FCAP>*>(dyn_raw);
@@ -649,37 +655,41 @@ topk_rows_kernel(const float* __restrict__ x, float* __restrict__ vals, int* __r
             __syncthreads();
         }
 
-        // ---- selection.  More than kRankMax candidates are sorted (the large-K
+        // ---- selection.  More than RANKMAX candidates are sorted (the large-K
         // build) or first cut to the K best by a radix select on their order
-        // keys (K <= 64).  Up to kRankMax, thread t ranks candidate t by
+        // keys (K <= 64).  Up to RANKMAX, thread t ranks candidate t by
         // counting the candidates that beat it; rank r < K puts it in slot r
-        // of the list.  Each warp holding candidates loads all of them into
-        // registers in one batch (lane l of slab s holds candidate 32 s + l)
-        // and compares against them by broadcast shuffles, so the count is a
-        // few hundred shuffles with no shared-memory round trip in between.
+        // of the list.  Each warp holding candidates loads them into registers
+        // in batches of kSlabBatch slabs (lane l of slab s holds candidate
+        // 32 s + l) and compares against them by broadcast shuffles, so the
+        // count is a few hundred shuffles with few shared-memory round trips.
         if constexpr (KMAX <= 64) {
-            if (n > kRankMax) {  // uniform
+            if (n > RANKMAX) {  // uniform
                 radix_select_compact<THREADS, CAP / THREADS>(sm.cand, n, K, dyn.flagged + 1024,
                                                              reinterpret_cast<Cand*>(dyn.flagged));
                 n = K;
             }
         }
-        if (n <= kRankMax) {  // uniform
-            constexpr int SL = kRankMax / 32;  // slabs of 32 candidates
-            if (warp * 32 < n) {               // warp-uniform
+        if (n <= RANKMAX) {  // uniform
+            if (warp * 32 < n) {  // warp-uniform
                 const Cand mine = tid < n ? sm.cand[tid] : pad;
-                Cand slab[SL];
-#pragma unroll
-                for (int s = 0; s < SL; ++s) slab[s] = 32 * s + lane < n ? sm.cand[32 * s + lane] : pad;
                 int r = 0;
+                for (int s0 = 0; s0 * 32 < n; s0 += kSlabBatch) {  // uniform
+                    Cand slab[kSlabBatch];
 #pragma unroll
-                for (int s = 0; s < SL; ++s) {
-                    if (32 * s < n) {  // uniform
+                    for (int s = 0; s < kSlabBatch; ++s) {
+                        const int i = 32 * (s0 + s) + lane;
+                        slab[s] = i < n ? sm.cand[i] : pad;
+                    }
+#pragma unroll
+                    for (int s = 0; s < kSlabBatch; ++s) {
+                        if (32 * (s0 + s) < n) {  // uniform
 #pragma unroll 8
-                        for (int q = 0; q < 32; ++q) {
-                            const float v = __shfl_sync(kFullMask, slab[s].v, q);
-                            const int jj = __shfl_sync(kFullMask, slab[s].j, q);
-                            r += beats(v, jj, mine.v, mine.j);
+                            for (int q = 0; q < 32; ++q) {
+                                const float v = __shfl_sync(kFullMask, slab[s].v, q);
+                                const int jj = __shfl_sync(kFullMask, slab[s].j, q);
+                                r += beats(v, jj, mine.v, mine.j);
+                            }
                         }
                     }
                 }
