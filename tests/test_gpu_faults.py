@@ -79,3 +79,26 @@ def test_status_clean_after_normal_work(st):
     st.softmax(x)
     st.softmax_topk(x, 64)
     st.os_device_status(_stream())
+
+
+def test_timeout_on_one_stream_reported_on_another(st):
+    """The status word is read and cleared in one atomic exchange on the
+    stream of the call: a wait that gave up in a kernel on a side stream is
+    reported by a call on the default stream (once that kernel has finished),
+    and the next call finds the word clear."""
+    x = (torch.randn(64, 32000, device="cuda") * 2)
+    st.os_device_status(_stream())
+    side = torch.cuda.Stream()
+    st.os_set_wait_timeout_ns(20 * 10 ** 6)
+    st.os_set_fault_injection(1)
+    try:
+        with torch.cuda.stream(side):
+            st.softmax(x, path="onchip")
+        side.synchronize()
+    finally:
+        st.os_set_fault_injection(0)
+        st.os_set_wait_timeout_ns(10 ** 9)
+    with pytest.raises(st.OsError) as e:
+        st.os_device_status(_stream())
+    assert e.value.name == "OS_ERR_TIMEOUT"
+    st.os_device_status(_stream())  # cleared by the exchange
