@@ -116,14 +116,18 @@ os_status softmax_entry(const void* x, void* y, int64_t rows, int64_t cols, os_d
     const bool in_place = x == y && in == out;
     if (!in_place && overlaps(x, rows * cols * elem_bytes(in), y, rows * cols * elem_bytes(out)))
         return OS_ERR_ALIAS;
+    const bool ptrs_aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                              reinterpret_cast<uintptr_t>(y) % 16 == 0;
     if (period > 0) {
-        const int64_t nv = (cols + elems_per_vector(in) - 1) / elems_per_vector(in);
+        // the vector slots a row needs (one more when rows are not 16-byte
+        // aligned whole vectors), as the plan counts them
+        const int epv = elems_per_vector(in);
+        const int64_t nv = (ptrs_aligned && cols % epv == 0) ? (cols + epv - 1) / epv
+                                                             : (cols + 2 * epv - 2) / epv;
         if (path == OS_PATH_AUTO) path = nv <= 256 ? OS_PATH_WARP : OS_PATH_STREAM;
         if (path != OS_PATH_WARP && path != OS_PATH_STREAM && path != OS_PATH_STREAM_POLY)
             return OS_ERR_PATH;
     }
-    const bool ptrs_aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
-                              reinterpret_cast<uintptr_t>(y) % 16 == 0;
     os_plan plan;
     st = kPairs[in][out].plan(rows, cols, path, ptrs_aligned, &plan);
     if (st != OS_OK) return st;

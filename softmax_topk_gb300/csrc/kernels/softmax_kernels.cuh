@@ -78,6 +78,67 @@ __device__ __forceinline__ void store_slot(TO* row, int64_t v, int cols, bool al
     }
 }
 
+// A row's vector slots.  Slot u of a row covers its columns
+// [u EPV - head, u EPV - head + EPV): head (0 .. EPV - 1) is the number of
+// elements between the start of the row's first 16-byte block of memory and
+// the row itself, so every slot is one aligned 16-byte block.  Rows whose
+// start is aligned (head = 0) have ceil(cols / EPV) slots; otherwise the
+// first and last slots hold columns of neighbouring rows, which are never
+// read or written.
+template <typename T>
+__device__ __forceinline__ int row_head(const T* row) {
+    return int((reinterpret_cast<uintptr_t>(row) & 15u) / sizeof(T));
+}
+
+// Whether the output row yr can take vector stores for input slots of a row
+// with this head: the slot's first column lands on an address aligned to the
+// store width (EPV outputs, at most 16 bytes).
+template <typename TO, int EPV>
+__device__ __forceinline__ bool out_vec_ok(const TO* yr, int head) {
+    constexpr uintptr_t A = EPV * sizeof(TO) < 16 ? EPV * sizeof(TO) : 16;
+    return ((reinterpret_cast<uintptr_t>(yr) - uintptr_t(head) * sizeof(TO)) & (A - 1)) == 0;
+}
+
+// Slot v of a row that does not start on a 16-byte boundary (head: the row
+// start's offset in its 16-byte block, row_head()): columns v EPV - head ..
+// v EPV - head + EPV - 1.  A slot wholly inside [0, lim) is one 16-byte load
+// (it is an aligned block of memory); the at most two partial slots of a row
+// are read element by element, columns outside [0, lim) as -inf.
+template <typename TI>
+__device__ __forceinline__ void load_slot_peeled(const TI* row, int head, int64_t v, int lim,
+                                                 float* out) {
+    constexpr int EPV = VecTraits<TI>::EPV;
+    const int64_t c0 = v * EPV - head;
+    if (c0 >= 0 && c0 + EPV <= lim) {
+        unpack(ld_coherent_v4(row + c0), out, TI());
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const int64_t j = c0 + e;
+            out[e] = j >= 0 && j < lim ? to_f32(row[j]) : kNegInf;
+        }
+    }
+}
+
+// The matching store: whole slots by one vector store when the output row
+// has the input's block phase (vec), otherwise and at the row ends element by
+// element, columns [0, cols) only.
+template <typename TI, typename TO>
+__device__ __forceinline__ void store_slot_peeled(TO* row, int head, bool vec, int64_t v, int cols,
+                                                  const float* vals) {
+    constexpr int EPV = VecTraits<TI>::EPV;
+    const int64_t c0 = v * EPV - head;
+    if (vec && c0 >= 0 && c0 + EPV <= cols) {
+        VecStore<TO, EPV>::run(row + c0, vals);
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const int64_t j = c0 + e;
+            if (j >= 0 && j < cols) row[j] = from_f32<TO>(vals[e]);
+        }
+    }
+}
+
 // The shift used for e^(x - m): m itself, or 0 where m = -inf (every x seen
 // so far is -inf, so every term is e^-inf = 0, the identity state's d).
 __device__ __forceinline__ float finite_shift(float m) { return m > kNegInf ? m : 0.f; }
@@ -143,7 +204,10 @@ __device__ __forceinline__ void scale_all(float* e, float s) {
 // warp_rows: L lanes per row (L in 1..32, power of two), VPT vectors per lane.
 // Lane l of a group owns vector slots l, l + L, ..., l + (VPT-1) L, so a warp
 // instruction covers 32 consecutive vectors of one row (or 32/L rows).
-template <typename TI, typename TO, int L, int VPT, int THREADS>
+// PEEL (rows not all 16-byte aligned whole vectors): slots follow each row's
+// 16-byte blocks (load_slot_peeled); otherwise `aligned` chooses between
+// 16-byte and element access for the whole launch.
+template <typename TI, typename TO, int L, int VPT, int THREADS, bool PEEL = false>
 __global__ void __launch_bounds__(THREADS)
 warp_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                  int aligned, int64_t period, int64_t offset) {
@@ -160,13 +224,15 @@ warp_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
         TO* yr = y + (live ? row : 0) * int64_t(cols);
         // causal mask: columns at or past `lim` are -inf and never read
         const int lim = live ? causal_limit(row, cols, period, offset) : 0;
+        const int head = PEEL ? row_head(xr) : 0;
 
         float e[EPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int64_t v = int64_t(k) * L + lane_in_row;
-            if (v * EPV < lim) {
-                load_slot(xr, v, lim, aligned && (v + 1) * EPV <= lim, e + k * EPV);
+            if (v * EPV - head < lim) {
+                if constexpr (PEEL) load_slot_peeled(xr, head, v, lim, e + k * EPV);
+                else load_slot(xr, v, lim, aligned && (v + 1) * EPV <= lim, e + k * EPV);
             } else {
 #pragma unroll
                 for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
@@ -178,10 +244,15 @@ warp_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
         group_merge<L>(m, d);
         scale_all<EPT>(e, rescale(m_t, m) * (1.0f / d));
         if (live) {
+            const bool yvec = PEEL && out_vec_ok<TO, EPV>(yr, head);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int64_t v = int64_t(k) * L + lane_in_row;
-                if (v < nv) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
+                if constexpr (PEEL) {
+                    if (v * EPV - head < cols) store_slot_peeled<TI, TO>(yr, head, yvec, v, cols, e + k * EPV);
+                } else {
+                    if (v < nv) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
+                }
             }
         }
     }
@@ -236,8 +307,8 @@ __device__ __forceinline__ float2 merge_row_state(RowMergeSmem<THREADS, CLUSTER>
 // ---------------------------------------------------------------------------
 // onchip_rows: one cluster of CLUSTER CTAs per row (persistent over rows).
 // CTA `rank` owns vector slots [rank*S, rank*S + S) with S = THREADS*VPT;
-// thread t owns slots rank*S + t + k*THREADS.
-template <typename TI, typename TO, int THREADS, int VPT, int CLUSTER>
+// thread t owns slots rank*S + t + k*THREADS.  PEEL as for warp_rows.
+template <typename TI, typename TO, int THREADS, int VPT, int CLUSTER, bool PEEL = false>
 __global__ void __launch_bounds__(THREADS, 1)
 onchip_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
                    int aligned) {
@@ -253,12 +324,15 @@ onchip_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
     for (int64_t row = cluster_id; row < rows; row += nclusters, parity ^= 1) {
         const TI* xr = x + row * int64_t(cols);
         TO* yr = y + row * int64_t(cols);
+        const int head = PEEL ? row_head(xr) : 0;
+        const int64_t nvr = PEEL ? (int64_t(cols) + head + EPV - 1) / EPV : nv;  // this row's slots
         float e[EPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int64_t v = v0 + int64_t(k) * THREADS;
-            if (v < nv) {
-                load_slot(xr, v, cols, aligned, e + k * EPV);
+            if (v < nvr) {
+                if constexpr (PEEL) load_slot_peeled(xr, head, v, cols, e + k * EPV);
+                else load_slot(xr, v, cols, aligned, e + k * EPV);
             } else {
 #pragma unroll
                 for (int q = 0; q < EPV; ++q) e[k * EPV + q] = kNegInf;
@@ -268,10 +342,14 @@ onchip_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
         const float d_t = exp_shift_sum<EPT>(e, m_t);
         const float2 md = merge_row_state<THREADS, CLUSTER>(sm, m_t, d_t, parity, rank);
         scale_all<EPT>(e, rescale(m_t, md.x) * (1.0f / md.y));
+        const bool yvec = PEEL && out_vec_ok<TO, EPV>(yr, head);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int64_t v = v0 + int64_t(k) * THREADS;
-            if (v < nv) store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
+            if (v < nvr) {
+                if constexpr (PEEL) store_slot_peeled<TI, TO>(yr, head, yvec, v, cols, e + k * EPV);
+                else store_slot<TI, TO>(yr, v, cols, aligned, e + k * EPV);
+            }
         }
     }
 }
@@ -612,18 +690,6 @@ __device__ __forceinline__ uint32_t packed_clamp_bound(float m) {
 // reference moves (e^30: sums of 2^((x - m) log2 e + 66) stay finite).
 constexpr float kRefWindow = 30.0f;
 
-// A row's vector slots.  Slot u of a row covers its columns
-// [u EPV - head, u EPV - head + EPV): head (0 .. EPV - 1) is the number of
-// elements between the start of the row's first 16-byte block of memory and
-// the row itself, so every slot is one aligned 16-byte block.  Rows whose
-// start is aligned (head = 0) have ceil(cols / EPV) slots; otherwise the
-// first and last slots hold columns of neighbouring rows, which are never
-// read or written.
-template <typename T>
-__device__ __forceinline__ int row_head(const T* row) {
-    return int((reinterpret_cast<uintptr_t>(row) & 15u) / sizeof(T));
-}
-
 // Which slots of a CTA's range [begin, begin + len) hold columns below a
 // limit `lim` (the row length, or its causal limit): [lo, full) wholly,
 // [0, lo) and [full, any) in part, none from `any` on.
@@ -740,14 +806,6 @@ __device__ __forceinline__ int row_slots(int cols) {  // cols can be 2^31 - 1
     return int((int64_t(cols) + (ALIGNED ? EPV - 1 : 2 * EPV - 2)) / EPV);
 }
 
-// Whether the output row yr can take vector stores for input slots of a row
-// with this head: the slot's first column lands on an address aligned to the
-// store width (EPV outputs, at most 16 bytes).
-template <typename TO, int EPV>
-__device__ __forceinline__ bool out_vec_ok(const TO* yr, int head) {
-    constexpr uintptr_t A = EPV * sizeof(TO) < 16 ? EPV * sizeof(TO) : 16;
-    return ((reinterpret_cast<uintptr_t>(yr) - uintptr_t(head) * sizeof(TO)) & (A - 1)) == 0;
-}
 
 // sum over N entries of e^(z_i), z given, on the SFU (statistics kernel)
 template <int N, bool FAST>

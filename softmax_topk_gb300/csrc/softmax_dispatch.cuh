@@ -57,31 +57,41 @@ struct SoftmaxFamily {
     static constexpr int TMA_EPT = tma_ept<TI>();
     using Ring = TmaRing<TI, kTmaThreads, TMA_EPT, TMA_STAGES>;
 
-    static WarpKernel warp(int lanes, int vpt) {
-        if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads>;
+    // PEEL: rows that are not all 16-byte aligned whole vectors move as the
+    // 16-byte blocks they cover (see warp_rows_kernel)
+    template <bool PEEL>
+    static WarpKernel warp_as(int lanes, int vpt) {
+        if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads, PEEL>;
         switch (lanes) {
-            case 1: return warp_rows_kernel<TI, TO, 1, 4, kWarpThreads>;
-            case 2: return warp_rows_kernel<TI, TO, 2, 4, kWarpThreads>;
-            case 4: return warp_rows_kernel<TI, TO, 4, 4, kWarpThreads>;
-            case 8: return warp_rows_kernel<TI, TO, 8, 4, kWarpThreads>;
-            case 16: return warp_rows_kernel<TI, TO, 16, 4, kWarpThreads>;
-            default: return warp_rows_kernel<TI, TO, 32, 4, kWarpThreads>;
+            case 1: return warp_rows_kernel<TI, TO, 1, 4, kWarpThreads, PEEL>;
+            case 2: return warp_rows_kernel<TI, TO, 2, 4, kWarpThreads, PEEL>;
+            case 4: return warp_rows_kernel<TI, TO, 4, 4, kWarpThreads, PEEL>;
+            case 8: return warp_rows_kernel<TI, TO, 8, 4, kWarpThreads, PEEL>;
+            case 16: return warp_rows_kernel<TI, TO, 16, 4, kWarpThreads, PEEL>;
+            default: return warp_rows_kernel<TI, TO, 32, 4, kWarpThreads, PEEL>;
         }
     }
-    static Kernel onchip(int threads, int cluster) {
+    static WarpKernel warp(int lanes, int vpt, bool peel = false) {
+        return peel ? warp_as<true>(lanes, vpt) : warp_as<false>(lanes, vpt);
+    }
+    template <bool PEEL>
+    static Kernel onchip_as(int threads, int cluster) {
         if (cluster == 1) {
             switch (threads) {
-                case 128: return onchip_rows_kernel<TI, TO, 128, VPT, 1>;
-                case 256: return onchip_rows_kernel<TI, TO, 256, VPT, 1>;
-                default: return onchip_rows_kernel<TI, TO, 512, VPT, 1>;
+                case 128: return onchip_rows_kernel<TI, TO, 128, VPT, 1, PEEL>;
+                case 256: return onchip_rows_kernel<TI, TO, 256, VPT, 1, PEEL>;
+                default: return onchip_rows_kernel<TI, TO, 512, VPT, 1, PEEL>;
             }
         }
         switch (cluster) {
-            case 2: return onchip_rows_kernel<TI, TO, 512, VPT, 2>;
-            case 4: return onchip_rows_kernel<TI, TO, 512, VPT, 4>;
-            case 8: return onchip_rows_kernel<TI, TO, 512, VPT, 8>;
-            default: return onchip_rows_kernel<TI, TO, 512, VPT, 16>;
+            case 2: return onchip_rows_kernel<TI, TO, 512, VPT, 2, PEEL>;
+            case 4: return onchip_rows_kernel<TI, TO, 512, VPT, 4, PEEL>;
+            case 8: return onchip_rows_kernel<TI, TO, 512, VPT, 8, PEEL>;
+            default: return onchip_rows_kernel<TI, TO, 512, VPT, 16, PEEL>;
         }
+    }
+    static Kernel onchip(int threads, int cluster, bool peel = false) {
+        return peel ? onchip_as<true>(threads, cluster) : onchip_as<false>(threads, cluster);
     }
     static TmaKernel tma(int cluster) {
         constexpr int T = kTmaThreads, E = TMA_EPT, S = TMA_STAGES;
@@ -156,7 +166,10 @@ struct SoftmaxFamily {
     static os_status plan(int64_t rows, int64_t cols, os_path path, bool aligned, os_plan* p) {
         const DeviceInfo* dev = device_info();
         if (!dev) return OS_ERR_CUDA;
-        const int64_t nv = ceil_div(cols, EPV);
+        // vector slots a row needs: one more for rows that are not 16-byte
+        // aligned whole vectors, whose first and last blocks are partial
+        const int64_t nv = (aligned && cols % EPV == 0) ? ceil_div(cols, EPV)
+                                                        : ceil_div(cols + EPV - 1, EPV);
         const bool warp_ok = nv <= 256;
         const int64_t cta_cap = int64_t(kOnchipThreadsMax) * VPT;
         const bool onchip_ok = nv <= int64_t(onchip_cluster_limit(*dev)) * cta_cap;
@@ -173,7 +186,8 @@ struct SoftmaxFamily {
                 q.threads = kWarpThreads;
                 q.cluster = 1;
                 const int64_t rows_per_cta = kWarpThreads / q.lanes_per_row;
-                const int occ = blocks_per_sm(warp(q.lanes_per_row, q.vectors_per_thread),
+                const int occ = blocks_per_sm(warp(q.lanes_per_row, q.vectors_per_thread,
+                                                   !(aligned && cols % EPV == 0)),
                                               kWarpThreads);
                 q.grid = min64(ceil_div(rows, rows_per_cta), int64_t(dev->sms) * (occ > 0 ? occ : 1));
                 break;
@@ -262,12 +276,12 @@ struct SoftmaxFamily {
                                  period, offset);
         }
         if (p.path == OS_PATH_WARP) {
-            WarpKernel k = warp(p.lanes_per_row, p.vectors_per_thread);
+            WarpKernel k = warp(p.lanes_per_row, p.vectors_per_thread, !aligned);
             if (!prepare_kernel(k, 1, 0)) return cudaErrorInvalidValue;
             return launch_kernel(k, p.grid, p.threads, 1, 0, stream, xi, yo, rows, cols,
                                  aligned ? 1 : 0, period, offset);
         }
-        Kernel k = onchip(p.threads, p.cluster);
+        Kernel k = onchip(p.threads, p.cluster, !aligned);
         if (!prepare_kernel(k, p.cluster, 0)) return cudaErrorInvalidValue;
         return launch_kernel(k, p.grid, p.threads, p.cluster, 0, stream, xi, yo, rows, cols,
                              aligned ? 1 : 0);

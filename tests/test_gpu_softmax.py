@@ -308,13 +308,14 @@ def test_misaligned_pointers(st, pair, cols):
 @pytest.mark.parametrize("xoff,yoff", [(0, 0), (1, 1), (0, 3), (2, 1), (3, 0)])
 @pytest.mark.parametrize("path", ["auto", "stream", "safe", "stream_poly"])
 def test_rows_not_whole_vectors(st, pair, xoff, yoff, path):
-    """Rows of 50257 and 16387 columns: every row starts at another offset in
-    its 16-byte block, so the kernels peel the partial blocks at both ends and
-    move the rest with 128-bit accesses; the output may have the input's block
-    phase (vector stores) or not (element stores).  300 rows: persistent CTAs
-    walk many rows and every head occurs; guard elements stay untouched."""
-    for cols in (50257, 16387):
-        rows = 300 if cols > 20000 else 40
+    """Rows of 50257, 16387, 3001, 1001 and 257 columns (streaming, on-chip and
+    warp kernels): every row starts at another offset in its 16-byte block,
+    so the kernels peel the partial blocks at both ends and move the rest
+    with 128-bit accesses; the output may have the input's block phase
+    (vector stores) or not (element stores).  Many rows: persistent CTAs walk
+    several rows and every head occurs; guard elements stay untouched."""
+    for cols in (50257, 16387, 3001, 1001, 257):
+        rows = 300 if cols > 20000 else (40 if cols > 10000 else 700)
         xin, xout = DT[pair[0]], DT[pair[1]]
         xbuf = torch.empty(rows * cols + 8, dtype=xin, device="cuda")
         ybuf = torch.full((rows * cols + 8,), 7.0, dtype=xout, device="cuda")
