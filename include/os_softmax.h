@@ -119,13 +119,12 @@ typedef struct {
  *             overwritten by its softmax) or no overlap with x at all; any
  *             other overlap is OS_ERR_ALIAS.
  *   in_dtype, out_dtype: OS_F32 or OS_BF16, in any combination.
- * Pointers must be aligned to their element size (OS_ERR_ALIGN).  Rows of
- * more than 4096 16-byte vectors move as the aligned 16-byte blocks they
- * cover (128-bit loads, and 128-bit stores when y's rows have x's offset
- * inside their 16-byte blocks), with element access only for the partial
- * block at each end of a row; shorter rows get 128-bit access when both
- * pointers are 16-byte aligned and cols is a multiple of 16/sizeof(in), and
- * element access otherwise.
+ * Pointers must be aligned to their element size (OS_ERR_ALIGN).  Rows move
+ * as the aligned 16-byte blocks they cover (128-bit loads, and 128-bit stores
+ * when y's rows have x's offset inside their 16-byte blocks), with element
+ * access only for the partial block at each end of a row.  A row that does
+ * not start on a 16-byte boundary can need one 16-byte slot more than
+ * cols / (16/sizeof(in)), which the choice of kernel family accounts for.
  */
 os_status os_softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols,
                          os_dtype in_dtype, os_dtype out_dtype, os_stream_t stream);
