@@ -247,12 +247,6 @@ __device__ __forceinline__ float2 exp_folded_pair(float2 x, float2 k) {
     return make_float2(add_exponent(p.x, u.x), add_exponent(p.y, u.y));
 }
 
-// e^z of a pair (z <= 0, -inf allowed) for fp32 results: the form above,
-// unbiased.  os_exp_pairs_f32 exposes it for its accuracy test.
-__device__ __forceinline__ float2 exp_pair_fma(float2 z) {
-    return mul2(exp_biased_pair<5>(z), splat2(expc::kUnbias));
-}
-
 __device__ __forceinline__ float ex2_sfu(float t) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
@@ -335,20 +329,14 @@ __device__ __forceinline__ uint4 ld_policy_v4(const void* p, uint64_t policy) {
     return v;
 }
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
-// Coherent (not read-only-path) forms of the two loads above, for inputs that
-// the same launch may overwrite: softmax exactly in place, where y == x.
-// Every softmax kernel reads an element before the thread that read it (or,
-// for rows staged in shared memory, its CTA) writes that element, and the
-// written value depends on the value read, so no load can be moved past the
-// store to its own address (so these need neither `volatile` nor a memory
-// clobber, and the compiler keeps its freedom to schedule them).
+// Coherent (not read-only-path) 16-byte loads, with and without an L2 policy,
+// for inputs that the same launch may overwrite: softmax exactly in place,
+// where y == x.  In every softmax kernel an element is written only by the
+// thread that read it (or, for rows staged in shared memory, by that CTA),
+// after reading it, and the value written depends on the value read, so no
+// load can move past the store to its own address.  The loads therefore need
+// neither `volatile` nor a memory clobber, and the compiler stays free to
+// schedule them.
 __device__ __forceinline__ uint4 ld_coherent_policy_v4(const void* p, uint64_t policy) {
     uint4 v;
     asm("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
@@ -467,11 +455,6 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t addr, float2 v) {
                  : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_b64(uint32_t addr, uint32_t lo, uint32_t hi) {
-    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" :: "r"(addr), "r"(lo), "r"(hi)
-                 : "memory");
-}
-
 // ------------------------------------------------------------------ async copies
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -552,14 +535,6 @@ __device__ __forceinline__ bool cta_wait_bounded(uint64_t* bar, uint32_t parity,
     if (threadIdx.x == 0) flag[which] = mbar_wait_bounded(bar, parity, ctl) ? 1 : 0;
     __syncthreads();
     return flag[which] != 0;
-}
-
-// Asks L2 to fetch [src, src + bytes) from memory ahead of its use, with an
-// eviction policy; nothing reaches this SM and nothing waits for it.  src
-// 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
-                 :: "l"(src), "r"(bytes), "l"(policy) : "memory");
 }
 
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.

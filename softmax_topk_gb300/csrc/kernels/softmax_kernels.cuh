@@ -160,25 +160,6 @@ __device__ __forceinline__ float exp_shift_sum(float* e, float m) {
     return acc.x + acc.y;
 }
 
-// sum of e^(e[i] - m) over N entries, leaving e unchanged.
-template <int N, bool FAST = false>
-__device__ __forceinline__ float exp_sum(const float* e, float m) {
-    static_assert(N % 2 == 0, "pairs");
-    float2 acc = make_float2(0.f, 0.f);
-    const float2 neg_m = splat2(-finite_shift(m));
-#pragma unroll
-    for (int i = 0; i < N; i += 2)
-        acc = add2(acc, exp_pair<FAST>(add2(make_float2(e[i], e[i + 1]), neg_m)));
-    return acc.x + acc.y;
-}
-
-// Load vector slot v with an L2 eviction policy (aligned rows only).
-template <typename TI>
-__device__ __forceinline__ void load_slot_policy(const TI* row, int64_t v, uint64_t policy,
-                                                 float* out) {
-    unpack(ld_coherent_policy_v4(row + v * VecTraits<TI>::EPV, policy), out, TI());
-}
-
 template <int N>
 __device__ __forceinline__ float max_of(const float* e) {
     float m = e[0];
