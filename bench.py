@@ -430,7 +430,8 @@ def kernel_of(st, label: str, path: str = "auto") -> str:
 def run_e2e(st, dev, args):
     """Same step through the public API from pinned host buffers: every
     input copied host->device and every result device->host inside the timed
-    region, pipelined over row blocks."""
+    region, pipelined over row blocks and, through two device buffer sets,
+    across consecutive steps."""
     host_in, host_out = [], []
     h2d = d2h = 0
     for n in SOFTMAX_STEP:
@@ -448,29 +449,45 @@ def run_e2e(st, dev, args):
         topk_out.append((torch.empty(w.rows, K).pin_memory(),
                          torch.empty(w.rows, K, dtype=torch.int32).pin_memory()))
         d2h += w.rows * K * 8
-    dev_in = [torch.empty_like(h, device=dev) for h in host_in]
-    dev_out = [torch.empty_like(h, device=dev) for h in host_in]
-    dev_xt = torch.empty_like(xt, device=dev)
-    dev_topk = [(torch.empty(w.rows, K, device=dev), torch.empty(w.rows, K, dtype=torch.int32,
-                                                                  device=dev)) for K in TOPK_KS]
+    # Two device buffer sets, alternating by step: the copy-in of a step's
+    # first blocks overlaps the copy-out of the previous step's last ones.  A
+    # set is refilled only after the step that used it two steps before has
+    # copied its results out (an event on the copy-out stream).
+    sets = []
+    for _ in range(2):
+        sets.append({"in": [torch.empty_like(h, device=dev) for h in host_in],
+                     "out": [torch.empty_like(h, device=dev) for h in host_in],
+                     "xt": torch.empty_like(xt, device=dev),
+                     "topk": [(torch.empty(w.rows, K, device=dev),
+                               torch.empty(w.rows, K, dtype=torch.int32, device=dev))
+                              for K in TOPK_KS]})
 
     # Pipelined over row blocks on three streams: copy-in of a block overlaps
     # the kernel on the block before and the copy-out of the one before that
     # (host->device and device->host copies run on separate copy engines).
+    # The TopK block (51 MB in, a few KB out) goes first and the softmax rows
+    # follow in blocks of about 130 MB, so the link's two directions are busy
+    # together for as much of the step as possible.
     s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     main = torch.cuda.current_stream(dev)
-    pieces = []  # (kind, host in, device in, device out, host out, K)
-    for h, d, o, ho, n in zip(host_in, dev_in, dev_out, host_out, SOFTMAX_STEP):
-        blocks = 8 if h.shape[0] >= 8192 else 4
-        step = -(-h.shape[0] // blocks)
-        for r0 in range(0, h.shape[0], step):
-            r1 = min(h.shape[0], r0 + step)
-            pieces.append(("softmax", h[r0:r1], d[r0:r1], o[r0:r1], ho[r0:r1], None))
-    pieces.append(("topk", xt, dev_xt, dev_topk, topk_out, None))
 
-    def one_step():
-        s_in.wait_stream(main)
-        for kind, h, d, o, ho, _ in pieces:
+    def pieces_of(bufs):
+        out = [("topk", xt, bufs["xt"], bufs["topk"], topk_out)]
+        for h, d, o, ho in zip(host_in, bufs["in"], bufs["out"], host_out):
+            blocks = max(1, -(-h.numel() * h.element_size() // (136 << 20)))
+            step = -(-h.shape[0] // blocks)
+            for r0 in range(0, h.shape[0], step):
+                r1 = min(h.shape[0], r0 + step)
+                out.append(("softmax", h[r0:r1], d[r0:r1], o[r0:r1], ho[r0:r1]))
+        return out
+    set_pieces = [pieces_of(b) for b in sets]
+    freed = [None, None]  # copy-out of the last step that used each set
+
+    def one_step(i):
+        k = i % 2
+        if freed[k] is not None:
+            s_in.wait_event(freed[k])
+        for kind, h, d, o, ho in set_pieces[k]:
             with torch.cuda.stream(s_in):
                 d.copy_(h, non_blocking=True)
             s_comp.wait_stream(s_in)
@@ -478,33 +495,39 @@ def run_e2e(st, dev, args):
                 if kind == "softmax":
                     st.softmax(d, out=o)
                 else:
-                    for K, (v, i) in zip(TOPK_KS, o):
-                        st.softmax_topk(d, K, vals=v, idx=i)
+                    for K, (v, ix) in zip(TOPK_KS, o):
+                        st.softmax_topk(d, K, vals=v, idx=ix)
             s_out.wait_stream(s_comp)
             with torch.cuda.stream(s_out):
                 if kind == "softmax":
                     ho.copy_(o, non_blocking=True)
                 else:
-                    for (v, i), (hv, hi) in zip(o, ho):
+                    for (v, ix), (hv, hi) in zip(o, ho):
                         hv.copy_(v, non_blocking=True)
-                        hi.copy_(i, non_blocking=True)
-        main.wait_stream(s_out)
+                        hi.copy_(ix, non_blocking=True)
+        freed[k] = torch.cuda.Event()
+        freed[k].record(s_out)
 
     steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        one_step()
+    for s_ in (s_in, s_comp, s_out):
+        s_.wait_stream(main)
+    for i in range(2):
+        one_step(i)
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        one_step()
+    for s_ in (s_in, s_comp, s_out):
+        s_.wait_stream(main)
+    for i in range(steps):
+        one_step(i)
+    main.wait_stream(s_out)
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
     step_bytes = sum(u[1] for u in step_units())
-    del host_in, host_out, dev_in, dev_out, dev_xt, dev_topk, xt, topk_out, pieces
+    del host_in, host_out, sets, set_pieces, xt, topk_out
     link = link_rates(dev)
     # the host link alone, at the rates measured above, with both directions
     # overlapped as the pipeline overlaps them: the bound of this leg
