@@ -210,21 +210,24 @@ def make_step_inputs(dev, st):
         w = workloads.WORKLOADS[n]
         x = workloads.make(w, device=dev)
         y = torch.empty_like(x)
-        items.append(("softmax", n, [x], y, None))
+        items.append(("softmax", n, [x], y, None, 0))
     w = workloads.WORKLOADS[TOPK_NAME]
     xt = workloads.make(w, device=dev)
     copies = -(-3 * l2 // (xt.numel() * 4)) + 1
     xs = [xt] + [xt.clone() for _ in range(copies - 1)]
-    for K in TOPK_KS:
+    for j, K in enumerate(TOPK_KS):
         vals = torch.empty(w.rows, K, device=dev)
         idx = torch.empty(w.rows, K, dtype=torch.int32, device=dev)
-        items.append(("topk", f"{TOPK_NAME}_K{K}", xs, (vals, idx), K))
+        items.append(("topk", f"{TOPK_NAME}_K{K}", xs, (vals, idx), K, j))
     return items, copies
 
 
 def launch(st, item, it):
-    kind, _, xs, out, K = item
-    x = xs[it % len(xs)]
+    """Launch one item of step `it`.  Each TopK launch of the step reads its
+    own copy of the input (copy (it * len(TOPK_KS) + j) mod copies), so none
+    reads a copy that an earlier launch of the last 3 x L2 bytes read."""
+    kind, _, xs, out, K, j = item
+    x = xs[(it * len(TOPK_KS) + j) % len(xs)]
     if kind == "softmax":
         st.softmax(x, out=out)
     else:

@@ -513,10 +513,11 @@ tma_rows_kernel(const TI* x, TO* y, int64_t rows, int cols,
 }
 
 // Chunks of a row that the streaming kernel keeps in shared memory between
-// its passes: as many as fit in kStreamKeptBytes (two CTAs share an SM).
-constexpr int kStreamKeptBytes = 96 * 1024;
+// its passes: as many as fit in kStreamKeptBytesPerThread per thread, 96 KB
+// for a CTA of 512 threads (two per SM), 48 KB for one of 256 (four per SM).
+constexpr int kStreamKeptBytesPerThread = 192;
 template <typename TI, int THREADS, int UNROLL>
-constexpr int stream_kept_chunks() { return kStreamKeptBytes / (THREADS * UNROLL * 16); }
+constexpr int stream_kept_chunks() { return kStreamKeptBytesPerThread / (UNROLL * 16); }
 
 // ---------------------------------------------------------------------------
 // Chunk arithmetic of the streaming kernel.  A chunk is UNROLL 16-byte

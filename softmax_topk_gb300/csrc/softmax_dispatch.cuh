@@ -2,7 +2,8 @@
 // pair.  Included by one translation unit per pair, which instantiates it.
 //
 // Families by row length, in 16-byte input vectors nv = ceil(cols / EPV);
-// AUTO takes WARP for nv <= 256, ONCHIP for nv <= 4096, STREAM beyond:
+// AUTO takes WARP for nv <= 256, ONCHIP for nv <= 2048 fp32 / 512 bf16
+// vectors, STREAM beyond:
 //   WARP    nv <= 256: L = 1..32 lanes per row with 4 vectors per lane, or 32
 //           lanes with 8 vectors (rows of up to 1024 fp32 / 2048 bf16).
 //   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV).
@@ -16,7 +17,9 @@
 //           Rows of up to 262144 fp32 / 524288 bf16 (16-CTA clusters only
 //           where the device can schedule them).
 //   STREAM  anything longer: one CTA per row when there are at least as many
-//           rows as SMs, else a cluster of 8 CTAs per row.
+//           rows as SMs (CTAs of 256 threads, four per SM, for rows of up to
+//           96 KB; of 512 threads, two per SM, beyond), else a cluster of 8
+//           CTAs of 512 threads per row.
 //   SAFE    the three-pass safe softmax, as a measurement baseline only.
 // "5.2 CUDA Online Softmax" (sections 6.3 and 8.3) makes the same split on
 // its hardware: the register-cached single read (V3) for short rows, the
@@ -32,13 +35,24 @@ constexpr int kWarpThreads = 256;
 constexpr int kOnchipThreadsMax = 512;
 constexpr int kOnchipElemsPerThread = 32;
 constexpr int kStreamThreads = 512;
+// Rows of at most this many input bytes stream through CTAs of
+// kStreamThreadsShort threads: four rows in flight per SM instead of two,
+// each kept on chip whole up to 48 KB.  Measured on GB300 (4096 rows, CUDA
+// events): fp32 24000 columns 6030 against 4706 GB/s, bf16 24000 5263
+// against 4592; from 128 KB rows on the 512-thread CTAs are as fast or faster.
+constexpr int kStreamThreadsShort = 256;
+constexpr int64_t kStreamShortRowBytes = 96 * 1024;
 // vectors per thread per chunk: 8 fp32 or 4 bf16 (32 elements either way; measured best)
 template <typename TI> constexpr int stream_unroll() { return sizeof(TI) == 4 ? 8 : 4; }
 constexpr int kTmaMinCols = 8192;
-// AUTO sends rows longer than this many 16-byte vectors (16384 fp32, 32768
-// bf16 elements) to the two-pass streaming kernel: measured on GB300 it beats
-// both on-chip families there (no exchange between SMs, second read from L2).
-constexpr int64_t kAutoOnchipMaxVectors = 4096;
+// AUTO sends rows longer than this many 16-byte vectors (8192 fp32, 4096
+// bf16 elements) to the two-pass streaming kernel: measured on GB300 (4096
+// rows) the register kernel wins up to there with CTAs of at most 256
+// threads (fp32 8192 columns: 5627 against 5481 GB/s; bf16 4096: 3587
+// against 2878), the streaming kernel beyond (fp32 8193: 4218 against 3194;
+// bf16 6000: 3902 against 3056; the bulk-copy ring kernel 3000-5070 GB/s on
+// 12000-32768 columns against the streaming kernel's 4245-6078).
+template <typename TI> constexpr int64_t auto_onchip_max_vectors() { return sizeof(TI) == 4 ? 2048 : 512; }
 // The bulk-copy ring kernel runs CTAs of 256 threads, two per SM, so one
 // CTA's reductions and exchange overlap the other's loads and arithmetic.
 // Elements per thread: 32 fp32 or 64 bf16, so a CTA's slice is 32 KB of input
@@ -115,22 +129,25 @@ struct SoftmaxFamily {
         return aligned ? safe_rows_kernel<TI, TO, T, U, true, SFU_DEFAULT>
                        : safe_rows_kernel<TI, TO, T, U, false, SFU_DEFAULT>;
     }
-    static constexpr int stream_smem_bytes() {
-        return stream_kept_chunks<TI, kStreamThreads, STREAM_UNROLL>() * kStreamThreads *
-               STREAM_UNROLL * 16;
+    static constexpr int stream_smem_bytes(int threads) {
+        return stream_kept_chunks<TI, kStreamThreads, STREAM_UNROLL>() * threads * STREAM_UNROLL * 16;
     }
+    // threads 256 (cluster 1 only) or 512
     template <bool SFU>
-    static StreamKernel streaming_as(int cluster, bool aligned) {
-        constexpr int T = kStreamThreads, U = STREAM_UNROLL;
+    static StreamKernel streaming_as(int threads, int cluster, bool aligned) {
+        constexpr int T = kStreamThreads, TS = kStreamThreadsShort, U = STREAM_UNROLL;
+        if (threads == TS)
+            return aligned ? stream_rows_kernel<TI, TO, TS, U, 1, true, SFU>
+                           : stream_rows_kernel<TI, TO, TS, U, 1, false, SFU>;
         if (aligned)
             return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, true, SFU>
                                 : stream_rows_kernel<TI, TO, T, U, 8, true, SFU>;
         return cluster == 1 ? stream_rows_kernel<TI, TO, T, U, 1, false, SFU>
                             : stream_rows_kernel<TI, TO, T, U, 8, false, SFU>;
     }
-    static StreamKernel streaming(int cluster, bool aligned, bool poly = false) {
-        if (poly || !SFU_DEFAULT) return streaming_as<false>(cluster, aligned);
-        return streaming_as<SFU_DEFAULT>(cluster, aligned);
+    static StreamKernel streaming(int threads, int cluster, bool aligned, bool poly = false) {
+        if (poly || !SFU_DEFAULT) return streaming_as<false>(threads, cluster, aligned);
+        return streaming_as<SFU_DEFAULT>(threads, cluster, aligned);
     }
 
     // Largest cluster size of the ONCHIP family the current device can run.
@@ -175,7 +192,7 @@ struct SoftmaxFamily {
         const bool onchip_ok = nv <= int64_t(onchip_cluster_limit(*dev)) * cta_cap;
         if (path == OS_PATH_AUTO)
             path = warp_ok ? OS_PATH_WARP
-                 : (nv <= kAutoOnchipMaxVectors && onchip_ok) ? OS_PATH_ONCHIP : OS_PATH_STREAM;
+                 : (nv <= auto_onchip_max_vectors<TI>() && onchip_ok) ? OS_PATH_ONCHIP : OS_PATH_STREAM;
         os_plan q = {};
         q.path = path;
         switch (path) {
@@ -222,12 +239,13 @@ struct SoftmaxFamily {
             }
             case OS_PATH_STREAM:
             case OS_PATH_STREAM_POLY: {
-                q.threads = kStreamThreads;
                 q.vectors_per_thread = STREAM_UNROLL;
                 q.cluster = rows >= int64_t(dev->sms) ? 1 : 8;  // measured: 1 CTA per row wins from one row per SM up
+                q.threads = q.cluster == 1 && cols * int64_t(sizeof(TI)) <= kStreamShortRowBytes
+                    ? kStreamThreadsShort : kStreamThreads;
                 {
-                    const int occ = blocks_per_sm(streaming(q.cluster, true), kStreamThreads,
-                                                  stream_smem_bytes());
+                    const int occ = blocks_per_sm(streaming(q.threads, q.cluster, true), q.threads,
+                                                  stream_smem_bytes(q.threads));
                     const int64_t resident = q.cluster == 1
                         ? int64_t(dev->sms) * (occ > 0 ? occ : 1)
                         : kMaxClustersPerLaunch;
@@ -269,8 +287,8 @@ struct SoftmaxFamily {
             return launch_kernel(k, p.grid, p.threads, 1, 0, stream, xi, yo, rows, cols);
         }
         if (p.path == OS_PATH_STREAM || p.path == OS_PATH_STREAM_POLY) {
-            StreamKernel k = streaming(p.cluster, aligned, p.path == OS_PATH_STREAM_POLY);
-            const int smem = stream_smem_bytes();
+            StreamKernel k = streaming(p.threads, p.cluster, aligned, p.path == OS_PATH_STREAM_POLY);
+            const int smem = stream_smem_bytes(p.threads);
             if (!prepare_kernel(k, p.cluster, smem)) return cudaErrorInvalidValue;
             return launch_kernel(k, p.grid, p.threads, p.cluster, smem, stream, xi, yo, rows, cols,
                                  period, offset);

@@ -337,6 +337,37 @@ def test_rows_not_whole_vectors(st, pair, xoff, yoff, path):
         assert torch.all(ybuf[:yoff] == 7.0) and torch.all(ybuf[yoff + rows * cols:] == 7.0)
 
 
+SHORT_STREAM_COLS = [257, 1000, 4097, 8191, 8192, 8193, 12000, 16385, 24575, 24576, 24577,
+                     32000, 49152, 49153]
+
+
+@pytest.mark.parametrize("path", ["auto", "stream", "stream_poly"])
+@pytest.mark.parametrize("pair", PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+def test_stream_short_row_ctas(st, pair, path):
+    """At least as many rows as SMs, rows of up to 96 KB: the streaming kernel
+    runs CTAs of 256 threads (four per SM, 48 KB kept on chip), 512 beyond.
+    Columns cross its chunk sizes, the kept part, the 96 KB switch (24576
+    fp32, 49152 bf16) and the vector width; aligned and unaligned bases."""
+    rows = 160
+    esz = 4 if pair[0] == "f32" else 2
+    code = (0 if pair[0] == "f32" else 1, 0 if pair[1] == "f32" else 1)
+    for cols in SHORT_STREAM_COLS:
+        p = st.plan((rows, cols), code[0], code[1], path=path)
+        if p["path"] in (st.OS_PATH_STREAM, st.OS_PATH_STREAM_POLY):
+            assert p["cluster"] == 1 and p["threads"] == (256 if cols * esz <= 96 * 1024 else 512), (cols, p)
+        for off in (0, 1):
+            xbuf = torch.empty(rows * cols + 8, dtype=DT[pair[0]], device="cuda")
+            x = xbuf[off:off + rows * cols].view(rows, cols)
+            x.copy_(_inputs(rows, cols, pair[0], seed=cols + 3 * off))
+            y = torch.empty(rows, cols, dtype=DT[pair[1]], device="cuda")
+            st.os_softmax_fwd_path(x.data_ptr(), y.data_ptr(), rows, cols, code[0], code[1],
+                                   st.PATHS[path], torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            xx = x.double().cpu().numpy()
+            assert_softmax_close(xx, y.double().cpu().numpy(), oracle.softmax(xx), pair[1],
+                                 f"{path} {pair} cols={cols} offset {off}")
+
+
 @pytest.mark.parametrize("cols", [128, 1024, 4096, 32000, 128256, 300000])
 def test_output_guard_bands_untouched(st, cols):
     rows = 7
@@ -372,6 +403,15 @@ def test_plans_of_the_workloads(st):
     assert p["path"] == st.OS_PATH_WARP and p["lanes_per_row"] == 8
     p = st.plan((65536, 4096), st.OS_F32)
     assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 1 and p["threads"] == 128
+    # AUTO's family boundaries and the streaming kernel's CTA size
+    assert st.plan((4096, 8192), st.OS_F32)["path"] == st.OS_PATH_ONCHIP
+    assert st.plan((4096, 8193), st.OS_F32)["path"] == st.OS_PATH_STREAM
+    assert st.plan((4096, 4096), st.OS_BF16)["path"] == st.OS_PATH_ONCHIP
+    assert st.plan((4096, 4097), st.OS_BF16)["path"] == st.OS_PATH_STREAM
+    assert st.plan((4096, 24576), st.OS_F32)["threads"] == 256
+    assert st.plan((4096, 24577), st.OS_F32)["threads"] == 512
+    assert st.plan((4096, 49152), st.OS_BF16)["threads"] == 256
+    assert st.plan((100, 24576), st.OS_F32)["threads"] == 512  # fewer rows than SMs: clusters
     with pytest.raises(st.OsError):
         st.plan((10, 5000), st.OS_F32, path="warp")
 

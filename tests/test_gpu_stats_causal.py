@@ -94,7 +94,9 @@ def test_stats_agree_with_softmax_output(st):
 
 CAUSAL = [  # rows, cols, period, offset: warp rows, stream rows, offsets past the end
     (384, 128, 128, 0), (100, 33, 7, 0), (64, 1000, 64, 900), (48, 4096, 16, 4000),
-    (40, 50257, 40, 50000), (12, 131073, 6, 131000), (20, 300, 5, 1000)]
+    (40, 50257, 40, 50000), (12, 131073, 6, 131000), (20, 300, 5, 1000),
+    # at least as many rows as SMs, rows of up to 96 KB: 256-thread streaming CTAs
+    (160, 4097, 160, 3000), (200, 24576, 50, 24500), (160, 12001, 160, 11900)]
 
 
 @pytest.mark.parametrize("rows,cols,period,offset", CAUSAL)
