@@ -9,7 +9,8 @@ write of y; TopK: one read of x plus K*8 bytes of output) divided by the
 device time of the step, summed over all ranks' work, over the max rank time.
 
 Timing: CUDA events on the launching stream, W untimed warm-up steps, then K
-timed steps between barriers and synchronisations.  The softmax inputs are
+timed steps between barriers and synchronisations; inside them only the
+dominant kernel is bracketed by events (its duration gives `roofline`).  The softmax inputs are
 larger than L2; the TopK input (51 MB) rotates over enough copies to cover
 three times the L2 size, so no timed launch reads a cache-resident input.
 
@@ -18,10 +19,12 @@ buffers: host->device copy of every input and device->host copy of every
 output inside the timed region), `roofline` of the dominant kernel,
 `cpu_baseline` (the float64 oracle on the host cores on a bounded sample),
 `clocks` (nvidia-smi samples taken during the timed region),
-`per_workload` (each launch of the step, and after the step, in loops of
-their own, the other configurations -- 64x1024 fp32, causal 1048576x128,
-increasing 65536x4096 --, rows that are not whole 16-byte vectors (4096 x 50257
-fp32) and the ex2.approx-free kernel on the bf16 workload),
+`per_workload` (after the timed region, each kernel of the step in a loop
+of its own, with its share of the step from events recorded between the
+step's launches; then the other configurations -- 64x1024 fp32, causal
+1048576x128, increasing 65536x4096 --, rows that are not whole 16-byte
+vectors (4096 x 50257 fp32) and the ex2.approx-free kernel on the bf16
+workload, in loops of their own),
 `unfused_baselines` (three-pass safe softmax against the online kernel,
 softmax-then-TopK against the fused kernel), `stats_and_causal` (row
 statistics; causal mask applied in the kernel), `attention` (the tensor-core
@@ -222,6 +225,22 @@ def make_step_inputs(dev, st):
     return items, copies
 
 
+def step_attribution(st, items, stream, dev, steps):
+    """Mean device time of each launch of the step, from events recorded
+    between all launches (they add about 2 us each to the stream)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(items) + 1)]
+           for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for it in range(steps):
+        evs[it][0].record(stream)
+        for j, item in enumerate(items):
+            launch(st, item, it)
+            evs[it][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    return [sum(evs[it][j].elapsed_time(evs[it][j + 1]) for it in range(steps)) / steps
+            for j in range(len(items))]
+
+
 def launch(st, item, it):
     """Launch one item of step `it`.  Each TopK launch of the step reads its
     own copy of the input (copy (it * len(TOPK_KS) + j) mod copies), so none
@@ -252,8 +271,12 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     n_items = len(items)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_items + 1)]
-           for _ in range(args.steps)]
+    # Inside the timed region only the dominant kernel (the most bytes) is
+    # bracketed by events: an event recorded between two launches costs the
+    # stream about 2 us, which would weigh on the short TopK launches.
+    dom = max(range(n_items), key=lambda j: units[j][1])
+    dom_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     clocks = ClockSampler(local) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
@@ -263,10 +286,12 @@ def run_ours(args):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for it in range(args.steps):
-        evs[it][0].record(stream)
         for j, item in enumerate(items):
+            if j == dom:
+                dom_evs[it][0].record(stream)
             launch(st, item, it)
-            evs[it][j + 1].record(stream)
+            if j == dom:
+                dom_evs[it][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -276,9 +301,13 @@ def run_ours(args):
 
     from softmax_topk_gb300 import multi
     total_ms = multi.max_over_ranks(start.elapsed_time(end), device=dev)
-    per_item_ms = [sum(evs[it][j].elapsed_time(evs[it][j + 1]) for it in range(args.steps))
-                   / args.steps for j in range(n_items)]
+    dom_ms = sum(a.elapsed_time(b) for a, b in dom_evs) / args.steps
     ms_per_step = total_ms / args.steps
+    # after the timed region: each launch's share of the step (events between
+    # all launches, same inputs), and each kernel in a loop of its own
+    in_step_ms = step_attribution(st, items, stream, dev, args.steps)
+    own_ms = [_time_ms(lambda i, item=item: launch(st, item, i), dev, max(20, args.steps))
+              for item in items]
     step_bytes = sum(u[1] for u in units)
     value = multi.whole_job_rate(step_bytes, world, ms_per_step * 1e-3) / 1e9
 
@@ -296,14 +325,18 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     per = {}
-    for (label, b, rows), ms in zip(units, per_item_ms):
+    for j, (label, b, rows) in enumerate(units):
+        ms = own_ms[j]
         per[label] = {"ms": round(ms, 5), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
                       "rows_per_s": round(rows / (ms * 1e-3), 1),
                       "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
-                      "frac_of_8tbs_nominal": round(b / (ms * 1e-3) / 1e9 / 8000.0, 4)}
-    dom = max(range(n_items), key=lambda j: per_item_ms[j])
+                      "frac_of_8tbs_nominal": round(b / (ms * 1e-3) / 1e9 / 8000.0, 4),
+                      "timing": "own loop of back-to-back launches, inputs as in the step",
+                      "in_step_ms": round(in_step_ms[j], 5),
+                      "in_step_share": round(in_step_ms[j] / sum(in_step_ms), 4)}
+    per[units[dom][0]]["timed_region_ms"] = round(dom_ms, 5)
     dom_label, dom_bytes, _ = units[dom]
-    achieved = dom_bytes / (per_item_ms[dom] * 1e-3) / 1e9
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     kernel_name = kernel_of(st, dom_label)
     traffic = recorded_traffic(kernel_name)
     line = {
