@@ -537,6 +537,14 @@ __device__ __forceinline__ bool cta_wait_bounded(uint64_t* bar, uint32_t parity,
     return flag[which] != 0;
 }
 
+// Asks L2 to fetch [src, src + bytes) from memory ahead of its use, with an
+// eviction policy; nothing reaches this SM and nothing waits for it.  src
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
+                 :: "l"(src), "r"(bytes), "l"(policy) : "memory");
+}
+
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,
