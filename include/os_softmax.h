@@ -32,14 +32,15 @@
  *     softmax and its outputs are unspecified (NaN in practice).
  *   - Arithmetic: fp32 throughout (bf16 inputs widened exactly, fp32
  *     accumulation, bf16 outputs rounded to nearest even).  Per-element
- *     exponentials: the two-pass streaming kernel (every row longer than
- *     4096 16-byte vectors, and the three-pass baseline) uses the library's
- *     own FMA-pipe exponential for every output dtype (no ex2.approx:
- *     base-2 reduction, a degree-5 polynomial for fp32 results and a
- *     degree-3 one for bf16 results, 2^n added to the exponent field); the
- *     register, on-chip, statistics and TopK kernels use the SFU's 2^x
- *     (ex2.approx) of (x - m) log2 e, log2 e in two fp32 parts for fp32
- *     results.  A value
+ *     exponentials: the two-pass streaming kernel (AUTO's choice for rows
+ *     longer than 8192 fp32 / 4096 bf16 elements) and the three-pass
+ *     baseline use the library's own FMA-pipe exponential for fp32 results
+ *     (no ex2.approx: base-2 reduction, a degree-5 polynomial, 2^n added to
+ *     the exponent field), and for bf16 results too under
+ *     OS_PATH_STREAM_POLY (degree 2 for the normaliser, 3 for the outputs);
+ *     bf16 results on OS_PATH_STREAM and the register, on-chip, statistics
+ *     and TopK kernels use the SFU's 2^x (ex2.approx) of (x - m) log2 e,
+ *     log2 e in two fp32 parts for fp32 results.  A value
  *     that carries a whole row (a merge's rescale factor, a TopK output
  *     value) uses the library's accurate exponential (os_exp_f32).
  *   - Work runs on the device current at the call (cudaGetDevice); the
@@ -94,7 +95,7 @@ typedef enum {
                            ex2.approx anywhere in the kernel).  For fp32
                            results this is the STREAM kernel itself; for bf16
                            results it replaces the SFU's 2^x (STREAM's and
-                           AUTO's choice there, about 25 % faster on GB300)
+                           AUTO's choice there, about 20 % faster on GB300)
                            by degree-2 (normaliser) and degree-3 (outputs)
                            fits of 2^f; never chosen by AUTO */
 } os_path;
