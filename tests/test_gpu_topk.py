@@ -118,6 +118,44 @@ def test_many_rows_short(st):
     _run(st, _rand(5000, 40, seed=3), 16, "5000 x 40")
 
 
+MANY_ROWS = 640  # at least four CTAs of 256 threads per SM
+
+
+@pytest.mark.parametrize("cols", [1000, 8193, 32000, 50257, 65536, 65537])
+@pytest.mark.parametrize("K", [1, 8, 64])
+def test_many_row_batches(st, cols, K):
+    """Batches of at least as many rows as resident 256-thread CTAs run the
+    256-thread build (rows of up to 65536 columns, K <= 64); fused and plain,
+    with ties planted at each row's maximum in half the rows."""
+    rows = MANY_ROWS
+    plan = st.os_topk_plan(rows, cols, K)
+    assert plan["cluster"] == 1 and plan["threads"] == (256 if cols <= 65536 else 512), plan
+    x = _rand(rows, cols, seed=cols + K)
+    top = x.max(dim=1, keepdim=True).values
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cols * 7 + K)
+    pos = torch.randint(0, cols, (rows // 2, 5), generator=g, device="cuda")
+    x[: rows // 2].scatter_(1, pos, top[: rows // 2].expand(-1, 5))
+    _run(st, x, K, f"{rows}x{cols} K={K}")
+    _run_plain(st, x, K, f"plain {rows}x{cols} K={K}")
+
+
+@pytest.mark.parametrize("offset", [1, 3])
+def test_many_row_batches_misaligned(st, offset):
+    rows, cols, K = MANY_ROWS, 20011, 64
+    buf = torch.empty(rows * cols + 8, device="cuda")
+    x = buf[offset:offset + rows * cols].view(rows, cols)
+    x.copy_(_rand(rows, cols, seed=offset + 5))
+    assert st.os_topk_plan(rows, cols, K)["threads"] == 256
+    vals = torch.empty(rows, K, device="cuda")
+    idx = torch.empty(rows, K, dtype=torch.int32, device="cuda")
+    st.os_softmax_topk(x.data_ptr(), vals.data_ptr(), idx.data_ptr(), rows, cols, K,
+                       torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    rv, ri = oracle.topk(x.double().cpu().numpy(), K)
+    assert_topk_equal(vals.cpu().numpy(), idx.cpu().numpy(), rv, ri, f"{rows} rows offset {offset}")
+
+
 def test_values_equal_softmax_output(st):
     x = _rand(16, 32000, seed=11)
     vals, idx = st.softmax_topk(x, 64)
@@ -218,9 +256,10 @@ def _check_fused_and_plain(st, x, K, label):
 
 
 # (rows, cols): 320 rows run one CTA per row; 16 rows of 50257 split each row
-# over a cluster; 5000 and 7003 columns with more than 2048 zeros overflow the
-# candidate buffer, so the row takes the exact path
-@pytest.mark.parametrize("shape", [(320, 5000), (16, 50257), (7, 7003)])
+# over a cluster; 640 rows run CTAs of 256 threads for K <= 64; 5000 and 7003
+# columns with more than 2048 zeros overflow the candidate buffer, so the row
+# takes the exact path
+@pytest.mark.parametrize("shape", [(320, 5000), (16, 50257), (7, 7003), (640, 5000)])
 @pytest.mark.parametrize("K", [8, 64, 256])
 def test_exact_path_signed_zero_ties(st, shape, K):
     """More than 2048 candidates tied at zero, half of them -0.0: the exact
