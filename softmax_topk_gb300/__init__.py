@@ -286,13 +286,21 @@ def softmax_causal(x, period: int, offset: int = 0, out_dtype=None, out=None):
     return out
 
 
-def softmax_stats(x):
-    """(m, d, lse) fp32 [rows] each: row maximum, sum of e^(x - m), and m + ln d."""
+def softmax_stats(x, m=None, d=None, lse=None):
+    """(m, d, lse) fp32 [rows] each: row maximum, sum of e^(x - m), and m + ln d
+    (into the given tensors where passed)."""
     import torch
     if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D CUDA tensor")
     rows = x.shape[0]
-    m, d, lse = (torch.empty(rows, dtype=torch.float32, device=x.device) for _ in range(3))
+    outs = []
+    for t in (m, d, lse):
+        if t is None:
+            t = torch.empty(rows, dtype=torch.float32, device=x.device)
+        elif t.shape != (rows,) or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("m, d and lse must be contiguous float32 tensors of shape [rows]")
+        outs.append(t)
+    m, d, lse = outs
     with _OnDevice(x.device):
         os_softmax_stats(x.data_ptr(), m.data_ptr(), d.data_ptr(), lse.data_ptr(), rows,
                          x.shape[1], _dtype_code(x.dtype), _stream_handle(x))
