@@ -847,16 +847,19 @@ __device__ __forceinline__ void exp_scale_all(float* e, float2 scale) {
 // L2), marks its loads evict_first (last use) and writes y = e^(x - m) / d
 // with streaming stores.  The row's first NS chunks (the ones pass 1 read
 // longest ago, so the likeliest to have left L2) are also kept raw in shared
-// memory by the thread that loaded them, and pass 2 takes them from there.
+// memory by the thread that loaded them, and pass 2 takes them from there
+// (bf16 rows on 512-thread CTAs read them with evict_first, see KEPT_FIRST).
 // When pass 2 begins (it reads nothing from memory) the CTA asks L2 for the
 // start of its next row, so that the next pass 1 finds it there and memory
 // stays busy between the rows.
 // With one CTA per row there is no exchange between SMs at all: each row
 // costs one __syncthreads-level merge.
-// Every per-element exponential is the FMA-pipe form exp_biased_pair (no
-// ex2.approx): pass 1 sums a chunk's biased values and scales the sum once,
-// pass 2 multiplies each by the row's 2^-66 / d (one product per element
-// normalises and unbiases together).
+// Per-element exponentials (SFU = false): the FMA-pipe form exp_biased_pair
+// (no ex2.approx): pass 1 sums a chunk's biased values and scales the sum
+// once, pass 2 multiplies each by the row's 2^-66 / d (one product per
+// element normalises and unbiases together); bf16 -> bf16 folds the shift
+// into the rounding constant (exp_folded_pair).  SFU = true (bf16 results,
+// AUTO's choice): the SFU's 2^x against a running maximum.
 // Every slot wholly inside the row moves with one 128-bit load and store;
 // ALIGNED (rows start on 16-byte boundaries and are whole slots) drops the
 // per-row head and output-phase arithmetic.  Chunks lying wholly inside the
