@@ -2,8 +2,8 @@
 // pair.  Included by one translation unit per pair, which instantiates it.
 //
 // Families by row length, in 16-byte input vectors nv = ceil(cols / EPV);
-// AUTO takes WARP for nv <= 256, ONCHIP for nv <= 2048 fp32 / 512 bf16
-// vectors, STREAM beyond:
+// AUTO takes WARP for nv <= 256 fp32 / 128 bf16, ONCHIP for nv <= 2048 fp32
+// / 1024 bf16 vectors, STREAM beyond:
 //   WARP    nv <= 256: L = 1..32 lanes per row with 4 vectors per lane, or 32
 //           lanes with 8 vectors (rows of up to 1024 fp32 / 2048 bf16).
 //   ONCHIP  nv <= 16 x 512 x VPT (VPT = 32 elements per thread / EPV).
@@ -45,14 +45,19 @@ constexpr int64_t kStreamShortRowBytes = 96 * 1024;
 // vectors per thread per chunk: 8 fp32 or 4 bf16 (32 elements either way; measured best)
 template <typename TI> constexpr int stream_unroll() { return sizeof(TI) == 4 ? 8 : 4; }
 constexpr int kTmaMinCols = 8192;
-// AUTO sends rows longer than this many 16-byte vectors (8192 fp32, 4096
-// bf16 elements) to the two-pass streaming kernel: measured on GB300 (4096
-// rows) the register kernel wins up to there with CTAs of at most 256
-// threads (fp32 8192 columns: 5627 against 5481 GB/s; bf16 4096: 3587
-// against 2878), the streaming kernel beyond (fp32 8193: 4218 against 3194;
-// bf16 6000: 3902 against 3056; the bulk-copy ring kernel 3000-5070 GB/s on
-// 12000-32768 columns against the streaming kernel's 4245-6078).
-template <typename TI> constexpr int64_t auto_onchip_max_vectors() { return sizeof(TI) == 4 ? 2048 : 512; }
+// AUTO sends rows longer than this many 16-byte vectors (8192 elements of
+// either dtype) to the two-pass streaming kernel: measured on GB300 (1 GB
+// inputs) the register kernel wins up to there with CTAs of at most 256
+// threads (fp32 8192 columns: 7146 against 6413 GB/s; bf16 8192: 6704
+// against 6432; bf16 6000: 5585 against 5230), the streaming kernel beyond
+// (fp32 8193: 4689 against 3437 with a 512-thread CTA; bf16 8193: 4098
+// against 1593; the bulk-copy ring kernel 3780-5465 GB/s on fp32 rows of
+// 10000-16384 columns against the streaming kernel's 4497-6342).
+template <typename TI> constexpr int64_t auto_onchip_max_vectors() { return sizeof(TI) == 4 ? 2048 : 1024; }
+// AUTO's WARP family: rows of up to 256 fp32 / 128 bf16 vectors (1024
+// elements either way: 32 per thread); longer bf16 rows run the register
+// kernel with 128-thread CTAs (2048 columns: 4673 against 3340 GB/s).
+template <typename TI> constexpr int64_t auto_warp_max_vectors() { return sizeof(TI) == 4 ? 256 : 128; }
 // The bulk-copy ring kernel runs CTAs of 256 threads, two per SM, so one
 // CTA's reductions and exchange overlap the other's loads and arithmetic.
 // Elements per thread: 32 fp32 or 64 bf16, so a CTA's slice is 32 KB of input
@@ -191,7 +196,7 @@ struct SoftmaxFamily {
         const int64_t cta_cap = int64_t(kOnchipThreadsMax) * VPT;
         const bool onchip_ok = nv <= int64_t(onchip_cluster_limit(*dev)) * cta_cap;
         if (path == OS_PATH_AUTO)
-            path = warp_ok ? OS_PATH_WARP
+            path = nv <= auto_warp_max_vectors<TI>() ? OS_PATH_WARP
                  : (nv <= auto_onchip_max_vectors<TI>() && onchip_ok) ? OS_PATH_ONCHIP : OS_PATH_STREAM;
         os_plan q = {};
         q.path = path;

@@ -406,8 +406,11 @@ def test_plans_of_the_workloads(st):
     # AUTO's family boundaries and the streaming kernel's CTA size
     assert st.plan((4096, 8192), st.OS_F32)["path"] == st.OS_PATH_ONCHIP
     assert st.plan((4096, 8193), st.OS_F32)["path"] == st.OS_PATH_STREAM
-    assert st.plan((4096, 4096), st.OS_BF16)["path"] == st.OS_PATH_ONCHIP
-    assert st.plan((4096, 4097), st.OS_BF16)["path"] == st.OS_PATH_STREAM
+    assert st.plan((4096, 8192), st.OS_BF16)["path"] == st.OS_PATH_ONCHIP
+    assert st.plan((4096, 8193), st.OS_BF16)["path"] == st.OS_PATH_STREAM
+    assert st.plan((4096, 1024), st.OS_BF16)["path"] == st.OS_PATH_WARP
+    assert st.plan((4096, 1025), st.OS_BF16)["path"] == st.OS_PATH_ONCHIP
+    assert st.plan((4096, 1024), st.OS_F32)["path"] == st.OS_PATH_WARP
     assert st.plan((4096, 24576), st.OS_F32)["threads"] == 256
     assert st.plan((4096, 24577), st.OS_F32)["threads"] == 512
     assert st.plan((4096, 49152), st.OS_BF16)["threads"] == 256
