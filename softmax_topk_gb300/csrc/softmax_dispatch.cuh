@@ -80,7 +80,14 @@ struct SoftmaxFamily {
     // 16-byte blocks they cover (see warp_rows_kernel)
     template <bool PEEL>
     static WarpKernel warp_as(int lanes, int vpt) {
-        if (vpt == 8) return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads, PEEL>;
+        if (vpt == 8) {
+            switch (lanes) {
+                case 4: return warp_rows_kernel<TI, TO, 4, 8, kWarpThreads, PEEL>;
+                case 8: return warp_rows_kernel<TI, TO, 8, 8, kWarpThreads, PEEL>;
+                case 16: return warp_rows_kernel<TI, TO, 16, 8, kWarpThreads, PEEL>;
+                default: return warp_rows_kernel<TI, TO, 32, 8, kWarpThreads, PEEL>;
+            }
+        }
         switch (lanes) {
             case 1: return warp_rows_kernel<TI, TO, 1, 4, kWarpThreads, PEEL>;
             case 2: return warp_rows_kernel<TI, TO, 2, 4, kWarpThreads, PEEL>;
@@ -203,8 +210,12 @@ struct SoftmaxFamily {
         switch (path) {
             case OS_PATH_WARP: {
                 if (!warp_ok) return OS_ERR_PATH;
-                q.vectors_per_thread = nv <= 128 ? 4 : 8;
-                q.lanes_per_row = q.vectors_per_thread == 8 ? 32 : pow2_at_least(ceil_div(nv, 4));
+                // 32 elements per thread where the row allows it: fp32 rows of
+                // 32-256 vectors take 8 vectors per thread (measured on GB300,
+                // 1048576x128: 6460 against 6060 GB/s with 4), bf16 rows 4
+                // (8 measured far slower: 64 values per thread)
+                q.vectors_per_thread = nv > 128 || (sizeof(TI) == 4 && nv >= 32) ? 8 : 4;
+                q.lanes_per_row = pow2_at_least(ceil_div(nv, q.vectors_per_thread));
                 q.threads = kWarpThreads;
                 q.cluster = 1;
                 const int64_t rows_per_cta = kWarpThreads / q.lanes_per_row;

@@ -400,7 +400,7 @@ def test_plans_of_the_workloads(st):
     p = st.plan((8192, 128256), st.OS_BF16, path="onchip")
     assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 8 and p["stages"] == 3
     p = st.plan((1048576, 128), st.OS_F32)
-    assert p["path"] == st.OS_PATH_WARP and p["lanes_per_row"] == 8
+    assert p["path"] == st.OS_PATH_WARP and p["lanes_per_row"] == 4 and p["vectors_per_thread"] == 8
     p = st.plan((65536, 4096), st.OS_F32)
     assert p["path"] == st.OS_PATH_ONCHIP and p["cluster"] == 1 and p["threads"] == 128
     # AUTO's family boundaries and the streaming kernel's CTA size
