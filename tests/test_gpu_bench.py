@@ -40,6 +40,12 @@ def test_bench_line_keeps_the_contract():
                 "increasing_65536x4096_f32", "softmax_4096x50257_f32",
                 "softmax_8192x128256_bf16_stream_poly"):
         assert pw[key]["gbs"] > 0 and pw[key]["ms"] > 0, key
+    step = ("softmax_4096x32000_f32", "softmax_8192x128256_bf16", "topk_256x50257_f32_K8",
+            "topk_256x50257_f32_K64")
+    for key in step:  # own-loop times plus the in-step attribution
+        assert pw[key]["in_step_ms"] > 0 and pw[key]["timing"], key
+    assert abs(sum(pw[key]["in_step_share"] for key in step) - 1.0) < 1e-3
+    assert pw[r["workload"]]["timed_region_ms"] > 0  # the roofline kernel, timed in the timed region
     assert e["link"]["h2d_gbs"] > 0 and e["link"]["d2h_gbs"] > 0 and e["frac_of_link_bound"] > 0
     assert d["unfused_baselines"]["softmax_4096x32000_f32"]["safe_over_online"] > 0
     assert d["stats_and_causal"]["causal_1048576x128_f32"]["read_over_mask"] > 0
